@@ -1,0 +1,168 @@
+"""CPU oracle for batched top-k / top-p truncation and sampling.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library (``top_selection_stats_gb300``) and never imports it.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision after the fp32
+temperature division); this module only marshals numpy arrays.
+
+Parity status of each function (what pins it is listed in the tests):
+  * orc_select_core  -- pinned: worked examples of the KB note (section 02-03),
+                        lecture exercises 7 and 8, O(V^2) brute force.
+  * orc_batch        -- pinned through orc_select_core plus decoder and
+                        front-end tests (greedy ties, masks, status codes).
+  * orc_philox4x32_10 -- pinned against cuRAND's host Philox4x32-10 generator
+                        where libcurand is present, and by uniformity tests.
+  * orc_row_stats    -- pinned against numpy on the same inputs.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+ORC_OK, ORC_EMPTY, ORC_NONFINITE, ORC_INVALID = 0, 1, 2, 3
+ORC_F32, ORC_BF16, ORC_F16 = 0, 1, 2
+FLAG_TOPP_BOUNDARY, FLAG_CDF_BOUNDARY = 1, 2
+
+_lib = None
+
+
+def load(path):
+    """Load an oracle shared library from ``path`` and declare its signatures."""
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    L.orc_bf16_to_f32.restype = ctypes.c_float
+    L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_f16_to_f32.restype = ctypes.c_float
+    L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_philox4x32_10.restype = None
+    L.orc_philox4x32_10.argtypes = [P, P, P]
+    L.orc_uniform.restype = ctypes.c_double
+    L.orc_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+    L.orc_select_core.restype = ctypes.c_int
+    L.orc_select_core.argtypes = [ctypes.c_int, P, P, P, ctypes.c_int32, ctypes.c_double,
+                                  ctypes.c_double, P, P, P, P, P, P]
+    L.orc_batch.restype = ctypes.c_int
+    L.orc_batch.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, P,
+                            P, P, P, P, P, ctypes.c_int, P, P, P, P, P, P, P, ctypes.c_int]
+    L.orc_row_stats.restype = ctypes.c_int
+    L.orc_row_stats.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
+    return L
+
+
+def lib():
+    """The oracle library, built from source on first use."""
+    global _lib
+    if _lib is None:
+        _lib = load(_build.build())
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def philox4x32_10(ctr, key, L=None):
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    (L or lib()).orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed, offset, L=None):
+    return (L or lib()).orc_uniform(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1))
+
+
+def select_core(x, z, legal, top_k, top_p, u, L=None):
+    """Core selection on double arrays (used by the pins)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    legal = np.ascontiguousarray(legal, dtype=np.uint8)
+    n = x.shape[0]
+    kept = np.zeros(n, dtype=np.uint8)
+    prob = np.zeros(n, dtype=np.float64)
+    tok = np.zeros(1, dtype=np.int32)
+    ntk = np.zeros(1, dtype=np.int32)
+    nkp = np.zeros(1, dtype=np.int32)
+    fl = np.zeros(1, dtype=np.int32)
+    st = (L or lib()).orc_select_core(n, _ptr(x), _ptr(z), _ptr(legal), int(top_k),
+                                      float(top_p), float(u), _ptr(kept), _ptr(prob),
+                                      _ptr(tok), _ptr(ntk), _ptr(nkp), _ptr(fl))
+    return dict(status=st, kept=kept.astype(bool), prob=prob, token=int(tok[0]),
+                n_topk=int(ntk[0]), n_kept=int(nkp[0]), flags=int(fl[0]))
+
+
+_DT = {"f32": ORC_F32, "bf16": ORC_BF16, "f16": ORC_F16}
+
+
+def run_batch(logits_bits, dtype, V, temperature=None, top_k=None, top_p=None, seed=None,
+              offset=None, bitmask=None, mode="sample", want_mask=True, want_probs=False,
+              n_threads=1, ld=None, L=None):
+    """Run the oracle over a batch.
+
+    logits_bits: numpy array [B, ld] -- float32 for "f32", uint16 bit patterns
+    for "bf16" / "f16".  bitmask: uint32 [B, ceil(V/32)] or None.
+    Returns a dict of numpy arrays.
+    """
+    dt = _DT[dtype]
+    arr = np.ascontiguousarray(logits_bits)
+    if dt == ORC_F32:
+        assert arr.dtype == np.float32
+    else:
+        assert arr.dtype == np.uint16
+    B = arr.shape[0]
+    ld = arr.shape[1] if ld is None else ld
+    W = (V + 31) // 32
+    m = 1 if mode == "argmax" else 0
+
+    def arrf(a, dtp, default):
+        if a is None:
+            return np.full(B, default, dtype=dtp)
+        return np.ascontiguousarray(a, dtype=dtp)
+
+    t = arrf(temperature, np.float32, 1.0)
+    k = arrf(top_k, np.int32, V)
+    p = arrf(top_p, np.float32, 1.0)
+    s = arrf(seed, np.uint64, 0)
+    o = arrf(offset, np.uint64, 0)
+    bm = None if bitmask is None else np.ascontiguousarray(bitmask, dtype=np.uint32)
+    status = np.zeros(B, dtype=np.int32)
+    token = np.zeros(B, dtype=np.int32)
+    count = np.zeros(B, dtype=np.int32)
+    flags = np.zeros(B, dtype=np.int32)
+    u = np.zeros(B, dtype=np.float64)
+    kmask = np.zeros((B, W), dtype=np.uint32) if want_mask else None
+    probs = np.zeros((B, V), dtype=np.float64) if want_probs else None
+    (L or lib()).orc_batch(_ptr(arr), dt, B, V, ld, _ptr(bm), _ptr(t), _ptr(k), _ptr(p),
+                           _ptr(s), _ptr(o), m, _ptr(status), _ptr(token), _ptr(count),
+                           _ptr(kmask), _ptr(probs), _ptr(flags), _ptr(u), int(n_threads))
+    return dict(status=status, token=token, kept_count=count, kept_mask=kmask, probs=probs,
+                flags=flags, u=u)
+
+
+def row_stats(logits_row_bits, dtype, V, temperature=1.0, mask_row=None):
+    arr = np.ascontiguousarray(logits_row_bits)
+    out = np.zeros(8, dtype=np.float64)
+    mr = None if mask_row is None else np.ascontiguousarray(mask_row, dtype=np.uint32)
+    lib().orc_row_stats(_ptr(arr), _DT[dtype], V, _ptr(mr), float(temperature), _ptr(out))
+    return dict(max=out[0], argmax=int(out[1]), n_legal=int(out[2]), mean=out[3], std=out[4],
+                logsumexp=out[5], nonfinite=bool(out[6]))
+
+
+def bf16_to_f32(bits):
+    return lib().orc_bf16_to_f32(int(bits))
+
+
+def f16_to_f32(bits):
+    return lib().orc_f16_to_f32(int(bits))
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1

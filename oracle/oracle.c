@@ -1,0 +1,389 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for batched top-k / top-p truncation and
+ * sampling.  TEST INFRASTRUCTURE ONLY: the product path never links it.
+ *
+ * It writes out the definitions directly: a full sort of every row by
+ * (logit descending, id ascending), a double-precision softmax, prefix cuts
+ * for top-k and top-p, and a linear inverse-CDF scan in token-id order.  No
+ * blocking, truncation heuristic, pivot search or fusion: those belong to the
+ * fast path this oracle is used to check.
+ *
+ * Citations are to the pages' titles and sections:
+ *   [KB]   AI Infra KB note M012 (token selection after the LM head)
+ *   [BLOG] "Sampling system design: from logits to controllable generation"
+ *          (mini vLLM series)
+ *   [QR]   "Qrita: High-performance Top-k and Top-p using Pivot-based
+ *          Truncation and Selection" (paper notes)
+ *   [LEC]  CMU 11-868 lecture 9 notes, "Decoding: Sampling, Beam Search and
+ *          Speculative Decoding"
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------------- */
+/* Input decoding.  Both conversions are exact; written from the IEEE 754  */
+/* binary16 layout and the bfloat16 definition (upper half of a binary32). */
+/* ---------------------------------------------------------------------- */
+
+float orc_bf16_to_f32(uint16_t h) {
+  uint32_t bits = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return f;
+}
+
+float orc_f16_to_f32(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int expo = (h >> 10) & 0x1f;
+  int mant = h & 0x3ff;
+  double v;
+  if (expo == 0) {
+    v = ldexp((double)mant, -24); /* zero or subnormal: mant * 2^-24 */
+  } else if (expo == 31) {
+    v = mant ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(1024 + mant), expo - 25); /* (1 + mant/1024) * 2^(e-15) */
+  }
+  return (float)(sign ? -v : v);
+}
+
+static float load_logit(const void* row, int dtype, int i) {
+  switch (dtype) {
+    case ORC_F32: return ((const float*)row)[i];
+    case ORC_BF16: return orc_bf16_to_f32(((const uint16_t*)row)[i]);
+    default: return orc_f16_to_f32(((const uint16_t*)row)[i]);
+  }
+}
+
+static int mask_allows(const uint32_t* mask_row, int i) {
+  if (!mask_row) return 1;
+  return (int)((mask_row[i >> 5] >> (i & 31)) & 1u);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Philox4x32-10, from the round function and key schedule published by    */
+/* Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as     */
+/* 1, 2, 3" (SC'11).  [KB] section 06 asks for explicit (seed, offset)     */
+/* random state; the counter/key layout below is this build's choice.      */
+/* ---------------------------------------------------------------------- */
+
+#define ORC_PHILOX_M0 0xD2511F53u
+#define ORC_PHILOX_M1 0xCD9E8D57u
+#define ORC_PHILOX_W0 0x9E3779B9u
+#define ORC_PHILOX_W1 0xBB67AE85u
+
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+  uint32_t k[2] = {key_in[0], key_in[1]};
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k[0] += ORC_PHILOX_W0;
+      k[1] += ORC_PHILOX_W1;
+    }
+    uint64_t p0 = (uint64_t)ORC_PHILOX_M0 * (uint64_t)c[0];
+    uint64_t p1 = (uint64_t)ORC_PHILOX_M1 * (uint64_t)c[2];
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c[1] ^ k[0];
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c[3] ^ k[1];
+    uint32_t n3 = lo0;
+    c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+  }
+  out[0] = c[0]; out[1] = c[1]; out[2] = c[2]; out[3] = c[3];
+}
+
+double orc_uniform(uint64_t seed, uint64_t offset) {
+  uint32_t ctr[4] = {(uint32_t)offset, (uint32_t)(offset >> 32), 0u, 0u};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  return (double)(out[0] >> 8) * (1.0 / 16777216.0);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Core selection                                                          */
+/* ---------------------------------------------------------------------- */
+
+typedef struct {
+  double x;
+  int id;
+} orc_item;
+
+/* (x descending, id ascending): a total order, so any sort of the ids by
+ * this key equals a stable sort by x alone.  Ties keep the earliest ids
+ * ([QR] key design 3). */
+static int rank_cmp(const void* a, const void* b) {
+  const orc_item* p = (const orc_item*)a;
+  const orc_item* q = (const orc_item*)b;
+  if (p->x > q->x) return -1;
+  if (p->x < q->x) return 1;
+  return (p->id < q->id) ? -1 : (p->id > q->id);
+}
+
+static int id_cmp(const void* a, const void* b) {
+  int p = *(const int*)a, q = *(const int*)b;
+  return (p > q) - (p < q);
+}
+
+int orc_select_core(int n, const double* x, const double* z, const unsigned char* legal,
+                    int32_t top_k, double top_p, double u,
+                    unsigned char* kept, double* prob, int32_t* token,
+                    int32_t* n_topk, int32_t* n_kept, int32_t* flags) {
+  if (kept) memset(kept, 0, (size_t)n);
+  if (prob) for (int i = 0; i < n; ++i) prob[i] = 0.0;
+  if (token) *token = -1;
+  if (n_topk) *n_topk = 0;
+  if (n_kept) *n_kept = 0;
+  if (flags) *flags = 0;
+
+  /* Legal set L: [KB] section 05 sets illegal logits to -inf before the
+   * draw; the front end folds that into legal[]. */
+  int nl = 0;
+  for (int i = 0; i < n; ++i) nl += legal[i] ? 1 : 0;
+  if (nl == 0) return ORC_EMPTY; /* [KB] section 03: an empty set is an error */
+
+  orc_item* order = (orc_item*)malloc(sizeof(orc_item) * (size_t)nl);
+  double* w = (double*)malloc(sizeof(double) * (size_t)n);
+  int* sp = (int*)malloc(sizeof(int) * (size_t)nl);
+  int j = 0;
+  for (int i = 0; i < n; ++i)
+    if (legal[i]) { order[j].x = x[i]; order[j].id = i; ++j; }
+
+  /* Rank L by (x desc, id asc). */
+  qsort(order, (size_t)nl, sizeof(orc_item), rank_cmp);
+
+  /* Softmax over L in double ([LEC] 3.3: temperature divides the logits,
+   * then normalise). */
+  double m = -INFINITY;
+  for (int i = 0; i < n; ++i)
+    if (legal[i] && z[i] > m) m = z[i];
+  double total = 0.0;
+  for (int i = 0; i < n; ++i) {
+    w[i] = legal[i] ? exp(z[i] - m) : 0.0;
+    total += w[i];
+  }
+
+  /* Top-k: keep the first K of the rank order and renormalise ([KB] 02,
+   * [LEC] 3.3).  K = min(top_k, |L|). */
+  int K = top_k < nl ? top_k : nl;
+  double mass_k = 0.0;
+  for (int r = 0; r < K; ++r) mass_k += w[order[r].id] / total;
+
+  /* Top-p: the shortest prefix of the top-k order whose renormalised mass
+   * reaches p (">=": the worked answer to exercise 7 of [LEC] keeps the prefix
+   * whose mass equals p).  If rounding leaves every prefix short, keep all K. */
+  int nstar = K;
+  double cum_at = 0.0, cum_before = 0.0;
+  if (top_p < 1.0) {
+    double cum = 0.0;
+    for (int r = 0; r < K; ++r) {
+      double q = (w[order[r].id] / total) / mass_k;
+      double prev = cum;
+      cum += q;
+      if (cum >= top_p) { nstar = r + 1; cum_at = cum; cum_before = prev; break; }
+    }
+    if (flags) {
+      if (fabs(cum_at - top_p) <= 1e-5 || (nstar > 1 && fabs(top_p - cum_before) <= 1e-5))
+        *flags |= ORC_FLAG_TOPP_BOUNDARY;
+    }
+  }
+
+  /* Final renormalisation over S_p. */
+  double mass_p = 0.0;
+  for (int r = 0; r < nstar; ++r) mass_p += (w[order[r].id] / total) / mass_k;
+
+  for (int r = 0; r < nstar; ++r) {
+    int id = order[r].id;
+    if (kept) kept[id] = 1;
+    if (prob) prob[id] = ((w[id] / total) / mass_k) / mass_p;
+    sp[r] = id;
+  }
+
+  /* Inverse-CDF draw in token-id order ([KB] section 02 figure note): the
+   * token is the first id whose cumulative probability exceeds u; if
+   * rounding leaves none, the last kept id. */
+  qsort(sp, (size_t)nstar, sizeof(int), id_cmp);
+  double cum = 0.0, dmin = INFINITY;
+  int tok = sp[nstar - 1];
+  int found = 0;
+  for (int r = 0; r < nstar; ++r) {
+    int id = sp[r];
+    cum += ((w[id] / total) / mass_k) / mass_p;
+    double d = fabs(cum - u);
+    if (d < dmin) dmin = d;
+    if (!found && cum > u) { tok = id; found = 1; }
+  }
+  if (flags && dmin <= 1e-6) *flags |= ORC_FLAG_CDF_BOUNDARY;
+
+  if (token) *token = tok;
+  if (n_topk) *n_topk = K;
+  if (n_kept) *n_kept = nstar;
+  free(order);
+  free(w);
+  free(sp);
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Row front end: decode, validate, legal set, greedy path, fp32 scaling.  */
+/* ---------------------------------------------------------------------- */
+
+static int row_params_valid(float t, int32_t k, float p) {
+  /* [BLOG] parameter validation: reject negative temperature, top_p > 1 and
+   * non-positive top_k (the build's reading: top_k < 1 is invalid). */
+  if (isnan(t) || t < 0.0f) return 0;
+  if (k < 1) return 0;
+  if (isnan(p) || !(p > 0.0f) || p > 1.0f) return 0;
+  return 1;
+}
+
+static int oracle_row(const void* row, int dtype, int V, const uint32_t* mask_row,
+                      float t, int32_t k, float p, uint64_t seed, uint64_t offset, int mode,
+                      int32_t* token, int32_t* kept_count, uint32_t* kept_mask_row,
+                      double* probs_row, int32_t* flags, double* u_out) {
+  int W = (V + 31) / 32;
+  *token = -1;
+  *kept_count = 0;
+  *flags = 0;
+  if (kept_mask_row) memset(kept_mask_row, 0, sizeof(uint32_t) * (size_t)W);
+  if (probs_row) for (int i = 0; i < V; ++i) probs_row[i] = 0.0;
+  double u = orc_uniform(seed, offset);
+  if (u_out) *u_out = u;
+
+  if (mode == 1) {
+    t = 0.0f; k = 1; p = 1.0f; /* argmax entry point: every row greedy */
+  }
+  if (!row_params_valid(t, k, p)) return ORC_INVALID;
+  if (k > V) k = V;
+
+  float* xs = (float*)malloc(sizeof(float) * (size_t)V);
+  unsigned char* legal = (unsigned char*)malloc((size_t)V);
+  int nonfinite = 0, nl = 0;
+  for (int i = 0; i < V; ++i) {
+    xs[i] = load_logit(row, dtype, i);
+    legal[i] = (unsigned char)(mask_allows(mask_row, i) && !(isinf(xs[i]) && xs[i] < 0));
+    if (legal[i]) {
+      ++nl;
+      if (isnan(xs[i]) || isinf(xs[i])) nonfinite = 1; /* [KB] 07: explicit error */
+    }
+  }
+  int status = ORC_OK;
+  if (nonfinite) status = ORC_NONFINITE;
+  else if (nl == 0) status = ORC_EMPTY;
+  else if (t == 0.0f) {
+    /* Greedy is a separate argmax path ([KB] 02, [BLOG]); ties go to the
+     * earlier vocabulary id ([LEC] answer 1). */
+    int best = -1;
+    for (int i = 0; i < V; ++i)
+      if (legal[i] && (best < 0 || xs[i] > xs[best])) best = i;
+    *token = best;
+    *kept_count = 1;
+    if (kept_mask_row) kept_mask_row[best >> 5] |= 1u << (best & 31);
+    if (probs_row) probs_row[best] = 1.0;
+  } else {
+    double* xd = (double*)malloc(sizeof(double) * (size_t)V);
+    double* zd = (double*)malloc(sizeof(double) * (size_t)V);
+    unsigned char* kept = (unsigned char*)malloc((size_t)V);
+    for (int i = 0; i < V; ++i) {
+      xd[i] = legal[i] ? (double)xs[i] : 0.0;
+      /* z = fl32(x / T): correctly rounded binary32 division. */
+      float zf = legal[i] ? xs[i] / t : 0.0f;
+      zd[i] = (double)zf;
+    }
+    int32_t tok, ntk, nkp, fl;
+    status = orc_select_core(V, xd, zd, legal, k, (double)p, u, kept, probs_row, &tok, &ntk,
+                             &nkp, &fl);
+    if (status == ORC_OK) {
+      *token = tok;
+      *kept_count = nkp;
+      *flags = fl;
+      if (kept_mask_row)
+        for (int i = 0; i < V; ++i)
+          if (kept[i]) kept_mask_row[i >> 5] |= 1u << (i & 31);
+    }
+    free(xd);
+    free(zd);
+    free(kept);
+  }
+  if (status != ORC_OK) {
+    *token = -1;
+    *kept_count = 0;
+    if (kept_mask_row) memset(kept_mask_row, 0, sizeof(uint32_t) * (size_t)W);
+    if (probs_row) for (int i = 0; i < V; ++i) probs_row[i] = 0.0;
+  }
+  free(xs);
+  free(legal);
+  return status;
+}
+
+int orc_batch(const void* logits, int dtype, int B, int V, int64_t ld,
+              const uint32_t* bitmask,
+              const float* temperature, const int32_t* top_k, const float* top_p,
+              const uint64_t* seed, const uint64_t* offset, int mode,
+              int32_t* status, int32_t* token, int32_t* kept_count,
+              uint32_t* kept_mask, double* probs, int32_t* flags, double* u_out,
+              int n_threads) {
+  int W = (V + 31) / 32;
+  size_t es = (dtype == ORC_F32) ? 4 : 2;
+  if (n_threads < 1) n_threads = 1;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+#endif
+  for (int r = 0; r < B; ++r) {
+    const char* row = (const char*)logits + (size_t)r * (size_t)ld * es;
+    const uint32_t* mrow = bitmask ? bitmask + (size_t)r * (size_t)W : NULL;
+    status[r] = oracle_row(row, dtype, V, mrow, mode == 1 ? 0.0f : temperature[r],
+                           mode == 1 ? 1 : top_k[r], mode == 1 ? 1.0f : top_p[r],
+                           seed ? seed[r] : 0, offset ? offset[r] : 0, mode,
+                           &token[r], &kept_count[r],
+                           kept_mask ? kept_mask + (size_t)r * (size_t)W : NULL,
+                           probs ? probs + (size_t)r * (size_t)V : NULL,
+                           &flags[r], u_out ? &u_out[r] : NULL);
+  }
+  return 0;
+}
+
+int orc_row_stats(const void* row, int dtype, int V, const uint32_t* mask_row,
+                  float t, double out[8]) {
+  double mx = -INFINITY, s = 0.0, s2 = 0.0;
+  int arg = -1, n = 0, nonfinite = 0;
+  for (int i = 0; i < V; ++i) {
+    float xf = load_logit(row, dtype, i);
+    if (!mask_allows(mask_row, i) || (isinf(xf) && xf < 0)) continue;
+    if (isnan(xf) || isinf(xf)) { nonfinite = 1; continue; }
+    ++n;
+    if (xf > mx) { mx = xf; arg = i; }
+    s += xf;
+    s2 += (double)xf * (double)xf;
+  }
+  double mean = n ? s / n : 0.0;
+  double var = n ? s2 / n - mean * mean : 0.0;
+  double lse = -INFINITY;
+  if (n && t > 0.0f) {
+    double m = (double)((float)mx / t), acc = 0.0;
+    for (int i = 0; i < V; ++i) {
+      float xf = load_logit(row, dtype, i);
+      if (!mask_allows(mask_row, i) || isnan(xf) || isinf(xf)) continue;
+      float zf = xf / t;
+      acc += exp((double)zf - m);
+    }
+    lse = m + log(acc);
+  }
+  out[0] = mx;
+  out[1] = arg;
+  out[2] = n;
+  out[3] = mean;
+  out[4] = var > 0 ? sqrt(var) : 0.0;
+  out[5] = lse;
+  out[6] = nonfinite;
+  out[7] = 0.0;
+  return 0;
+}

@@ -1,0 +1,90 @@
+/*
+ * oracle.h -- plain CPU oracle for batched top-k / top-p truncation and sampling.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this code: only tests/, the package's smoke check and the CPU-baseline
+ * leg of bench.py use it.  It shares no code, header or constant with the CUDA
+ * library; it carries its own status codes, its own fp16/bf16 decoders and its
+ * own Philox4x32-10.
+ *
+ * What it computes (the contract of "AI Infra KB M012", sections 02-03, and of
+ * the CMU 11-868 lecture 9 notes, section 3.3), per row:
+ *   temperature (0 = separate greedy argmax path) -> legal-token mask ->
+ *   top-k with renormalisation -> top-p as the shortest prefix of descending
+ *   probability whose mass reaches p -> renormalise -> inverse-CDF draw in
+ *   token-id order.
+ * Ranking is by (logit descending, token id ascending): ties keep the earliest
+ * ids (Qrita paper notes, key design 3).  Everything after the fp32 scaling
+ * z = fl32(x / temperature) is done in double.
+ */
+#ifndef TSS_ORACLE_H
+#define TSS_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_OK = 0, ORC_EMPTY = 1, ORC_NONFINITE = 2, ORC_INVALID = 3 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F16 = 2 };
+
+/* flags[] bits */
+enum { ORC_FLAG_TOPP_BOUNDARY = 1, ORC_FLAG_CDF_BOUNDARY = 2 };
+
+float orc_bf16_to_f32(uint16_t h);
+float orc_f16_to_f32(uint16_t h);
+
+/* Philox4x32-10 block function (Salmon, Moraes, Dror, Shaw, SC'11). */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+/* u in [0,1) for a row: key = (lo32 seed, hi32 seed), counter = (lo32 off,
+ * hi32 off, 0, 0); u = (word0 >> 8) * 2^-24. */
+double orc_uniform(uint64_t seed, uint64_t offset);
+
+/*
+ * Core selection on one row given in double precision.
+ *   n       : vocabulary size
+ *   x       : value used for ranking (the fp32 logit, as a double)
+ *   z       : value used for the softmax (fl32(x / T), as a double)
+ *   legal   : 1 = candidate (mask allows it and x != -inf), 0 = excluded
+ *   top_k   : already validated, >= 1 (clamped to n inside)
+ *   top_p   : already validated, in (0, 1]
+ *   u       : uniform draw in [0, 1)
+ * Outputs (all nullable): kept[n] (1 = in the final kept set), prob[n]
+ * (final renormalised probability, 0 outside the kept set), token, counts,
+ * boundary flags.  Returns ORC_OK or ORC_EMPTY.
+ */
+int orc_select_core(int n, const double* x, const double* z, const unsigned char* legal,
+                    int32_t top_k, double top_p, double u,
+                    unsigned char* kept, double* prob, int32_t* token,
+                    int32_t* n_topk, int32_t* n_kept, int32_t* flags);
+
+/*
+ * Whole batch.  logits is [B][ld] of dtype; bitmask is [B][ceil(V/32)] or
+ * NULL (bit j%32 of word j/32, 1 = allowed).  Per-row parameter arrays have
+ * length B.  mode: 0 = sample, 1 = argmax only (every row greedy).
+ * Outputs: status, token (-1 on error rows), kept_count, kept_mask
+ * [B][ceil(V/32)] (nullable), probs [B][V] (nullable), flags, u (nullable).
+ * Rows are independent; n_threads > 1 runs them in parallel.
+ */
+int orc_batch(const void* logits, int dtype, int B, int V, int64_t ld,
+              const uint32_t* bitmask,
+              const float* temperature, const int32_t* top_k, const float* top_p,
+              const uint64_t* seed, const uint64_t* offset, int mode,
+              int32_t* status, int32_t* token, int32_t* kept_count,
+              uint32_t* kept_mask, double* probs, int32_t* flags, double* u_out,
+              int n_threads);
+
+/*
+ * Row statistics over legal finite logits: max and its smallest id, count,
+ * mean and standard deviation of x, logsumexp of z = fl32(x / T) (T > 0),
+ * and whether a NaN / +inf sits in a legal slot.
+ * out[8] = {max, argmax, n_legal, mean, std, logsumexp, nonfinite, 0}.
+ */
+int orc_row_stats(const void* logits_row, int dtype, int V, const uint32_t* mask_row,
+                  float temperature, double out[8]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

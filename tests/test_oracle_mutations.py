@@ -1,0 +1,79 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins catch
+each one.  The mutants are built from a temporary copy of oracle.c on the
+CPU; the committed oracle is never modified."""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+
+# (name, original text, replacement)
+MUTATIONS = [
+    ("top-p uses > instead of >=", "if (cum >= top_p)", "if (cum > top_p)"),
+    ("ties keep the latest ids", "return (p->id < q->id) ? -1 : (p->id > q->id);",
+     "return (p->id > q->id) ? -1 : (p->id < q->id);"),
+    ("top-p before top-k (mass over all of L)", "for (int r = 0; r < K; ++r) mass_k +=",
+     "for (int r = 0; r < nl; ++r) mass_k +="),
+    ("temperature dropped", "w[i] = legal[i] ? exp(z[i] - m) : 0.0;",
+     "w[i] = legal[i] ? exp(x[i] - m) : 0.0;"),
+    ("draw in rank order instead of id order", "qsort(sp, (size_t)nstar, sizeof(int), id_cmp);",
+     ";"),
+    ("greedy tie keeps the last id", "if (legal[i] && (best < 0 || xs[i] > xs[best])) best = i;",
+     "if (legal[i] && (best < 0 || xs[i] >= xs[best])) best = i;"),
+    ("final renormalisation dropped", "if (prob) prob[id] = ((w[id] / total) / mass_k) / mass_p;",
+     "if (prob) prob[id] = ((w[id] / total) / mass_k);"),
+    ("mask bit order reversed", "return (int)((mask_row[i >> 5] >> (i & 31)) & 1u);",
+     "return (int)((mask_row[i >> 5] >> (31 - (i & 31))) & 1u);"),
+    ("fp16 exponent bias off by one", "v = ldexp((double)(1024 + mant), expo - 25);",
+     "v = ldexp((double)(1024 + mant), expo - 24);"),
+    ("Philox multipliers swapped", "uint64_t p0 = (uint64_t)ORC_PHILOX_M0 * (uint64_t)c[0];",
+     "uint64_t p0 = (uint64_t)ORC_PHILOX_M1 * (uint64_t)c[0];"),
+    ("Philox key schedule constant wrong", "k[1] += ORC_PHILOX_W1;", "k[1] += ORC_PHILOX_W0;"),
+    ("u uses 23 bits", "return (double)(out[0] >> 8) * (1.0 / 16777216.0);",
+     "return (double)(out[0] >> 9) * (1.0 / 16777216.0);"),
+    ("-inf counted as legal", "legal[i] = (unsigned char)(mask_allows(mask_row, i) && !(isinf(xs[i]) && xs[i] < 0));",
+     "legal[i] = (unsigned char)(mask_allows(mask_row, i));"),
+    ("K clamped to top_k - 1", "int K = top_k < nl ? top_k : nl;",
+     "int K = top_k < nl ? (top_k > 1 ? top_k - 1 : 1) : nl;"),
+]
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    d = tempfile.mkdtemp(prefix="oracle_mut_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(workdir, name, old, new):
+    src = open(os.path.join(SRC, "oracle.c")).read()
+    assert src.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    tag = str(abs(hash(name)))
+    d = os.path.join(workdir, tag)
+    os.makedirs(d, exist_ok=True)
+    shutil.copy(os.path.join(SRC, "oracle.h"), d)
+    with open(os.path.join(d, "oracle.c"), "w") as f:
+        f.write(src.replace(old, new))
+    so = os.path.join(d, "libmut.so")
+    res = subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                          os.path.join(d, "oracle.c"), "-o", so, "-lm"],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    L = oracle.load(so)
+    caught = []
+    for chk in pins.ALL_CHECKS:
+        try:
+            out = chk(L=L)
+        except AssertionError:
+            caught.append(chk.__name__)
+            break
+        if out is False:   # check skipped (e.g. no libcurand)
+            continue
+    assert caught, f"no pin caught the planted mistake: {name}"
