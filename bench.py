@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark: batched exact top-k / top-p truncation and sampling.
+
+One step = one smp_sample call (temperature, mask, top-k, top-p, draw, kept
+mask + count) over one batch of the named workload.  Default workload:
+B=256 rows x V=128256 bf16 logits with mixed per-row parameters.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Prints one JSON line.  `value` = rows/s over all ranks, device-timed with CUDA
+events, inputs resident in HBM and rotated over enough copies to exceed L2.
+`e2e` = the same metric through the C ABI with the logits and parameters
+copied from pinned host memory and the results read back every step.
+`--impl reference` times the CPU oracle (plain full-sort reference) on the
+host cores on a bounded sample of the same workload.
+Multi-GPU (torchrun): rows are independent, every rank runs its own batch,
+no collective on the data path (weak scaling).
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "rows/sec and achieved HBM GB/s (fraction of roofline), B=256 V=128256 bf16"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["top_selection_stats_gb300/csrc/smp_kernel.cuh",
+                  "top_selection_stats_gb300/csrc/smp_device.cuh",
+                  "top_selection_stats_gb300/csrc/smp_api.cu"]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank, world, local = 0, 1, 0
+    if n_gpus > 1 or "RANK" in os.environ:
+        import torch.distributed as dist
+        rank = int(os.environ.get("RANK", 0))
+        world = int(os.environ.get("WORLD_SIZE", 1))
+        local = int(os.environ.get("LOCAL_RANK", 0))
+        if world > 1:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(local)
+            dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def row_bytes(V, has_mask, write_mask, esize):
+    W = (V + 31) // 32
+    b = V * esize + 28 + 12  # logits, params (t, k, p, seed, offset), token + status + count
+    if has_mask:
+        b += 4 * W
+    if write_mask:
+        b += 4 * W
+    return b
+
+
+def cpu_oracle_rate(case, rows):
+    import oracle
+    from top_selection_stats_gb300 import workloads
+    x = workloads.bits_numpy(case["logits"])
+    bm = None if case["bitmask"] is None else case["bitmask"].cpu().numpy().view(np.uint32)
+    sel = np.arange(rows)
+    p = {k: case[k].cpu().numpy()[sel] for k in ("temperature", "top_k", "top_p", "seed",
+                                                 "offset")}
+    cores = oracle.host_cores()
+    xs = np.ascontiguousarray(x[sel])
+    bms = None if bm is None else np.ascontiguousarray(bm[sel])
+    t0 = time.perf_counter()
+    oracle.run_batch(xs, case["dtype"], case["V"], bitmask=bms, n_threads=cores, **p)
+    dt = time.perf_counter() - t0
+    return rows / dt, cores, dt
+
+
+def run_reference(args, rank, world):
+    """CPU oracle arm: rank 0 alone, each step a bounded sample of the workload."""
+    if rank != 0:
+        return
+    from top_selection_stats_gb300 import workloads
+    case = workloads.make(args.workload, device="cpu")
+    rows = min(case["B"], args.ref_rows)
+    for _ in range(args.warmup):
+        cpu_oracle_rate(case, rows)
+    t0 = time.perf_counter()
+    cores = 1
+    for _ in range(args.steps):
+        _, cores, _ = cpu_oracle_rate(case, rows)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": case["B"], "V": case["V"],
+                   "logits": case["dtype"]},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {rows} rows of {args.workload} per step"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    from top_selection_stats_gb300 import Sampler, workloads
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = workloads.make(args.workload, device="cpu")
+    B, V = case["B"], case["V"]
+    esize = 4 if case["dtype"] == "f32" else 2
+    bytes_logits = B * V * esize
+    nbuf = max(2, -(-3 * L2_BYTES // bytes_logits))
+    stream = torch.cuda.current_stream(dev)
+    logits = [case["logits"].to(dev) for _ in range(nbuf)]
+    bitmask = None if case["bitmask"] is None else case["bitmask"].to(dev)
+    t = case["temperature"].to(dev)
+    k = case["top_k"].to(dev)
+    p = case["top_p"].to(dev)
+    seed = case["seed"].to(dev)
+    total = args.warmup + args.steps
+    offsets = [(case["offset"] + s * B).to(dev) for s in range(total)]
+    smp = Sampler(local, max_batch=max(B, 64), max_vocab=max(V, 1024))
+    plan = smp.plan(case["logits"].dtype, V)
+    W = (V + 31) // 32
+    tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    kmask = torch.empty((B, W), dtype=torch.int32, device=dev)
+    kcount = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def step(s, lg=None):
+        smp.sample(logits[s % nbuf] if lg is None else lg, t, k, p, seed, offsets[s],
+                   bitmask=bitmask, kept_mask=kmask, kept_count=kcount, tokens=tokens,
+                   status=status)
+
+    # path statistics (untimed)
+    smp.set_row_info(True, max_batch=B)
+    step(0)
+    torch.cuda.synchronize(dev)
+    info = smp.row_info(B).cpu().numpy()
+    smp.set_row_info(False)
+    paths = {name: int((info[:, 0] == code).sum())
+             for code, name in {0: "error", 1: "greedy", 2: "all", 3: "sigma", 4: "full"}.items()}
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clk = ClockSampler(local) if rank == 0 else None
+    if clk:
+        clk.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(args.warmup + i)
+        ev[i][1].record(stream)
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = clk.stop() if clk else None
+    elapsed_ms = g0.elapsed_time(g1)
+    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    kern_ms = max_over_ranks(kern_ms, world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = B * world / (ms_per_step / 1000.0)
+
+    # end to end through the C ABI with host buffers
+    host_logits = case["logits"].pin_memory()
+    host_par = [x.pin_memory() for x in (case["temperature"], case["top_k"], case["top_p"],
+                                         case["seed"])]
+    host_off = [o.cpu().pin_memory() for o in offsets]
+    host_mask = None if case["bitmask"] is None else case["bitmask"].pin_memory()
+    out_tok = torch.empty(B, dtype=torch.int32).pin_memory()
+    out_st = torch.empty(B, dtype=torch.int32).pin_memory()
+    out_mask = torch.empty((B, W), dtype=torch.int32).pin_memory()
+    out_cnt = torch.empty(B, dtype=torch.int32).pin_memory()
+    dl = torch.empty_like(logits[0])
+    dpar = [torch.empty_like(x, device=dev) for x in host_par]
+    doff = torch.empty(B, dtype=torch.int64, device=dev)
+    dmask = None if host_mask is None else torch.empty_like(host_mask, device=dev)
+
+    def e2e_step(s):
+        dl.copy_(host_logits, non_blocking=True)
+        for d_, h_ in zip(dpar, host_par):
+            d_.copy_(h_, non_blocking=True)
+        doff.copy_(host_off[s], non_blocking=True)
+        if dmask is not None:
+            dmask.copy_(host_mask, non_blocking=True)
+        smp.sample(dl, dpar[0], dpar[1], dpar[2], dpar[3], doff, bitmask=dmask,
+                   kept_mask=kmask, kept_count=kcount, tokens=tokens, status=status)
+        out_tok.copy_(tokens, non_blocking=True)
+        out_st.copy_(status, non_blocking=True)
+        out_mask.copy_(kmask, non_blocking=True)
+        out_cnt.copy_(kcount, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    e2e_steps = min(args.steps, max(3, args.steps // 2))
+    for s in range(min(3, args.warmup)):
+        e2e_step(s)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        e2e_step(s % total)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    h2d = bytes_logits + B * 28 + (0 if host_mask is None else host_mask.numel() * 4)
+    d2h = B * 4 * 3 + B * W * 4
+    e2e = {"value": B * world * e2e_steps / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    peak, peak_kind = measured_peaks()
+    alg_bytes = B * row_bytes(V, bitmask is not None, True, esize)
+    achieved = alg_bytes / (kern_ms / 1000.0) / 1e9
+    traffic = profiled_traffic(args.workload)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kern_ms}
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
+        rows = min(B, args.cpu_rows)
+        rate, cores, dt = cpu_oracle_rate(case, rows)
+        cpu = {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {rows} rows of {args.workload}, one pass ({dt:.2f} s wall)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "V": V, "logits": case["dtype"],
+                       "kept_mask": True,
+                       "l2": f"inputs rotated over {nbuf} copies ({nbuf * bytes_logits / 1e6:.0f} MB > L2)",
+                       "cluster": plan["cluster"], "slice": plan["slice"],
+                       "smem_per_cta": plan["smem"], "paths": paths},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    smp.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed256x128256_bf16")
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py --impl ours needs a CUDA GPU")
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,144 @@
+/*
+ * smp.h -- C ABI of libsmp: batched exact top-k / top-p truncation and
+ * sampling over a [B, V] logits matrix, hand-written for sm_103a (GB300).
+ *
+ * The contract (AI Infra KB note M012, section 02 "which candidates do top-k
+ * and top-p keep"; CMU 11-868 lecture 9 notes, section 3.3), per row:
+ *   1. temperature T: T == 0 takes a separate greedy argmax path and never
+ *      divides; T > 0 scales z = fl32(x / T)  (KB note section 02; "Sampling
+ *      system design" post, section on temperature);
+ *   2. legal-token mask: illegal tokens and -inf logits are excluded
+ *      (KB note section 05);
+ *   3. top-k: keep the K = min(top_k, |legal|) highest logits and
+ *      renormalise; ties at the boundary keep the earliest token ids
+ *      (Qrita paper notes, key design 3);
+ *   4. top-p: keep the shortest prefix, in descending probability, whose
+ *      renormalised mass reaches top_p (">=", the lecture's exercise 7
+ *      answer), again keeping the earliest ids among equal values;
+ *   5. renormalise and draw by inverse CDF in token-id order with
+ *      u = Philox4x32-10(seed, offset) (KB note section 02 figure note and
+ *      section 06 on explicit random state).
+ * An empty candidate set is an error; no substitute token is ever produced
+ * (KB note section 03, section 07).
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees, copies to the host or synchronises inside a
+ *     call.  Work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) on the handle's device.
+ *   - logits: row-major [B][ld] of `dtype`, ld >= V (elements).  Rows whose
+ *     start is 16-byte aligned are staged with bulk TMA copies; others with
+ *     plain loads (slower, same results).
+ *   - bitmask: nullable, uint32 [B][W], W = ceil(V/32), row stride W words.
+ *     Bit (j % 32) of word (j / 32) allows token j (1 = allowed).  Bits at or
+ *     past V are ignored.  NULL = every token allowed.
+ *   - kept_mask: same packed layout as bitmask, [B][W], 1 = token kept.
+ *   - The return value is the call status: SMP_OK, SMP_ERR_INVALID_PARAM for
+ *     bad arguments (NULL required pointers, B < 0, V < 1, ld < V, unknown
+ *     dtype), SMP_ERR_CAPACITY when B or V exceed the smp_create limits or V
+ *     exceeds what one thread-block cluster can hold, SMP_ERR_CUDA when the
+ *     launch fails.  Per-row outcomes go to row_status.
+ *   - A row whose status is not SMP_OK gets token -1, kept_count 0, an
+ *     all-zero kept_mask row and all-zero probabilities.
+ *   - RNG: every row reads exactly one Philox4x32-10 block, key =
+ *     (lo32 seed[r], hi32 seed[r]), counter = (lo32 offset[r], hi32
+ *     offset[r], 0, 0); u = (word0 >> 8) * 2^-24.  The library keeps no RNG
+ *     state: the caller advances offsets by the amount consumed (one block
+ *     per row per call), e.g. offset[r] = base + r and base += B per step.
+ *     Replaying a captured graph with frozen offsets repeats the draws.
+ */
+#ifndef SMP_H
+#define SMP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct smp_ctx* smp_handle;
+typedef void* smp_stream; /* a cudaStream_t */
+
+typedef enum { SMP_F32 = 0, SMP_BF16 = 1, SMP_F16 = 2 } smp_dtype;
+
+enum {
+  SMP_OK = 0,
+  SMP_ERR_EMPTY = 1,         /* row: no legal finite candidate            */
+  SMP_ERR_NONFINITE = 2,     /* row: NaN or +inf in a legal slot          */
+  SMP_ERR_INVALID_PARAM = 3, /* row: bad temperature/top_k/top_p; call: bad argument */
+  SMP_ERR_TIMEOUT = 4,       /* row: a bounded device wait expired        */
+  SMP_ERR_CUDA = 5,          /* call: CUDA error at launch or setup       */
+  SMP_ERR_CAPACITY = 6       /* call: B or V beyond the handle's limits   */
+};
+
+/* Per-row sampling parameters, all DEVICE arrays of length B ("Sampling
+ * system design" post: every sequence carries its own SamplingParams).
+ *   temperature: >= 0 (0 = greedy); NaN or < 0 -> row SMP_ERR_INVALID_PARAM
+ *   top_k      : >= 1; values above V mean V; < 1 -> SMP_ERR_INVALID_PARAM
+ *   top_p      : in (0, 1]; 1 disables top-p; else SMP_ERR_INVALID_PARAM
+ *   seed, offset: Philox key and counter (see above). */
+typedef struct {
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const uint64_t* seed;
+  const uint64_t* offset;
+} smp_row_params;
+
+/* Create a handle bound to CUDA device `device` for calls with B <=
+ * max_batch and V <= max_vocab.  Queries the device, configures the kernels
+ * (cluster size, shared memory) and builds the host-side sigma-truncation
+ * table (Qrita paper notes, key design 1 and "training strategy": delta =
+ * Phi^-1(1 - k/V) from a precomputed table).  Allocates no device memory.
+ * Returns SMP_OK, SMP_ERR_INVALID_PARAM or SMP_ERR_CUDA. */
+int smp_create(smp_handle* h, int device, int max_batch, int max_vocab);
+
+/* Release a handle (NULL is accepted). */
+int smp_destroy(smp_handle h);
+
+/* Kept set of every row: after temperature, mask, top-k and top-p (steps
+ * 1-4 above), write kept_mask [B][W] and kept_count [B].  Greedy rows keep
+ * {argmax} with probability 1.  probs_out (nullable) receives [B][V] fp32
+ * final probabilities (0 outside the kept set) -- a test aid that costs 4*V
+ * bytes of writes per row.  No random number is drawn. */
+int smp_topk_topp_mask(smp_handle h, const void* logits, smp_dtype dtype, int B, int V,
+                       int64_t ld, const uint32_t* bitmask, const smp_row_params* params,
+                       uint32_t* kept_mask, int32_t* kept_count, int32_t* row_status,
+                       float* probs_out, smp_stream stream);
+
+/* Full contract (steps 1-5): tokens [B] and row_status [B]; kept_mask and
+ * kept_count (both nullable) as in smp_topk_topp_mask. */
+int smp_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+               const uint32_t* bitmask, const smp_row_params* params, int32_t* tokens,
+               int32_t* row_status, uint32_t* kept_mask, int32_t* kept_count,
+               smp_stream stream);
+
+/* Greedy path alone (KB note section 02; lecture 9 answer 1): the legal
+ * finite token with the largest logit, the smallest id on ties.  Rows with
+ * no legal finite logit get SMP_ERR_EMPTY, rows with NaN / +inf in a legal
+ * slot SMP_ERR_NONFINITE. */
+int smp_argmax(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+               const uint32_t* bitmask, int32_t* tokens, int32_t* row_status,
+               smp_stream stream);
+
+/* Optional per-row diagnostics for subsequent calls on this handle: when
+ * row_info is not NULL, each call writes int32 [B][4] to it (DEVICE memory
+ * owned by the caller, at least max_batch*4 entries): {path, band size,
+ * selection rounds, refinement rounds}.  path: 0 error, 1 greedy, 2 all
+ * legal kept, 3 sigma-truncation hit, 4 full-row refinement.  NULL turns it
+ * off.  Not thread-safe against concurrent calls on the same handle. */
+int smp_set_row_info(smp_handle h, int32_t* row_info);
+
+/* Launch plan for (dtype, V): cluster size, slice length (elements per CTA),
+ * dynamic shared memory per CTA (bytes) and candidate capacity.  Any output
+ * pointer may be NULL.  Returns SMP_ERR_CAPACITY when V cannot be held. */
+int smp_plan(smp_handle h, smp_dtype dtype, int V, int* cluster, int* slice, int* smem_bytes,
+             int* capacity);
+
+/* Static description of a status code. */
+const char* smp_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMP_H */

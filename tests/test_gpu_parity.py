@@ -1,0 +1,179 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from top_selection_stats_gb300 import workloads
+import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_compare(case, modes=("sample", "mask"), check_probs=True, rows=None):
+    r = H.oracle_run(case, want_probs=True, rows=rows)
+    out = {}
+    for mode in modes:
+        g = H.gpu_run(case, mode=mode, want_probs=check_probs)
+        out[mode] = H.compare(case, g, r, mode=mode, rows=rows,
+                              check_probs=check_probs and mode == "mask")
+    return out
+
+
+def test_tiny_mixed_f32():
+    run_and_compare(workloads.make("tiny4x1024_f32"))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("V", [1, 7, 31, 33, 1000, 2049, 5003, 32000, 70001])
+def test_random_shapes(dtype, V):
+    case = workloads.random_case(V * 7 + len(dtype), 24, V, dtype=dtype, mask_frac=0.3,
+                                 neg_inf_frac=0.01 if V > 8 else 0.0)
+    run_and_compare(case)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ties_on_integer_grid(dtype):
+    case = workloads.random_case(11, 32, 4096, dtype=dtype, grid=6, mask_frac=0.2,
+                                 topks=(1, 3, 40, 700, 2000, 4096), topps=(0.5, 0.9, 1.0))
+    run_and_compare(case)
+
+
+def test_full_row_fallback_paths():
+    """Large k beyond the candidate buffer and flat rows under top-p force the
+    exact refinement path; it must agree with the oracle too."""
+    case = workloads.random_case(5, 32, 60000, dtype="bf16", sigma=0.5, n_head=(0, 4),
+                                 temps=(1.0, 2.0), topks=(5000, 20000, 60000),
+                                 topps=(0.5, 0.9, 0.99, 1.0), mask_frac=0.25)
+    g = H.gpu_run(case, mode="sample", row_info=True)
+    r = H.oracle_run(case, want_probs=True)
+    H.compare(case, g, r)
+    paths = g["row_info"][:, 0]
+    assert (paths == 4).any(), paths  # the refinement path ran
+
+
+def test_topk_only_f32_full():
+    case = workloads.make("topk64x32000_f32")
+    out = run_and_compare(case)
+    assert out["sample"]["token_checked"] > 50
+
+
+def test_mixed_bf16_full():
+    case = workloads.make("mixed256x128256_bf16")
+    run_and_compare(case, check_probs=True)
+
+
+def test_ties_masks_bf16_full():
+    case = workloads.make("ties512x151936_bf16")
+    r = H.oracle_run(case, want_probs=False)
+    assert (r["status"] == 1).sum() == 1  # the row with an empty mask
+    g = H.gpu_run(case, mode="sample")
+    H.compare(case, g, r)
+
+
+def test_decode_f16_sampled_rows():
+    rng = np.random.default_rng(0)
+    for step in (0, 1, 199):
+        case = workloads.make("decode1024x256000_f16", step=step, device="cuda")
+        case_cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in case.items()}
+        rows = np.sort(rng.choice(case["B"], size=48, replace=False))
+        r = H.oracle_run(case_cpu, rows=rows)
+        g = H.gpu_run(case_cpu, mode="sample")
+        H.compare(case_cpu, g, r, rows=rows)
+
+
+def test_argmax_matches_oracle():
+    for name in ("tiny4x1024_f32", "topk64x32000_f32"):
+        case = workloads.make(name)
+        g = H.gpu_run(case, mode="argmax")
+        r = H.oracle_run(case, mode="argmax")
+        H.compare(case, g, r, mode="argmax")
+    case = workloads.random_case(3, 64, 3001, dtype="bf16", grid=3, mask_frac=0.5,
+                                 neg_inf_frac=0.05)
+    H.compare(case, H.gpu_run(case, mode="argmax"), H.oracle_run(case, mode="argmax"),
+              mode="argmax")
+
+
+def test_error_rows():
+    V = 300
+    x = np.random.default_rng(1).standard_normal((6, V)).astype(np.float32)
+    x[1, 5] = np.nan
+    x[2, :] = -np.inf
+    x[3, 7] = np.inf
+    allowed = np.ones((6, V), bool)
+    allowed[4] = False
+    case = dict(name="errors", B=6, V=V, dtype="f32", logits=torch.from_numpy(x),
+                bitmask=torch.from_numpy(workloads.mask_from_allowed(allowed).view(np.int32)),
+                temperature=torch.tensor([1, 1, 1, 1, 1, -1.0], dtype=torch.float32),
+                top_k=torch.tensor([5] * 6, dtype=torch.int32),
+                top_p=torch.tensor([0.9] * 6, dtype=torch.float32),
+                seed=torch.zeros(6, dtype=torch.int64), offset=torch.arange(6))
+    g = H.gpu_run(case)
+    assert list(g["status"]) == [0, 2, 1, 2, 1, 3]
+    H.compare(case, g, H.oracle_run(case))
+
+
+def test_strided_and_unaligned_rows():
+    """ld > V (padded rows) and rows that are not 16-byte aligned (plain loads)."""
+    for dtype, V, ld in (("bf16", 1003, 1011), ("f32", 5001, 5003), ("f16", 4096, 4100)):
+        base = workloads.random_case(V + ld, 16, ld, dtype=dtype, topps=(0.9, 1.0))
+        full = base["logits"]
+        case = dict(base)
+        case["V"] = V
+        # oracle sees [B, ld] storage, V columns
+        x = workloads.bits_numpy(full)
+        p = {k: base[k].numpy() for k in ("temperature", "top_k", "top_p", "seed", "offset")}
+        p["top_k"] = np.minimum(p["top_k"], V)
+        r = oracle.run_batch(x, dtype, V, ld=ld, n_threads=4, **p)
+        s = H.sampler()
+        d = {k: torch.as_tensor(v).cuda() for k, v in p.items()}
+        lg = full.cuda()
+        out = s.sample(lg, d["temperature"], d["top_k"], d["top_p"], d["seed"], d["offset"],
+                       V=V, want_mask=True)
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy() for k, v in out.items()}
+        g["kept_mask"] = g["kept_mask"].view(np.uint32)
+        case["B"] = 16
+        case["name"] = f"strided-{dtype}"
+        H.compare(case, g, r)
+
+
+def test_determinism_repeated_calls():
+    case = workloads.make("mixed256x128256_bf16")
+    a = H.gpu_run(case, mode="sample")
+    for _ in range(5):
+        b = H.gpu_run(case, mode="sample")
+        assert (a["tokens"] == b["tokens"]).all()
+        assert (a["kept_mask"] == b["kept_mask"]).all()
+
+
+def test_sampling_frequencies_tv():
+    """10^6 draws of one row (replicated, distinct offsets) against the
+    oracle's exact probabilities: total variation within the noise floor."""
+    V = 2000
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(V) * 2).astype(np.float32)
+    x[rng.choice(V, 30, replace=False)] += 6
+    n_per, calls = 4096, 245
+    case1 = dict(name="tv", B=1, V=V, dtype="f32", logits=torch.from_numpy(x[None, :].copy()),
+                 bitmask=None, temperature=torch.tensor([0.9]), top_k=torch.tensor([50], dtype=torch.int32),
+                 top_p=torch.tensor([0.9]), seed=torch.tensor([3]), offset=torch.tensor([0]))
+    r = H.oracle_run(case1, want_probs=True)
+    p = r["probs"][0]
+    s = H.sampler()
+    lg = torch.from_numpy(np.repeat(x[None, :], n_per, axis=0)).cuda()
+    t = torch.full((n_per,), 0.9, device="cuda")
+    k = torch.full((n_per,), 50, dtype=torch.int32, device="cuda")
+    pp = torch.full((n_per,), 0.9, device="cuda")
+    sd = torch.full((n_per,), 3, dtype=torch.int64, device="cuda")
+    counts = torch.zeros(V, dtype=torch.int64, device="cuda")
+    for c in range(calls):
+        off = torch.arange(n_per, device="cuda", dtype=torch.int64) + c * n_per
+        out = s.sample(lg, t, k, pp, sd, off)
+        counts += torch.bincount(out["tokens"].long(), minlength=V)
+    n = n_per * calls
+    freq = counts.cpu().numpy() / n
+    tv = 0.5 * np.abs(freq - p).sum()
+    floor = 0.5 * np.sum(np.sqrt(2 * p * (1 - p) / (np.pi * n)))
+    assert tv <= max(0.01, 3 * floor), (tv, floor)
+    assert tv <= 0.01

@@ -1,0 +1,196 @@
+"""ctypes binding of libsmp (include/smp.h).  Argument marshalling only."""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(HERE, "libsmp.so")
+
+SMP_OK, SMP_ERR_EMPTY, SMP_ERR_NONFINITE, SMP_ERR_INVALID_PARAM = 0, 1, 2, 3
+SMP_ERR_TIMEOUT, SMP_ERR_CUDA, SMP_ERR_CAPACITY = 4, 5, 6
+SMP_F32, SMP_BF16, SMP_F16 = 0, 1, 2
+PATH_NAMES = {0: "error", 1: "greedy", 2: "all", 3: "sigma", 4: "full"}
+
+_DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_F16}
+
+EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
+           "smp_set_row_info", "smp_plan", "smp_status_string")
+
+
+class SmpError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: status {code}")
+        self.code = code
+
+
+class RowParams(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_void_p), ("top_k", ctypes.c_void_p),
+                ("top_p", ctypes.c_void_p), ("seed", ctypes.c_void_p),
+                ("offset", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path=None):
+    """Load libsmp.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or lib_path
+    if not os.path.exists(p):
+        raise FileNotFoundError(
+            f"{p} is missing: build it with __graft_entry__.build() (nvcc, sm_103a)")
+    L = ctypes.CDLL(p)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.smp_create.argtypes = [ctypes.POINTER(P), I, I, I]
+    L.smp_destroy.argtypes = [P]
+    L.smp_topk_topp_mask.argtypes = [P, P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams),
+                                     P, P, P, P, P]
+    L.smp_sample.argtypes = [P, P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams), P, P,
+                             P, P, P]
+    L.smp_argmax.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P]
+    L.smp_set_row_info.argtypes = [P, P]
+    L.smp_plan.argtypes = [P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
+                           ctypes.POINTER(I)]
+    L.smp_status_string.restype = ctypes.c_char_p
+    L.smp_status_string.argtypes = [I]
+    for name in EXPORTS:
+        getattr(L, name).restype = getattr(L, name).restype or ctypes.c_int
+    if path is None:
+        _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc, what):
+    if rc != SMP_OK:
+        raise SmpError(rc, what)
+
+
+class Sampler:
+    """A libsmp handle bound to one CUDA device.
+
+    All tensors must be contiguous CUDA tensors on that device.  logits:
+    [B, V] (or [B, ld] with ld >= V via ``ld``) float32 / bfloat16 / float16;
+    bitmask: int32 [B, ceil(V/32)] holding uint32 bit patterns, or None;
+    temperature float32 [B]; top_k int32 [B]; top_p float32 [B]; seed, offset
+    int64 [B] holding uint64 bit patterns.
+    """
+
+    def __init__(self, device=0, max_batch=4096, max_vocab=1 << 20, lib=None):
+        self.lib = lib or load_library()
+        self.device = torch.device("cuda", device) if isinstance(device, int) else device
+        h = ctypes.c_void_p()
+        _check(self.lib.smp_create(ctypes.byref(h), self.device.index or 0, max_batch, max_vocab),
+               "smp_create")
+        self.h = h
+        self._row_info = None
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.smp_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- helpers ----------------------------------------------------------------
+    def _stream(self):
+        return ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
+
+    def _check_tensor(self, t, name, dtype=None):
+        if t is None:
+            return
+        if not t.is_cuda or t.device != self.device:
+            raise ValueError(f"{name} must be on {self.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+    def _prep(self, logits, V, bitmask, temperature, top_k, top_p, seed, offset):
+        if logits.dtype not in _DTYPES:
+            raise ValueError(f"unsupported logits dtype {logits.dtype}")
+        self._check_tensor(logits, "logits")
+        B, ld = logits.shape
+        V = ld if V is None else V
+        self._check_tensor(bitmask, "bitmask", torch.int32)
+        if bitmask is not None and tuple(bitmask.shape) != (B, (V + 31) // 32):
+            raise ValueError("bitmask must be [B, ceil(V/32)]")
+        for name, t, dt in (("temperature", temperature, torch.float32),
+                            ("top_k", top_k, torch.int32), ("top_p", top_p, torch.float32),
+                            ("seed", seed, torch.int64), ("offset", offset, torch.int64)):
+            self._check_tensor(t, name, dt)
+            if t is not None and t.numel() != B:
+                raise ValueError(f"{name} must have B={B} entries")
+        params = RowParams(*(None if t is None else t.data_ptr()
+                             for t in (temperature, top_k, top_p, seed, offset)))
+        return B, V, ld, params
+
+    def set_row_info(self, enable=True, max_batch=4096):
+        """Per-row diagnostics {path, band, selection rounds, refinement rounds}."""
+        if enable:
+            self._row_info = torch.zeros((max_batch, 4), dtype=torch.int32, device=self.device)
+            _check(self.lib.smp_set_row_info(self.h, _ptr(self._row_info)), "smp_set_row_info")
+        else:
+            self._row_info = None
+            _check(self.lib.smp_set_row_info(self.h, None), "smp_set_row_info")
+
+    def row_info(self, B):
+        return None if self._row_info is None else self._row_info[:B]
+
+    def plan(self, dtype, V):
+        out = [ctypes.c_int() for _ in range(4)]
+        rc = self.lib.smp_plan(self.h, _DTYPES[dtype], V, *[ctypes.byref(o) for o in out])
+        _check(rc, "smp_plan")
+        return dict(cluster=out[0].value, slice=out[1].value, smem=out[2].value,
+                    capacity=out[3].value)
+
+    # -- entry points -------------------------------------------------------------
+    def sample(self, logits, temperature, top_k, top_p, seed, offset, bitmask=None, V=None,
+               kept_mask=None, kept_count=None, want_mask=False, tokens=None, status=None):
+        B, V, ld, params = self._prep(logits, V, bitmask, temperature, top_k, top_p, seed, offset)
+        dev = self.device
+        tokens = torch.empty(B, dtype=torch.int32, device=dev) if tokens is None else tokens
+        status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+        if want_mask and kept_mask is None:
+            kept_mask = torch.empty((B, (V + 31) // 32), dtype=torch.int32, device=dev)
+            kept_count = torch.empty(B, dtype=torch.int32, device=dev)
+        rc = self.lib.smp_sample(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V, ld,
+                                 _ptr(bitmask), ctypes.byref(params), _ptr(tokens), _ptr(status),
+                                 _ptr(kept_mask), _ptr(kept_count), self._stream())
+        _check(rc, "smp_sample")
+        return dict(tokens=tokens, status=status, kept_mask=kept_mask, kept_count=kept_count)
+
+    def topk_topp_mask(self, logits, temperature, top_k, top_p, bitmask=None, V=None,
+                       want_probs=False):
+        B, V, ld, params = self._prep(logits, V, bitmask, temperature, top_k, top_p, None, None)
+        dev = self.device
+        kept_mask = torch.empty((B, (V + 31) // 32), dtype=torch.int32, device=dev)
+        kept_count = torch.empty(B, dtype=torch.int32, device=dev)
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+        probs = torch.empty((B, V), dtype=torch.float32, device=dev) if want_probs else None
+        rc = self.lib.smp_topk_topp_mask(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V, ld,
+                                         _ptr(bitmask), ctypes.byref(params), _ptr(kept_mask),
+                                         _ptr(kept_count), _ptr(status), _ptr(probs),
+                                         self._stream())
+        _check(rc, "smp_topk_topp_mask")
+        return dict(kept_mask=kept_mask, kept_count=kept_count, status=status, probs=probs)
+
+    def argmax(self, logits, bitmask=None, V=None):
+        B, V, ld, _ = self._prep(logits, V, bitmask, None, None, None, None, None)
+        dev = self.device
+        tokens = torch.empty(B, dtype=torch.int32, device=dev)
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+        rc = self.lib.smp_argmax(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V, ld,
+                                 _ptr(bitmask), _ptr(tokens), _ptr(status), self._stream())
+        _check(rc, "smp_argmax")
+        return dict(tokens=tokens, status=status)

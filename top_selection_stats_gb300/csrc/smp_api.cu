@@ -1,0 +1,310 @@
+// smp_api.cu -- host side of the C ABI declared in include/smp.h: argument
+// checks, launch planning (cluster size, slice length, shared memory) and the
+// sigma-truncation table.  All work is enqueued on the caller's stream; no
+// call allocates, copies to the host or synchronises.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/smp.h"
+#include "smp_kernel.cuh"
+
+using namespace smp;
+
+struct PlanEntry {
+  int dt, V, S, L, cap, smem, ok;
+};
+
+struct smp_ctx {
+  int device;
+  int max_batch, max_vocab;
+  int sm_count;
+  int smem_optin;
+  float delta[DTAB];
+  int32_t* row_info;
+  std::mutex mu;
+  PlanEntry cache[16];
+  int ncache;
+};
+
+namespace {
+
+// Upper-tail normal quantile: z with 0.5 * erfc(z / sqrt 2) = q, by bisection
+// (Qrita paper notes, "training strategy": delta = Phi^-1(1 - k/V)).
+double upper_quantile(double q) {
+  if (q >= 1.0) return -8.0;
+  double lo = -8.0, hi = 8.0;
+  for (int i = 0; i < 200; ++i) {
+    const double mid = 0.5 * (lo + hi);
+    const double tail = 0.5 * std::erfc(mid / std::sqrt(2.0));
+    if (tail > q) lo = mid;
+    else hi = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
+template <int DT>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&smp_rows_kernel<DT>);
+}
+const void* kernel_for(int dt) {
+  switch (dt) {
+    case DT_F32: return kernel_ptr<DT_F32>();
+    case DT_BF16: return kernel_ptr<DT_BF16>();
+    default: return kernel_ptr<DT_F16>();
+  }
+}
+
+constexpr int SLICE_TARGET_BYTES = 48 * 1024;
+constexpr int CAP_DEFAULT = 4096;
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+// Choose cluster size S, slice length L and candidate capacity for (dtype, V).
+int make_plan(smp_ctx* h, int dt, int V, PlanEntry* out) {
+  std::lock_guard<std::mutex> lock(h->mu);
+  for (int i = 0; i < h->ncache; ++i)
+    if (h->cache[i].dt == dt && h->cache[i].V == V) {
+      *out = h->cache[i];
+      return out->ok ? SMP_OK : SMP_ERR_CAPACITY;
+    }
+  const int es = esize_of(dt), al = slice_align(dt);
+  PlanEntry p{dt, V, 0, 0, 0, 0, 0};
+  const void* k = kernel_for(dt);
+  for (int slice_bytes = SLICE_TARGET_BYTES; slice_bytes <= 160 * 1024 && !p.ok;
+       slice_bytes += 16 * 1024) {
+    int S = (int)(((long long)V * es + slice_bytes - 1) / slice_bytes);
+    if (S < 1) S = 1;
+    if (S > MAX_CLUSTER) continue;
+    for (; S <= MAX_CLUSTER && !p.ok; ++S) {
+      int L = (V + S - 1) / S;
+      L = (L + al - 1) / al * al;
+      if ((long long)L * (S - 1) >= V && S > 1) break;  // a CTA would hold nothing
+      const int cap = CAP_DEFAULT;
+      const Layout lay = make_layout(L, dt, cap, S);
+      if (lay.total > h->smem_optin) break;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = S;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(S, 1, 1);
+      cfg.blockDim = dim3(NT, 1, 1);
+      cfg.dynamicSmemBytes = lay.total;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int nclusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&nclusters, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        nclusters = 0;
+      }
+      if (nclusters > 0) {
+        p.S = S;
+        p.L = L;
+        p.cap = cap;
+        p.smem = lay.total;
+        p.ok = 1;
+      }
+      break;  // larger S for the same slice size only shrinks slices; try bigger slices
+    }
+  }
+  if (h->ncache < 16) h->cache[h->ncache++] = p;
+  *out = p;
+  return p.ok ? SMP_OK : SMP_ERR_CAPACITY;
+}
+
+int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64_t ld,
+           const uint32_t* bitmask, const smp_row_params* params, int32_t* tokens,
+           int32_t* status, uint32_t* kept_mask, int32_t* kept_count, float* probs,
+           smp_stream stream) {
+  if (!h || !logits || !status) return SMP_ERR_INVALID_PARAM;
+  if (dt != DT_F32 && dt != DT_BF16 && dt != DT_F16) return SMP_ERR_INVALID_PARAM;
+  if (B < 0 || V < 1 || ld < V) return SMP_ERR_INVALID_PARAM;
+  if (mode != MODE_ARGMAX &&
+      (!params || !params->temperature || !params->top_k || !params->top_p))
+    return SMP_ERR_INVALID_PARAM;
+  if (mode == MODE_SAMPLE && (!params->seed || !params->offset || !tokens))
+    return SMP_ERR_INVALID_PARAM;
+  if (mode == MODE_MASK && (!kept_mask || !kept_count)) return SMP_ERR_INVALID_PARAM;
+  if (mode == MODE_ARGMAX && !tokens) return SMP_ERR_INVALID_PARAM;
+  if (B > h->max_batch || V > h->max_vocab) return SMP_ERR_CAPACITY;
+  if (B == 0) return SMP_OK;
+  DeviceGuard guard(h->device);
+  PlanEntry p;
+  int rc = make_plan(h, dt, V, &p);
+  if (rc != SMP_OK) return rc;
+  if ((long long)B * p.S > 0x7fffffffLL) return SMP_ERR_CAPACITY;
+
+  KArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.logits = logits;
+  a.ld = ld;
+  a.B = B;
+  a.V = V;
+  a.W = (V + 31) / 32;
+  a.bitmask = bitmask;
+  if (params) {
+    a.temperature = params->temperature;
+    a.top_k = params->top_k;
+    a.top_p = params->top_p;
+    a.seed = reinterpret_cast<const unsigned long long*>(params->seed);
+    a.offset = reinterpret_cast<const unsigned long long*>(params->offset);
+  }
+  a.tokens = tokens;
+  a.status = status;
+  a.kept_mask = kept_mask;
+  a.kept_count = kept_count;
+  a.probs = probs;
+  a.row_info = h->row_info;
+  a.mode = mode;
+  a.L = p.L;
+  a.cap = p.cap;
+  const size_t es = (size_t)esize_of(dt);
+  a.use_tma = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
+  std::memcpy(a.delta, h->delta, sizeof(a.delta));
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(B * p.S), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err;
+  switch (dt) {
+    case DT_F32: err = cudaLaunchKernelEx(&cfg, smp_rows_kernel<DT_F32>, a); break;
+    case DT_BF16: err = cudaLaunchKernelEx(&cfg, smp_rows_kernel<DT_BF16>, a); break;
+    default: err = cudaLaunchKernelEx(&cfg, smp_rows_kernel<DT_F16>, a); break;
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return SMP_ERR_CUDA;
+  }
+  return SMP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
+  if (!out || max_batch < 1 || max_vocab < 1) return SMP_ERR_INVALID_PARAM;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return SMP_ERR_CUDA;
+  }
+  DeviceGuard guard(device);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return SMP_ERR_CUDA;
+  smp_ctx* h = new smp_ctx();
+  h->device = device;
+  h->max_batch = max_batch;
+  h->max_vocab = max_vocab;
+  h->sm_count = prop.multiProcessorCount;
+  h->smem_optin = (int)prop.sharedMemPerBlockOptin;
+  h->row_info = nullptr;
+  h->ncache = 0;
+  for (int i = 0; i < DTAB; ++i) {
+    const double l2q = -24.0 + 0.25 * i;
+    h->delta[i] = (float)upper_quantile(std::pow(2.0, l2q));
+  }
+  const void* ks[3] = {kernel_for(DT_F32), kernel_for(DT_BF16), kernel_for(DT_F16)};
+  for (const void* k : ks) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      delete h;
+      return SMP_ERR_CUDA;
+    }
+  }
+  *out = h;
+  return SMP_OK;
+}
+
+int smp_destroy(smp_handle h) {
+  delete h;
+  return SMP_OK;
+}
+
+int smp_topk_topp_mask(smp_handle h, const void* logits, smp_dtype dtype, int B, int V,
+                       int64_t ld, const uint32_t* bitmask, const smp_row_params* params,
+                       uint32_t* kept_mask, int32_t* kept_count, int32_t* row_status,
+                       float* probs_out, smp_stream stream) {
+  return launch(h, MODE_MASK, logits, (int)dtype, B, V, ld, bitmask, params, nullptr,
+                row_status, kept_mask, kept_count, probs_out, stream);
+}
+
+int smp_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+               const uint32_t* bitmask, const smp_row_params* params, int32_t* tokens,
+               int32_t* row_status, uint32_t* kept_mask, int32_t* kept_count,
+               smp_stream stream) {
+  return launch(h, MODE_SAMPLE, logits, (int)dtype, B, V, ld, bitmask, params, tokens,
+                row_status, kept_mask, kept_count, nullptr, stream);
+}
+
+int smp_argmax(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+               const uint32_t* bitmask, int32_t* tokens, int32_t* row_status,
+               smp_stream stream) {
+  return launch(h, MODE_ARGMAX, logits, (int)dtype, B, V, ld, bitmask, nullptr, tokens,
+                row_status, nullptr, nullptr, nullptr, stream);
+}
+
+int smp_set_row_info(smp_handle h, int32_t* row_info) {
+  if (!h) return SMP_ERR_INVALID_PARAM;
+  h->row_info = row_info;
+  return SMP_OK;
+}
+
+int smp_plan(smp_handle h, smp_dtype dtype, int V, int* cluster, int* slice, int* smem_bytes,
+             int* capacity) {
+  if (!h || V < 1) return SMP_ERR_INVALID_PARAM;
+  if ((int)dtype < 0 || (int)dtype > 2) return SMP_ERR_INVALID_PARAM;
+  DeviceGuard guard(h->device);
+  PlanEntry p;
+  const int rc = make_plan(h, (int)dtype, V, &p);
+  if (cluster) *cluster = p.S;
+  if (slice) *slice = p.L;
+  if (smem_bytes) *smem_bytes = p.smem;
+  if (capacity) *capacity = p.cap;
+  return rc;
+}
+
+const char* smp_status_string(int code) {
+  switch (code) {
+    case SMP_OK: return "ok";
+    case SMP_ERR_EMPTY: return "empty candidate set";
+    case SMP_ERR_NONFINITE: return "NaN or +inf in a legal slot";
+    case SMP_ERR_INVALID_PARAM: return "invalid parameter";
+    case SMP_ERR_TIMEOUT: return "bounded device wait expired";
+    case SMP_ERR_CUDA: return "CUDA error";
+    case SMP_ERR_CAPACITY: return "beyond capacity";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,202 @@
+// smp_device.cuh -- device helpers for the sampling kernels (sm_103a):
+// mbarrier + bulk-TMA staging, thread-block-cluster exchange, order-preserving
+// float keys, Philox4x32-10 and block-level reductions.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace smp {
+namespace cg = cooperative_groups;
+
+constexpr int NT = 256;           // threads per CTA
+constexpr int NWARP = NT / 32;    // warps per CTA
+constexpr int NBINS = 256;        // refinement histogram bins (one per thread)
+constexpr int NCHUNK = 4;         // bulk-copy chunks per slice (one mbarrier each)
+constexpr int MAX_CLUSTER = 16;   // CTAs per row, at most
+constexpr int DTAB = 97;          // sigma-truncation table: log2(q) in [-24, 0], step 1/4
+constexpr int NTHR = 4;           // sigma thresholds probed in one counting pass
+
+enum Dtype { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+enum Mode { MODE_SAMPLE = 0, MODE_MASK = 1, MODE_ARGMAX = 2 };
+enum Status { ST_OK = 0, ST_EMPTY = 1, ST_NONFINITE = 2, ST_INVALID = 3, ST_TIMEOUT = 4 };
+enum Path { PATH_ERROR = 0, PATH_GREEDY = 1, PATH_ALL = 2, PATH_SIGMA = 3, PATH_FULL = 4 };
+
+// --------------------------------------------------------------------------
+// Order-preserving keys.  Finite floats map to uint32 so that unsigned order
+// equals numeric order; -0 is folded onto +0 so that equal values share a key.
+// Every legal finite value has a key >= 0x00800000; key 0 is never legal.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t fkey(float x) {
+  uint32_t b = __float_as_uint(x);
+  if ((b << 1) == 0u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(b);
+}
+
+// --------------------------------------------------------------------------
+// Shared-memory addressing, mbarriers and bulk copies (inline PTX).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Bounded wait: gives up after `limit` SM clock cycles and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit) {
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+
+// --------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): round function and key
+// schedule from the paper.  key = (lo32 seed, hi32 seed), counter = (lo32
+// offset, hi32 offset, 0, 0); u = (word0 >> 8) * 2^-24 in [0, 1).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t offset) {
+  uint32_t c0 = (uint32_t)offset, c1 = (uint32_t)(offset >> 32), c2 = 0u, c3 = 0u;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+    uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+    uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  return (double)(c0 >> 8) * (1.0 / 16777216.0);
+}
+
+// --------------------------------------------------------------------------
+// Warp and block reductions (block = NT threads; `scratch` holds NWARP slots
+// and is reused: every block_* call starts and ends with __syncthreads()).
+// --------------------------------------------------------------------------
+template <class T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
+  return __reduce_min_sync(0xffffffffu, v);
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+  return __reduce_max_sync(0xffffffffu, v);
+}
+
+template <class T>
+__device__ T block_sum(T v, T* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  T r = scratch[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) r += scratch[w];
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, uint32_t* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_min_u32(v);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  uint32_t r = scratch[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) r = min(r, scratch[w]);
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max_u32(v);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  uint32_t r = scratch[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) r = max(r, scratch[w]);
+  __syncthreads();
+  return r;
+}
+
+// (min key, multiplicity of that key) pairs.
+struct MinCnt {
+  uint32_t key;
+  int cnt;
+};
+__device__ __forceinline__ MinCnt mc_combine(MinCnt a, MinCnt b) {
+  if (a.key < b.key) return a;
+  if (b.key < a.key) return b;
+  return MinCnt{a.key, a.cnt + b.cnt};
+}
+__device__ __forceinline__ MinCnt warp_mincnt(MinCnt v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MinCnt w{__shfl_xor_sync(0xffffffffu, v.key, o), __shfl_xor_sync(0xffffffffu, v.cnt, o)};
+    v = mc_combine(v, w);
+  }
+  return v;
+}
+
+// Inclusive warp scan (lane order).
+template <class T>
+__device__ __forceinline__ T warp_incl_scan(T v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+}  // namespace smp
