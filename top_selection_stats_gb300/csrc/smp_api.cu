@@ -24,6 +24,7 @@ struct smp_ctx {
   int max_batch, max_vocab;
   int sm_count;
   int smem_optin;
+  int smem_per_sm;
   float delta[DTAB];
   int32_t* row_info;
   std::mutex mu;
@@ -59,7 +60,6 @@ const void* kernel_for(int dt) {
   }
 }
 
-constexpr int SLICE_TARGET_BYTES = 48 * 1024;
 constexpr int CAP_DEFAULT = 4096;
 
 struct DeviceGuard {
@@ -75,7 +75,9 @@ struct DeviceGuard {
   }
 };
 
-// Choose cluster size S, slice length L and candidate capacity for (dtype, V).
+// Choose cluster size S, slice length L and candidate capacity for (dtype, V):
+// the smallest cluster whose CTAs fit two per SM (so that one CTA streams its
+// slice while the other selects), else the smallest that fits at all.
 int make_plan(smp_ctx* h, int dt, int V, PlanEntry* out) {
   std::lock_guard<std::mutex> lock(h->mu);
   for (int i = 0; i < h->ncache; ++i)
@@ -83,21 +85,19 @@ int make_plan(smp_ctx* h, int dt, int V, PlanEntry* out) {
       *out = h->cache[i];
       return out->ok ? SMP_OK : SMP_ERR_CAPACITY;
     }
-  const int es = esize_of(dt), al = slice_align(dt);
+  const int al = slice_align(dt);
+  const int two_per_sm = (h->smem_per_sm - 2 * 1024) / 2;
   PlanEntry p{dt, V, 0, 0, 0, 0, 0};
   const void* k = kernel_for(dt);
-  for (int slice_bytes = SLICE_TARGET_BYTES; slice_bytes <= 160 * 1024 && !p.ok;
-       slice_bytes += 16 * 1024) {
-    int S = (int)(((long long)V * es + slice_bytes - 1) / slice_bytes);
-    if (S < 1) S = 1;
-    if (S > MAX_CLUSTER) continue;
-    for (; S <= MAX_CLUSTER && !p.ok; ++S) {
+  for (int pass = 0; pass < 2 && !p.ok; ++pass) {
+    const int limit = pass == 0 ? two_per_sm : h->smem_optin;
+    for (int S = 1; S <= MAX_CLUSTER && !p.ok; ++S) {
       int L = (V + S - 1) / S;
       L = (L + al - 1) / al * al;
-      if ((long long)L * (S - 1) >= V && S > 1) break;  // a CTA would hold nothing
+      if (S > 1 && (long long)L * (S - 1) >= V) continue;  // a CTA would hold nothing
       const int cap = CAP_DEFAULT;
       const Layout lay = make_layout(L, dt, cap, S);
-      if (lay.total > h->smem_optin) break;
+      if (lay.total > limit) continue;
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -121,7 +121,6 @@ int make_plan(smp_ctx* h, int dt, int V, PlanEntry* out) {
         p.smem = lay.total;
         p.ok = 1;
       }
-      break;  // larger S for the same slice size only shrinks slices; try bigger slices
     }
   }
   if (h->ncache < 16) h->cache[h->ncache++] = p;
@@ -225,6 +224,7 @@ int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
   h->max_vocab = max_vocab;
   h->sm_count = prop.multiProcessorCount;
   h->smem_optin = (int)prop.sharedMemPerBlockOptin;
+  h->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
   h->row_info = nullptr;
   h->ncache = 0;
   for (int i = 0; i < DTAB; ++i) {
