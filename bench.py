@@ -34,9 +34,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "rows/sec and achieved HBM GB/s (fraction of roofline), B=256 V=128256 bf16"
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = ["top_selection_stats_gb300/csrc/smp_kernel.cuh",
+KERNEL_SOURCES = ["top_selection_stats_gb300/csrc/smp_stream.cuh",
                   "top_selection_stats_gb300/csrc/smp_device.cuh",
-                  "top_selection_stats_gb300/csrc/smp_kernel_main.cuh",
+                  "top_selection_stats_gb300/csrc/smp_stream_main.cuh",
                   "top_selection_stats_gb300/csrc/smp_api.cu"]
 
 

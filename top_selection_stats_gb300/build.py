@@ -7,7 +7,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libsmp.so")
 SOURCES = [os.path.join(CSRC, "smp_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("smp_kernel.cuh", "smp_kernel_main.cuh", "smp_device.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("smp_stream.cuh", "smp_stream_main.cuh", "smp_device.cuh")] + [
     os.path.join(ROOT, "include", "smp.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

@@ -11,13 +11,9 @@
 #include <mutex>
 
 #include "../../include/smp.h"
-#include "smp_kernel.cuh"
+#include "smp_stream.cuh"
 
 using namespace smp;
-
-struct PlanEntry {
-  int dt, V, S, L, cap, smem, ok;
-};
 
 struct smp_ctx {
   int device;
@@ -25,11 +21,9 @@ struct smp_ctx {
   int sm_count;
   int smem_optin;
   int smem_per_sm;
+  int grid_max;
   float delta[DTAB];
   int32_t* row_info;
-  std::mutex mu;
-  PlanEntry cache[16];
-  int ncache;
 };
 
 namespace {
@@ -50,7 +44,7 @@ double upper_quantile(double q) {
 
 template <int DT>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&smp_rows_kernel<DT>);
+  return reinterpret_cast<const void*>(&smp_stream_kernel<DT>);
 }
 const void* kernel_for(int dt) {
   switch (dt) {
@@ -60,7 +54,7 @@ const void* kernel_for(int dt) {
   }
 }
 
-constexpr int CAP_DEFAULT = 4096;
+int chunk_elems(int dt) { return STAGE_BYTES / esize_of(dt); }
 
 struct DeviceGuard {
   int prev = -1;
@@ -74,59 +68,6 @@ struct DeviceGuard {
     if (changed) cudaSetDevice(prev);
   }
 };
-
-// Choose cluster size S, slice length L and candidate capacity for (dtype, V):
-// the smallest cluster whose CTAs fit two per SM (so that one CTA streams its
-// slice while the other selects), else the smallest that fits at all.
-int make_plan(smp_ctx* h, int dt, int V, PlanEntry* out) {
-  std::lock_guard<std::mutex> lock(h->mu);
-  for (int i = 0; i < h->ncache; ++i)
-    if (h->cache[i].dt == dt && h->cache[i].V == V) {
-      *out = h->cache[i];
-      return out->ok ? SMP_OK : SMP_ERR_CAPACITY;
-    }
-  const int al = slice_align(dt);
-  const int two_per_sm = (h->smem_per_sm - 2 * 1024) / 2;
-  PlanEntry p{dt, V, 0, 0, 0, 0, 0};
-  const void* k = kernel_for(dt);
-  for (int pass = 0; pass < 2 && !p.ok; ++pass) {
-    const int limit = pass == 0 ? two_per_sm : h->smem_optin;
-    for (int S = 1; S <= MAX_CLUSTER && !p.ok; ++S) {
-      int L = (V + S - 1) / S;
-      L = (L + al - 1) / al * al;
-      if (S > 1 && (long long)L * (S - 1) >= V) continue;  // a CTA would hold nothing
-      const int cap = CAP_DEFAULT;
-      const Layout lay = make_layout(L, dt, cap, S);
-      if (lay.total > limit) continue;
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = S;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(S, 1, 1);
-      cfg.blockDim = dim3(NT, 1, 1);
-      cfg.dynamicSmemBytes = lay.total;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int nclusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&nclusters, k, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        nclusters = 0;
-      }
-      if (nclusters > 0) {
-        p.S = S;
-        p.L = L;
-        p.cap = cap;
-        p.smem = lay.total;
-        p.ok = 1;
-      }
-    }
-  }
-  if (h->ncache < 16) h->cache[h->ncache++] = p;
-  *out = p;
-  return p.ok ? SMP_OK : SMP_ERR_CAPACITY;
-}
 
 int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64_t ld,
            const uint32_t* bitmask, const smp_row_params* params, int32_t* tokens,
@@ -143,12 +84,9 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   if (mode == MODE_MASK && (!kept_mask || !kept_count)) return SMP_ERR_INVALID_PARAM;
   if (mode == MODE_ARGMAX && !tokens) return SMP_ERR_INVALID_PARAM;
   if (B > h->max_batch || V > h->max_vocab) return SMP_ERR_CAPACITY;
+  if ((long long)V > (long long)MAXCH * chunk_elems(dt)) return SMP_ERR_CAPACITY;
   if (B == 0) return SMP_OK;
   DeviceGuard guard(h->device);
-  PlanEntry p;
-  int rc = make_plan(h, dt, V, &p);
-  if (rc != SMP_OK) return rc;
-  if ((long long)B * p.S > 0x7fffffffLL) return SMP_ERR_CAPACITY;
 
   KArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -172,34 +110,19 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   a.probs = probs;
   a.row_info = h->row_info;
   a.mode = mode;
-  a.L = p.L;
-  a.cap = p.cap;
   const size_t es = (size_t)esize_of(dt);
   a.use_tma = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
   std::memcpy(a.delta, h->delta, sizeof(a.delta));
 
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)(B * p.S), 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = p.smem;
-  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t err;
+  // one CTA per row, at most two resident per SM; CTAs loop over rows
+  const int grid = B < h->grid_max ? B : h->grid_max;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   switch (dt) {
-    case DT_F32: err = cudaLaunchKernelEx(&cfg, smp_rows_kernel<DT_F32>, a); break;
-    case DT_BF16: err = cudaLaunchKernelEx(&cfg, smp_rows_kernel<DT_BF16>, a); break;
-    default: err = cudaLaunchKernelEx(&cfg, smp_rows_kernel<DT_F16>, a); break;
+    case DT_F32: smp_stream_kernel<DT_F32><<<grid, NT, SMEM_TOTAL, st>>>(a); break;
+    case DT_BF16: smp_stream_kernel<DT_BF16><<<grid, NT, SMEM_TOTAL, st>>>(a); break;
+    default: smp_stream_kernel<DT_F16><<<grid, NT, SMEM_TOTAL, st>>>(a); break;
   }
-  if (err != cudaSuccess) {
-    cudaGetLastError();
-    return SMP_ERR_CUDA;
-  }
+  if (cudaGetLastError() != cudaSuccess) return SMP_ERR_CUDA;
   return SMP_OK;
 }
 
@@ -226,22 +149,28 @@ int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
   h->smem_optin = (int)prop.sharedMemPerBlockOptin;
   h->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
   h->row_info = nullptr;
-  h->ncache = 0;
   for (int i = 0; i < DTAB; ++i) {
     const double l2q = -24.0 + 0.25 * i;
     h->delta[i] = (float)upper_quantile(std::pow(2.0, l2q));
   }
   const void* ks[3] = {kernel_for(DT_F32), kernel_for(DT_BF16), kernel_for(DT_F16)};
+  int per_sm = 1 << 30;
   for (const void* k : ks) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin) !=
+    int nb = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess) {
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, NT, SMEM_TOTAL) != cudaSuccess) {
       cudaGetLastError();
       delete h;
       return SMP_ERR_CUDA;
     }
+    per_sm = nb < per_sm ? nb : per_sm;
   }
+  if (per_sm < 1) {
+    delete h;
+    return SMP_ERR_CUDA;
+  }
+  h->grid_max = per_sm * h->sm_count;
   *out = h;
   return SMP_OK;
 }
@@ -284,14 +213,12 @@ int smp_plan(smp_handle h, smp_dtype dtype, int V, int* cluster, int* slice, int
              int* capacity) {
   if (!h || V < 1) return SMP_ERR_INVALID_PARAM;
   if ((int)dtype < 0 || (int)dtype > 2) return SMP_ERR_INVALID_PARAM;
-  DeviceGuard guard(h->device);
-  PlanEntry p;
-  const int rc = make_plan(h, (int)dtype, V, &p);
-  if (cluster) *cluster = p.S;
-  if (slice) *slice = p.L;
-  if (smem_bytes) *smem_bytes = p.smem;
-  if (capacity) *capacity = p.cap;
-  return rc;
+  const int ce = chunk_elems((int)dtype);
+  if (cluster) *cluster = 1;
+  if (slice) *slice = ce;
+  if (smem_bytes) *smem_bytes = SMEM_TOTAL;
+  if (capacity) *capacity = CAP;
+  return ((long long)V > (long long)MAXCH * ce) ? SMP_ERR_CAPACITY : SMP_OK;
 }
 
 const char* smp_status_string(int code) {
