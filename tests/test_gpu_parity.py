@@ -177,3 +177,37 @@ def test_sampling_frequencies_tv():
     floor = 0.5 * np.sum(np.sqrt(2 * p * (1 - p) / (np.pi * n)))
     assert tv <= max(0.01, 3 * floor), (tv, floor)
     assert tv <= 0.01
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_tie_groups_beyond_list_capacity(dtype):
+    """Rows of three values only: every boundary value has ~17k copies, more than
+    the candidate list holds, so the earliest-id tie quota is resolved by ranking
+    the copies in id order over the whole row."""
+    case = workloads.random_case(17 + len(dtype), 24, 50000, dtype=dtype, grid=3,
+                                 temps=(0.5, 1.0, 3.0), topks=(5000, 20000, 40000, 50000),
+                                 topps=(0.2, 0.6, 0.95, 1.0), mask_frac=0.2,
+                                 mask_density=(0.5, 0.9))
+    g = H.gpu_run(case, mode="sample", row_info=True)
+    r = H.oracle_run(case, want_probs=True)
+    H.compare(case, g, r)
+    gm = H.gpu_run(case, mode="mask", want_probs=True)
+    H.compare(case, gm, r, mode="mask", check_probs=True)
+
+
+def test_few_legal_tokens_take_the_whole_legal_set():
+    """Grammar masks that leave a handful of tokens: the list takes every legal
+    token, k beyond the legal count keeps them all."""
+    V = 151936
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((12, V)) * 2).astype(np.float32)
+    allowed = np.zeros((12, V), bool)
+    for r_ in range(12):
+        allowed[r_, rng.choice(V, size=int(rng.integers(1, 3000)), replace=False)] = True
+    case = dict(name="fewlegal", B=12, V=V, dtype="bf16", logits=workloads.to_dtype(x, "bf16"),
+                bitmask=torch.from_numpy(workloads.mask_from_allowed(allowed).view(np.int32)),
+                temperature=torch.tensor([0.8, 1.0, 1.3] * 4, dtype=torch.float32),
+                top_k=torch.tensor([40, 1000, 4096, V] * 3, dtype=torch.int32),
+                top_p=torch.tensor([0.95, 1.0, 0.5, 0.9] * 3, dtype=torch.float32),
+                seed=torch.full((12,), 9, dtype=torch.int64), offset=torch.arange(12))
+    run_and_compare(case)

@@ -1,17 +1,28 @@
-"""Build libsmp.so (the CUDA library behind include/smp.h) in-tree for sm_103a."""
+"""Build libsmp.so (the CUDA library behind include/smp.h) in-tree for sm_103a.
+
+The host API and the three element-type instantiations of the kernel are
+separate translation units, compiled in parallel and linked into one shared
+library.
+"""
 import os
 import subprocess
+from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libsmp.so")
-SOURCES = [os.path.join(CSRC, "smp_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("smp_stream.cuh", "smp_stream_main.cuh", "smp_device.cuh")] + [
-    os.path.join(ROOT, "include", "smp.h")]
+OBJDIR = os.path.join(HERE, "_build")
+SOURCES = [os.path.join(CSRC, f) for f in ("smp_api.cu", "smp_k_f32.cu", "smp_k_bf16.cu",
+                                           "smp_k_f16.cu")]
+HEADERS = [os.path.join(CSRC, f) for f in ("smp_device.cuh", "smp_core.cuh", "smp_list.cuh",
+                                           "smp_stream_passes.cuh", "smp_general.cuh",
+                                           "smp_kernel.cuh")]
+DEPS = SOURCES + HEADERS + [os.path.join(ROOT, "include", "smp.h")]
 
-NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-              "-Xcompiler", "-fPIC", "-shared", "--expt-relaxed-constexpr"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                     "--expt-relaxed-constexpr"]
 
 
 def nvcc():
@@ -26,17 +37,29 @@ def up_to_date():
     return all(os.path.getmtime(d) <= t for d in DEPS)
 
 
+def _run(cmd):
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+    return res.stdout + res.stderr
+
+
 def build(force=False, verbose=False, extra=()):
     """Compile the library unless it is newer than every source."""
     if not force and up_to_date():
         return LIB
+    os.makedirs(OBJDIR, exist_ok=True)
+    objs, cmds = [], []
+    for src in SOURCES:
+        obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+        objs.append(obj)
+        cmds.append([nvcc(), *NVCC_FLAGS, *extra, "-c", src, "-o", obj])
+    with ThreadPoolExecutor(max_workers=len(cmds)) as ex:
+        logs = list(ex.map(_run, cmds))
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), *NVCC_FLAGS, *extra, *SOURCES, "-o", tmp]
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+    logs.append(_run([nvcc(), *ARCH, "-shared", *objs, "-o", tmp]))
     if verbose:
-        print(res.stdout + res.stderr)
+        print("".join(logs))
     os.replace(tmp, LIB)
     return LIB
 

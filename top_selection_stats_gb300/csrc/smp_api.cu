@@ -11,7 +11,16 @@
 #include <mutex>
 
 #include "../../include/smp.h"
-#include "smp_stream.cuh"
+#include "smp_core.cuh"
+
+namespace smp {
+const void* kernel_f32();
+const void* kernel_bf16();
+const void* kernel_f16();
+cudaError_t launch_f32(const KArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_bf16(const KArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_f16(const KArgs& a, int grid, cudaStream_t st);
+}  // namespace smp
 
 using namespace smp;
 
@@ -42,15 +51,11 @@ double upper_quantile(double q) {
   return 0.5 * (lo + hi);
 }
 
-template <int DT>
-const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&smp_stream_kernel<DT>);
-}
 const void* kernel_for(int dt) {
   switch (dt) {
-    case DT_F32: return kernel_ptr<DT_F32>();
-    case DT_BF16: return kernel_ptr<DT_BF16>();
-    default: return kernel_ptr<DT_F16>();
+    case DT_F32: return kernel_f32();
+    case DT_BF16: return kernel_bf16();
+    default: return kernel_f16();
   }
 }
 
@@ -117,12 +122,13 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   // one CTA per row, at most two resident per SM; CTAs loop over rows
   const int grid = B < h->grid_max ? B : h->grid_max;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
   switch (dt) {
-    case DT_F32: smp_stream_kernel<DT_F32><<<grid, NT, SMEM_TOTAL, st>>>(a); break;
-    case DT_BF16: smp_stream_kernel<DT_BF16><<<grid, NT, SMEM_TOTAL, st>>>(a); break;
-    default: smp_stream_kernel<DT_F16><<<grid, NT, SMEM_TOTAL, st>>>(a); break;
+    case DT_F32: e = launch_f32(a, grid, st); break;
+    case DT_BF16: e = launch_bf16(a, grid, st); break;
+    default: e = launch_f16(a, grid, st); break;
   }
-  if (cudaGetLastError() != cudaSuccess) return SMP_ERR_CUDA;
+  if (e != cudaSuccess) return SMP_ERR_CUDA;
   return SMP_OK;
 }
 

@@ -1,0 +1,674 @@
+// smp_general.cuh -- exact selection for rows whose kept set does not fit the
+// candidate list (flat rows under top-p, top_k beyond the list, failed sigma
+// bands), and the passes shared by every row whose kept set is decided by a
+// (value, id) boundary.
+//
+// Weight-histogram bracket.  The mass stream histograms the legal elements by
+// a = (x - ref) * log2(e) / T (WHS bins per factor of two).  Counts per bin
+// are exact, so the bin holding the k-th element is known; masses per bin are
+// bounded by count * 2^a at the bin's edges, so the bins that can hold the
+// top-p boundary form a short bracket.  One band pass then collects the
+// bracket into the list (where the boundary and its tie quota are resolved
+// exactly), and at the same time writes the kept mask, count and per-chunk
+// masses of everything above the bracket, which is kept whatever the exact
+// boundary.
+//
+// Radix descent (fallback).  Each pass re-reads the row and builds a 2^11-bin
+// histogram -- counts for a top-k boundary, fixed-point masses for a top-p
+// boundary -- of the next key digit inside the current prefix, until the
+// bin holding the boundary has at most CAP elements; a band pass collects it.
+// A single value with more than CAP copies is resolved by a tie pass that
+// ranks its copies in id order.  Masses are integers (2^-40 units of the row
+// maximum's weight), so every decision is independent of summation order.
+#pragma once
+
+#include "smp_stream_passes.cuh"
+
+namespace smp {
+
+template <int DT>
+__device__ __forceinline__ float vmax_f(const uint4 r) {
+  float x[ElemT<DT>::EPV];
+  unpack<DT>(r, x);
+  float m = x[0];
+#pragma unroll
+  for (int j = 1; j < ElemT<DT>::EPV; ++j) m = fmaxf(m, x[j]);
+  return m;
+}
+
+// Weight 2^((x - m) * log2(e) / T) in fixed point (nm = -m * log2(e) / T).
+__device__ __forceinline__ uint64_t fx_weight(float x, float c2, float nm) {
+  return to_fx(fast_exp2(fmaf(x, c2, nm)));
+}
+
+// Weight-histogram bin of x (nref = -ref * log2(e) / T, as in the mass stream).
+__device__ __forceinline__ int wbin(float x, float c2, float nref) {
+  const float a = fmaf(x, c2, nref);
+  return min(max(__float2int_rd(fmaf(a, -(float)WHS, (float)WHOFF)), 0), WBINS - 1);
+}
+
+// Writes the kept-mask word of 32 consecutive elements held by 4 (16-bit) or
+// 8 (fp32) consecutive lanes; all lanes of the warp call it.
+template <int DT>
+__device__ __forceinline__ void put_mask_word(const Ctx<DT>& X, uint32_t* mrow, uint32_t kb,
+                                              int id0) {
+  constexpr int EPV = ElemT<DT>::EPV;
+  const int lane = threadIdx.x & 31;
+  uint32_t wv;
+  int wi;
+  if constexpr (EPV == 8) {
+    wv = kb << (8 * (lane & 3));
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+    wi = ((lane & 3) == 0) ? (id0 >> 5) : -1;
+  } else {
+    wv = kb << (4 * (lane & 7));
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
+    wi = ((lane & 7) == 0) ? (id0 >> 5) : -1;
+  }
+  if (mrow && wi >= 0 && wi < X.W) mrow[wi] = wv;
+}
+
+// Per-(chunk, warp) cell of row element id (the order of the kept masses).
+template <int DT>
+__device__ __forceinline__ int cell_of(int id) {
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE, VW = ElemT<DT>::VW;
+  return (id / CE) * NWARP + ((id % CE) / EPV) / VW;
+}
+// Fixed-point kept masses of list entries, per cell (in the ring scratch).
+template <int DT>
+__device__ __forceinline__ uint64_t* cell_extra(const Ctx<DT>& X) {
+  return list_scratch(X) + 1024;
+}
+
+// ---------------------------------------------------------------------------
+// Bracket from the weight histogram.  Bins (descending weight) 0..WBINS-1.
+//   K mode : counts; the bin holding the k-th element (counts are exact).
+//   P mode : masses (units of the reference weight) from excess-weighted
+//            counts; the bins where the running mass crosses PZ * (1 -/+
+//            1e-3), the margin covering the 2^-11 quantisation of the excess
+//            and the rounding of the mass stream's sums.
+// Returns false when the bracket holds (or may hold) more than CAP elements.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ bool wh_bracket(Ctx<DT>& Xr, bool pmode, int K, double PZ, float amax,
+                                        int& b_lo, int& b_hi) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const uint32_t* wh = X.wh;
+  constexpr int BPT = WBINS / NT;
+  const int t = threadIdx.x;
+  double v[BPT];
+  double s = 0.0;
+#pragma unroll
+  for (int q = 0; q < BPT; ++q) {
+    const int b = t * BPT + q;
+    // P mode: wh[b] / 2^11 counts the bin's elements in units of its lower
+    // edge weight 2^((WHOFF - b - 1) / WHS); the clamped end bins are bounded
+    // by amax above and 0 below
+    v[q] = (double)wh[b];
+    if (pmode) {
+      const double lo_w = (b == WBINS - 1) ? 0.0 : exp2((double)(WHOFF - b - 1) / WHS);
+      v[q] = (b == 0) ? v[q] / 2048.0 * exp2((double)fmaxf(amax, (float)WHOFF / WHS))
+                      : v[q] / 2048.0 * lo_w;
+    }
+    s += v[q];
+  }
+  double tot;
+  double cum = bscan_excl<double>(s, X.sh->rd[0], tot);
+  if (t == 0) {
+    X.sh->bi[0] = WBINS;
+    X.sh->bi[1] = -1;
+  }
+  __syncthreads();
+  const double lo_t = pmode ? PZ * (1.0 - 1e-3) : (double)K;
+  const double hi_t = pmode ? PZ * (1.0 + 1e-3) : (double)K;
+#pragma unroll
+  for (int q = 0; q < BPT; ++q) {
+    const int b = t * BPT + q;
+    if (v[q] > 0.0 && cum + v[q] >= lo_t) atomicMin(&X.sh->bi[0], b);
+    if (v[q] > 0.0 && cum < hi_t) atomicMax(&X.sh->bi[1], b);
+    cum += v[q];
+  }
+  __syncthreads();
+  b_lo = X.sh->bi[0];
+  b_hi = X.sh->bi[1];
+  if (b_lo >= WBINS || b_hi < b_lo) {
+    __syncthreads();
+    return false;
+  }
+  double n = 0.0;
+#pragma unroll
+  for (int q = 0; q < BPT; ++q) {
+    const int b = t * BPT + q;
+    if (b >= b_lo && b <= b_hi) n += pmode ? (double)wh[b] / 2048.0 : v[q];
+  }
+  n = bsum_d(n, X.sh->rd[1]);
+  (void)amax;
+  return n <= (double)CAP;
+}
+
+// ---------------------------------------------------------------------------
+// Band-and-kept pass over a weight-histogram bracket [b_lo, b_hi]: legal
+// elements of bins inside go to the list; those of bins above (larger
+// weights) are kept: kept-mask bits, count, per-(chunk, warp) masses relative
+// to the row maximum (nm) and their fixed-point total.  Every mask word is
+// written (bracket elements still 0).
+// ---------------------------------------------------------------------------
+struct BandOut {
+  int above_n;
+  uint64_t above_q;
+};
+template <int DT>
+__device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, float nref, float nm) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* mrow = X.a->kept_mask ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
+  const float c2 = X.c2;
+  if (threadIdx.x == 0) X.sh->n = 0;
+  int nk = 0;
+  uint64_t aq = 0;
+  ring_begin(X);
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    const char* stage = warp_wait(X, c);
+    float cs = 0.f;
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, c, vi);
+      const int id0 = c * CE + vi * EPV;
+      float x[EPV];
+      unpack<DT>(r, x);
+      uint32_t kb = 0u, cm = 0u;
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) {
+        if (!(x[j] > -INFINITY)) continue;
+        const int b = wbin(x[j], c2, nref);
+        if (b < b_lo) {
+          kb |= 1u << j;
+          const float w = fast_exp2(fmaf(x[j], c2, nm));
+          cs += w;
+          aq += to_fx(w);
+        } else if (b <= b_hi) {
+          cm |= 1u << j;
+        }
+      }
+      nk += __popc(kb);
+      put_mask_word<DT>(X, mrow, kb, id0);
+      if (__any_sync(0xffffffffu, cm != 0u)) list_append(X, r, id0, cm);
+    }
+    const float ws = warp_sum(cs);
+    if (lane == 0) X.sh->cmass[c][warp] = ws;
+    warp_release(X, c);
+  }
+  BandOut o;
+  o.above_n = bsum_i(nk, X.sh->ri[0]);
+  o.above_q = bsum_q(aq, X.sh->rq[1]);
+  return o;
+}
+
+// ---------------------------------------------------------------------------
+// Descent histogram pass over the legal elements whose key has the plen-bit
+// prefix `prefix`: bins of key bits [shift, shift + nbits).  MASS histograms
+// count only S_k members (vK, idK) and also add their fixed-point masses.
+// Elements above the prefix region are summed into above_c / above_m.
+// ---------------------------------------------------------------------------
+template <int DT, bool MASS>
+__device__ __noinline__ void hist_pass(Ctx<DT>& Xr, uint32_t prefix, int plen, int shift, int nbits,
+                                       uint32_t vK, int idK, float nm, uint32_t& above_c,
+                                       uint64_t& above_m) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE, SIG = ElemT<DT>::SIG;
+  const int nb = 1 << nbits;
+  uint32_t* hc = X.lk;
+  uint64_t* hm = reinterpret_cast<uint64_t*>(X.lk + HBINS);
+  __syncthreads();
+  for (int b = threadIdx.x; b < nb; b += NT) {
+    hc[b] = 0u;
+    hm[b] = 0;
+  }
+  const uint32_t lo_key = plen ? (prefix << (SIG - plen)) : 0u;
+  const float lo_val = (plen && lo_key > ElemT<DT>::KLOW) ? key_value<DT>(lo_key) : -INFINITY;
+  uint32_t ac = 0u;
+  uint64_t am = 0;
+  ring_begin(X);
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    const char* stage = warp_wait(X, c);
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, c, vi);
+      if (!(vmax_f<DT>(r) >= lo_val)) continue;  // the whole vector is below the region
+      const int id0 = c * CE + vi * EPV;
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) {
+        const uint32_t b = elem_bits<DT>(r, j);
+        const float x = bits_value<DT>(b);
+        if (!(x > -INFINITY)) continue;
+        const uint32_t k = bits_key<DT>(b);
+        if (MASS && !in_set(k, id0 + j, vK, idK)) continue;
+        const uint32_t top = plen ? (k >> (SIG - plen)) : 0u;
+        if (top < prefix) continue;
+        const uint64_t w = MASS ? fx_weight(x, X.c2, nm) : 1ull;
+        if (top == prefix) {
+          const int d = (int)((k >> shift) & (uint32_t)(nb - 1));
+          atomicAdd(&hc[d], 1u);
+          if (MASS) atomicAdd(reinterpret_cast<unsigned long long*>(&hm[d]), (unsigned long long)w);
+        } else {
+          ++ac;
+          am += w;
+        }
+      }
+    }
+    warp_release(X, c);
+  }
+  above_c = (uint32_t)bsum_i((int)ac, X.sh->ri[0]);
+  above_m = bsum_q(am, X.sh->rq[1]);
+}
+
+// The bin (scanning from the largest digit down) where the running weight,
+// starting at `above`, reaches target.
+struct Cross {
+  int bin, ok;
+  uint64_t before, val;
+  uint32_t cnt;
+};
+template <int DT, bool MASS>
+__device__ __noinline__ Cross hist_cross(Ctx<DT>& Xr, int nbits, uint64_t above, uint64_t target) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const int nb = 1 << nbits;
+  const uint32_t* hc = X.lk;
+  const uint64_t* hm = reinterpret_cast<const uint64_t*>(X.lk + HBINS);
+  const int bpt = nb >= NT ? nb / NT : 1;
+  const int t = threadIdx.x;
+  const int hi = nb - 1 - t * bpt;  // this thread's bins: hi, hi - 1, ..., hi - bpt + 1
+  uint64_t loc = 0;
+  if (hi >= 0)
+    for (int q = 0; q < bpt; ++q) loc += MASS ? hm[hi - q] : (uint64_t)hc[hi - q];
+  uint64_t tot;
+  const uint64_t ex = bscan_excl<uint64_t>(loc, X.sh->rq[0], tot);
+  if (t == 0) X.sh->bi[0] = -1;
+  __syncthreads();
+  if (hi >= 0) {
+    uint64_t cum = above + ex;
+    for (int q = 0; q < bpt; ++q) {
+      const int b = hi - q;
+      const uint64_t v = MASS ? hm[b] : (uint64_t)hc[b];
+      if (v > 0 && cum < target && cum + v >= target) {
+        X.sh->bi[0] = b;
+        X.sh->bq[0] = cum;
+        X.sh->bq[1] = v;
+        X.sh->bu[0] = hc[b];
+      }
+      cum += v;
+    }
+  }
+  __syncthreads();
+  Cross o;
+  o.bin = X.sh->bi[0];
+  o.ok = o.bin >= 0;
+  o.before = X.sh->bq[0];
+  o.val = X.sh->bq[1];
+  o.cnt = X.sh->bu[0];
+  return o;
+}
+
+// Sum of a MASS histogram (the mass of S_k at the first descent level).
+template <int DT>
+__device__ uint64_t hist_total(Ctx<DT>& X, int nbits) {
+  const uint64_t* hm = reinterpret_cast<const uint64_t*>(X.lk + HBINS);
+  uint64_t s = 0;
+  for (int b = threadIdx.x; b < (1 << nbits); b += NT) s += hm[b];
+  return bsum_q(s, X.sh->rq[1]);
+}
+
+// Band pass: every legal element with lo <= key < hi (MASS: every S_k member)
+// goes to the list; legal elements with key >= hi are counted (and, MASS, the
+// S_k members' masses summed).
+template <int DT, bool MASS>
+__device__ __noinline__ void band_pass(Ctx<DT>& Xr, uint32_t lo, uint64_t hi, uint32_t vK, int idK,
+                                       float nm, uint32_t& above_c, uint64_t& above_m) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const float lo_val = (lo > ElemT<DT>::KLOW) ? key_value<DT>(lo) : -INFINITY;
+  if (threadIdx.x == 0) X.sh->n = 0;
+  uint32_t ac = 0u;
+  uint64_t am = 0;
+  ring_begin(X);
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    const char* stage = warp_wait(X, c);
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, c, vi);
+      const int id0 = c * CE + vi * EPV;
+      uint32_t cm = 0u;
+      if (vmax_f<DT>(r) >= lo_val) {
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) {
+          const uint32_t b = elem_bits<DT>(r, j);
+          const float x = bits_value<DT>(b);
+          if (!(x > -INFINITY)) continue;
+          const uint32_t k = bits_key<DT>(b);
+          if ((uint64_t)k >= hi) {
+            ++ac;
+            if (MASS && in_set(k, id0 + j, vK, idK)) am += fx_weight(x, X.c2, nm);
+          } else if (k >= lo && (!MASS || in_set(k, id0 + j, vK, idK))) {
+            cm |= 1u << j;  // a MASS band holds S_k members only, as its histogram
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, cm != 0u)) list_append(X, r, id0, cm);
+    }
+    warp_release(X, c);
+  }
+  above_c = (uint32_t)bsum_i((int)ac, X.sh->ri[0]);
+  above_m = bsum_q(am, X.sh->rq[1]);
+}
+
+// ---------------------------------------------------------------------------
+// Tie pass: id of the rank-th (1-based) legal element, in id order, among
+// those with key v that belong to S_k (vK, idK).
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ int tie_pass(Ctx<DT>& Xr, uint32_t v, int rank, uint32_t vK, int idK) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int c = threadIdx.x; c < X.nch; c += NT) X.sh->ctie[c] = 0;
+  ring_begin(X);
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    const char* stage = warp_wait(X, c);
+    int cnt = 0;
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, c, vi);
+      const int id0 = c * CE + vi * EPV;
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) {
+        const uint32_t b = elem_bits<DT>(r, j);
+        if (!(bits_value<DT>(b) > -INFINITY)) continue;
+        const uint32_t k = bits_key<DT>(b);
+        cnt += (k == v && in_set(k, id0 + j, vK, idK)) ? 1 : 0;
+      }
+    }
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0 && cnt) atomicAdd(&X.sh->ctie[c], cnt);
+    warp_release(X, c);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int cum = 0, cs = -1;
+    for (int c = 0; c < X.nch; ++c) {
+      if (cum + X.sh->ctie[c] >= rank) {
+        cs = c;
+        break;
+      }
+      cum += X.sh->ctie[c];
+    }
+    X.sh->bi[2] = cs;
+    X.sh->bi[3] = rank - cum;
+    X.sh->bi[4] = NOID;
+  }
+  __syncthreads();
+  const int cs = X.sh->bi[2];
+  const int want = X.sh->bi[3];
+  if (cs < 0) return NOID;
+  // rank the ties of chunk cs in element order (warp, it, lane, element)
+  __syncthreads();
+  if (threadIdx.x == 0) issue_chunk(X, cs, cs % NSTAGE);
+  const char* stage = ring_wait(X, cs);
+  int cnt[ITW];
+  uint32_t bits[ITW];
+#pragma unroll
+  for (int it = 0; it < ITW; ++it) {
+    const int vi = warp_vec<DT>(it);
+    const uint4 r = load_vec(X, stage, cs, vi);
+    const int id0 = cs * CE + vi * EPV;
+    uint32_t bb = 0u;
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) {
+      const uint32_t b = elem_bits<DT>(r, j);
+      if (!(bits_value<DT>(b) > -INFINITY)) continue;
+      const uint32_t k = bits_key<DT>(b);
+      if (k == v && in_set(k, id0 + j, vK, idK)) bb |= 1u << j;
+    }
+    bits[it] = bb;
+    cnt[it] = __popc(bb);
+  }
+  int incl[ITW], wt = 0, tw[ITW];
+#pragma unroll
+  for (int it = 0; it < ITW; ++it) {
+    incl[it] = warp_incl_scan(cnt[it]);
+    tw[it] = __shfl_sync(0xffffffffu, incl[it], 31);
+    wt += tw[it];
+  }
+  __syncthreads();
+  if (lane == 0) X.sh->ri[1][warp] = wt;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += X.sh->ri[1][w];
+#pragma unroll
+  for (int it = 0; it < ITW; ++it) {
+    const int b0 = base + incl[it] - cnt[it];
+    if (want > b0 && want <= b0 + cnt[it]) {
+      uint32_t bb = bits[it];
+      for (int q = 1; q < want - b0; ++q) bb &= bb - 1u;
+      X.sh->bi[4] = cs * CE + warp_vec<DT>(it) * EPV + (__ffs(bb) - 1);
+    }
+    base += tw[it];
+  }
+  __syncthreads();
+  return X.sh->bi[4];
+}
+
+// ---------------------------------------------------------------------------
+// Kept pass: the kept set is {legal, key > vF} + {legal, key == vF, id <= idF}.
+// Writes the kept mask, counts the kept elements and records per-(chunk,
+// warp) masses (weights relative to ref: nm = -ref * log2(e) / T).
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ int kept_pass(Ctx<DT>& Xr, uint32_t vF, int idF, float nm) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* mrow = X.a->kept_mask ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
+  const float v_val = (vF >= ElemT<DT>::KLOW) ? key_value<DT>(vF) : -INFINITY;
+  int nk = 0;
+  ring_begin(X);
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    const char* stage = warp_wait(X, c);
+    float cs = 0.f;
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, c, vi);
+      const int id0 = c * CE + vi * EPV;
+      uint32_t kb = 0u;
+      if (vmax_f<DT>(r) >= v_val) {
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) {
+          const uint32_t b = elem_bits<DT>(r, j);
+          const float x = bits_value<DT>(b);
+          if (!(x > -INFINITY)) continue;
+          if (in_set(bits_key<DT>(b), id0 + j, vF, idF)) {
+            kb |= 1u << j;
+            cs += fast_exp2(fmaf(x, X.c2, nm));
+          }
+        }
+      }
+      nk += __popc(kb);
+      put_mask_word<DT>(X, mrow, kb, id0);
+    }
+    const float ws = warp_sum(cs);
+    if (lane == 0) X.sh->cmass[c][warp] = ws;
+    warp_release(X, c);
+  }
+  return bsum_i(nk, X.sh->ri[0]);
+}
+
+// ---------------------------------------------------------------------------
+// Inverse-CDF draw over a kept set recorded per (chunk, warp) cell by
+// kept_pass, band_kept_pass or the keep-all stream (plus, when extra is given,
+// fixed-point masses of kept list entries per cell): T = u * (sum of the cell
+// masses, in order); the cell holding T is re-read and scanned in id order.
+// Returns the token (the last kept element of that cell if rounding leaves T
+// past its end) and the total mass in mtot.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ int sample_tail(Ctx<DT>& Xr, double u, uint32_t vF, int idF, float nm,
+                                        const uint64_t* extra, double& mtot) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nf = X.nch * NWARP;
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) X.sh->bi[5] = -1;
+    __syncwarp();
+    const int per = (nf + 31) / 32;
+    const int f0 = lane * per, f1 = min(nf, f0 + per);
+    double s = 0.0;
+    for (int f = f0; f < f1; ++f) {
+      double v = (double)X.sh->cmass[f / NWARP][f % NWARP];
+      if (extra) v += (double)extra[f] * (1.0 / 1099511627776.0);
+      s += v;
+    }
+    const double inc = warp_incl_scan(s);
+    const double tot = __shfl_sync(0xffffffffu, inc, 31);
+    const double T = u * tot;
+    double cum = inc - s;
+    int hit = -1, last = -1;
+    double before = 0.0;
+    for (int f = f0; f < f1; ++f) {
+      double v = (double)X.sh->cmass[f / NWARP][f % NWARP];
+      if (extra) v += (double)extra[f] * (1.0 / 1099511627776.0);
+      if (hit < 0 && v > 0.0 && cum <= T && cum + v > T) {
+        hit = f;
+        before = cum;
+      }
+      if (v > 0.0) last = f;
+      cum += v;
+    }
+    // the first cell in order holding T; if rounding leaves none, the last
+    // one with mass
+    const uint32_t bal = __ballot_sync(0xffffffffu, hit >= 0);
+    const int lst = (int)__reduce_max_sync(0xffffffffu, (uint32_t)(last + 1)) - 1;
+    if (bal) {
+      const int src = __ffs(bal) - 1;
+      if (lane == src) {
+        X.sh->bi[5] = hit;
+        X.sh->bd[0] = T - before;
+      }
+    } else if (lane == 0) {
+      X.sh->bi[5] = lst;
+      X.sh->bd[0] = 1e300;  // past the end: take the last kept element
+    }
+    if (lane == 0) X.sh->bd[1] = tot;
+  }
+  __syncthreads();
+  mtot = X.sh->bd[1];
+  const int f = X.sh->bi[5];
+  if (f < 0) return -1;
+  const int cs = f / NWARP, ws = f % NWARP;
+  const double Tl = X.sh->bd[0];
+  if (threadIdx.x == 0) issue_chunk(X, cs, cs % NSTAGE);
+  const char* stage = ring_wait(X, cs);
+  if (threadIdx.x == 0) X.sh->bi[6] = -1;
+  __syncthreads();
+  if (warp == ws) {
+    double base = 0.0;
+    int found = -1, lastk = -1;
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, cs, vi);
+      const int id0 = cs * CE + vi * EPV;
+      float w[EPV];
+      float vs = 0.f;
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) {
+        const uint32_t b = elem_bits<DT>(r, j);
+        const float x = bits_value<DT>(b);
+        w[j] = 0.f;
+        if (x > -INFINITY && in_set(bits_key<DT>(b), id0 + j, vF, idF)) {
+          w[j] = fast_exp2(fmaf(x, X.c2, nm));
+          lastk = id0 + j;
+        }
+        vs += w[j];
+      }
+      const double vd = (double)vs;
+      const double inc = warp_incl_scan(vd);
+      const double pre = base + inc - vd;
+      if (found < 0 && vd > 0.0 && pre <= Tl && pre + vd > Tl) {
+        double cum = pre;
+        int tok = -1, lastj = -1;
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) {
+          if (w[j] > 0.f) lastj = id0 + j;
+          cum += (double)w[j];
+          if (tok < 0 && w[j] > 0.f && cum > Tl) tok = id0 + j;
+        }
+        found = tok >= 0 ? tok : lastj;
+      }
+      const int fw = (int)__reduce_min_sync(0xffffffffu, (uint32_t)(found < 0 ? NOID : found));
+      found = (fw == NOID) ? -1 : fw;
+      base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    const int lk = (int)__reduce_max_sync(0xffffffffu, (uint32_t)(lastk + 1)) - 1;
+    if (lane == 0) X.sh->bi[6] = (found >= 0) ? found : lk;
+  }
+  __syncthreads();
+  return X.sh->bi[6];
+}
+
+// Probabilities of a boundary-decided kept set: the contract's weight
+// expf(fl32(x / T) - fl32(ref / T)) over mtot (the kept mass relative to ref)
+// for kept elements, 0 elsewhere.
+template <int DT>
+__device__ __noinline__ void probs_pass(Ctx<DT>& Xr, uint32_t vF, int idF, float zr, double mtot) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  float* prow = X.a->probs + (size_t)X.row * X.V;
+  ring_begin(X);
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    const char* stage = warp_wait(X, c);
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, c, vi);
+      const int id0 = c * CE + vi * EPV;
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) {
+        if (id0 + j >= X.V) break;
+        const uint32_t b = elem_bits<DT>(r, j);
+        const float x = bits_value<DT>(b);
+        float pr = 0.f;
+        if (x > -INFINITY && in_set(bits_key<DT>(b), id0 + j, vF, idF))
+          pr = (float)((double)expf(__fdiv_rn(x, X.temp) - zr) / mtot);
+        prow[id0 + j] = pr;
+      }
+    }
+    warp_release(X, c);
+  }
+}
+
+}  // namespace smp

@@ -1,0 +1,507 @@
+// smp_kernel.cuh -- per-row driver and the kernel entry of the sampler.
+//
+// Per row (contract of the AI Infra KB note M012, sections 02-03):
+//   temperature (0 = greedy argmax) -> legal mask -> top-k (earliest ids win
+//   ties) -> top-p (shortest prefix, value descending then id ascending,
+//   whose mass reaches p) -> renormalise -> inverse-CDF draw in token-id
+//   order with a Philox4x32-10 uniform.
+//
+// Rows are routed by their parameters:
+//   argmax    temperature 0, top_k = 1, or the argmax entry point;
+//   keep-all  top_k >= V and top_p = 1: every legal token is kept;
+//   list      top_k <= KLIST: sigma-truncated candidate list, resolved on chip;
+//   general   everything else, and lists that fail validation: the mass
+//             stream with a list attempt, then the weight-histogram bracket,
+//             then exact radix descent.
+#pragma once
+
+#include "smp_general.cuh"
+
+namespace smp {
+
+// ---------------------------------------------------------------------------
+// Outputs
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ void zero_outputs(Ctx<DT>& X) {
+  const KArgs& a = *X.a;
+  if (a.kept_mask) {
+    uint32_t* m = a.kept_mask + (size_t)X.row * X.W;
+    for (int w = threadIdx.x; w < X.W; w += NT) m[w] = 0u;
+  }
+  if (a.probs && a.mode == MODE_MASK) {
+    float* p = a.probs + (size_t)X.row * X.V;
+    for (int i = threadIdx.x; i < X.V; i += NT) p[i] = 0.f;
+  }
+}
+
+// Status, token, count and diagnostics of the row (one thread writes).
+template <int DT>
+__device__ void put_row(Ctx<DT>& X, int status, int token, int count, int path, int nlist) {
+  const KArgs& a = *X.a;
+  a.status[X.row] = status;
+  if (a.tokens) a.tokens[X.row] = (status == ST_OK) ? token : -1;
+  if (a.kept_count) a.kept_count[X.row] = (status == ST_OK) ? count : 0;
+  if (a.row_info) {
+    int* ri = a.row_info + (size_t)X.row * 4;
+    ri[0] = (status == ST_OK) ? path : PATH_ERROR;
+    ri[1] = nlist;
+  }
+}
+template <int DT>
+__device__ void write_row(Ctx<DT>& X, int status, int token, int count, int path) {
+  if (threadIdx.x == 0) put_row(X, status, token, count, path, X.sh->n);
+}
+
+// Error row; `where` (a source line) goes to the row diagnostics.
+template <int DT>
+__device__ __noinline__ void error_row(Ctx<DT>& Xr, int status, int where = 0) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  __syncthreads();
+  zero_outputs(X);
+  write_row(X, status, -1, 0, PATH_ERROR);
+  if (threadIdx.x == 0 && X.a->row_info) X.a->row_info[(size_t)X.row * 4 + 2] = where;
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Kept set resolved inside the list (the list holds every element of S_p):
+// top-k (K > 0: the K-th entry; K = 0: every entry is in S_k), top-p (target
+// Pq > 0 in fixed point, else p times the S_k mass), count, draw and outputs.
+// Outputs were zeroed beforehand.  Runs on a group of G threads; returns false
+// (nothing written) when the list does not hold the top-p boundary.
+// ---------------------------------------------------------------------------
+template <int G, int DT>
+__device__ bool list_solve(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float m_z, double u,
+                           int path) {
+  const KArgs& a = *X.a;
+  const uint32_t* lk = X.lk;
+  const int* li = X.li;
+  uint32_t vK = 0u;
+  int idK = -1;
+  if (K > 0 && !list_resolve_k<G>(X, n, K, vK, idK)) return false;
+  list_weights<G, DT, false>(X, n, m_z, 0.f, vK, idK);
+  Res R;
+  R.vK = R.vP = vK;
+  R.idK = R.idP = idK;
+  uint64_t mp = 0;
+  if (p < 1.f) {
+    if (!list_resolve_p<G, DT, false>(X, n, Pq, p, m_z, 0.f, R, mp)) return false;
+  } else {
+    const float* wq = list_w(X);
+    uint64_t s = 0;
+    for (int i = gtid<G>(); i < n; i += G) s += to_fx(wq[i]);
+    mp = gsum_q<G>(s, X.sh->rq[1]);
+  }
+  int nk = 0;
+  for (int i = gtid<G>(); i < n; i += G) nk += in_set(lk[i], li[i], R.vP, R.idP) ? 1 : 0;
+  nk = gsum_i<G>(nk, X.sh->ri[0]);
+  int tok = -1;
+  if (a.mode == MODE_SAMPLE) tok = list_draw<G>(X, n, R.vP, R.idP, mp, u);
+  const float* wq = list_w(X);
+  const double inv = 1099511627776.0 / (double)mp;
+  for (int i = gtid<G>(); i < n; i += G) {
+    const int id = li[i];
+    if (!in_set(lk[i], id, R.vP, R.idP)) continue;
+    if (a.kept_mask) atomicOr(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
+    if (a.probs && a.mode == MODE_MASK)
+      a.probs[(size_t)X.row * X.V + id] = (float)((double)wq[i] * inv);
+  }
+  if (gtid<G>() == 0) put_row(X, ST_OK, tok, nk, path, n);
+  return true;
+}
+
+// list_solve on one warp (short lists) or the whole CTA; every thread returns
+// the same verdict.
+template <int DT>
+__device__ __noinline__ bool list_finish(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float m_z,
+                                         double u, int path) {
+  __syncthreads();
+  zero_outputs(X);
+  __syncthreads();
+  bool ok;
+  if (n <= GSMALL) {
+    if (threadIdx.x < 32) {
+      ok = list_solve<32>(X, n, K, p, Pq, m_z, u, path);
+      if (threadIdx.x == 0) X.sh->bi[7] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    ok = X.sh->bi[7] != 0;
+  } else {
+    ok = list_solve<NT>(X, n, K, p, Pq, m_z, u, path);
+  }
+  __syncthreads();
+  return ok;
+}
+
+// ---------------------------------------------------------------------------
+// Kept set decided by a boundary over the whole row: kept pass (mask, count,
+// masses), draw and probabilities.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void finish_by_pass(Ctx<DT>& X, uint32_t vF, int idF, float ref, double u,
+                                            int path) {
+  const KArgs& a = *X.a;
+  const float nm = -ref * X.c2;
+  const int nk = kept_pass(X, vF, idF, nm);
+  double mtot = 0.0;
+  int tok = -1;
+  if (a.mode == MODE_SAMPLE || (a.probs && a.mode == MODE_MASK))
+    tok = sample_tail(X, u, vF, idF, nm, nullptr, mtot);
+  if (a.probs && a.mode == MODE_MASK) probs_pass(X, vF, idF, __fdiv_rn(ref, X.temp), mtot);
+  if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  write_row(X, ST_OK, tok, nk, path);
+  __syncthreads();
+}
+
+// Kept set = {above the bracket} (written by band_kept_pass) + the band list
+// entries in {key > vF} + {key == vF, id <= idF}: their mask bits and
+// per-cell masses are merged, then the draw and probabilities follow.
+template <int DT>
+__device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, uint32_t vF,
+                                         int idF, float m, double u, int path) {
+  const KArgs& a = *X.a;
+  const float nm = -m * X.c2;
+  uint64_t* extra = cell_extra(X);
+  const float* wq = list_w(X);
+  const uint32_t* lk = X.lk;
+  const int* li = X.li;
+  __syncthreads();
+  for (int f = threadIdx.x; f < X.nch * NWARP; f += NT) extra[f] = 0;
+  __syncthreads();
+  int nk = 0;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const int id = li[i];
+    if (!in_set(lk[i], id, vF, idF)) continue;
+    ++nk;
+    if (a.kept_mask) atomicOr(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
+    atomicAdd(reinterpret_cast<unsigned long long*>(&extra[cell_of<DT>(id)]),
+              (unsigned long long)to_fx(wq[i]));
+  }
+  nk = bsum_i(nk, X.sh->ri[1]) + bo.above_n;
+  double mtot = 0.0;
+  int tok = -1;
+  if (a.mode == MODE_SAMPLE || (a.probs && a.mode == MODE_MASK))
+    tok = sample_tail(X, u, vF, idF, nm, extra, mtot);
+  if (a.probs && a.mode == MODE_MASK) probs_pass(X, vF, idF, __fdiv_rn(m, X.temp), mtot);
+  if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  write_row(X, ST_OK, tok, nk, path);
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Radix descent to a boundary.  COUNT (MASS = false): the target-th largest
+// legal element (ties: earliest ids).  MASS: the top-p boundary of S_k (vK,
+// idK) for mass p * M_k, M_k taken from the first histogram.  Returns false if
+// no boundary was found (only possible when a bounded wait gave up mid-pass).
+// ---------------------------------------------------------------------------
+template <int DT, bool MASS>
+__device__ __noinline__ bool descend(Ctx<DT>& X, uint64_t target, float p, uint32_t vK, int idK,
+                                     float m, uint32_t& v_out, int& id_out) {
+  constexpr int SIG = ElemT<DT>::SIG;
+  constexpr int NLV = (SIG == 16) ? 2 : 3;  // digit widths: 11 + 5, or 11 + 11 + 10
+  const float nm = -m * X.c2;
+  uint32_t prefix = 0u;
+  int plen = 0;
+  Cross cr;
+  cr.cnt = 0;
+#pragma unroll 1
+  for (int lv = 0; lv < NLV; ++lv) {
+    const int nbits = (lv == 0) ? HB : ((SIG == 16) ? 5 : (lv == 1 ? HB : 10));
+    const int shift = SIG - plen - nbits;
+    uint32_t ac;
+    uint64_t am;
+    hist_pass<DT, MASS>(X, prefix, plen, shift, nbits, vK, idK, nm, ac, am);
+    if (MASS && lv == 0) {
+      const uint64_t mk = hist_total(X, nbits);
+      target = (uint64_t)ceil((double)p * (double)mk);
+      if (target == 0) target = 1;
+    }
+    cr = hist_cross<DT, MASS>(X, nbits, MASS ? am : (uint64_t)ac, target);
+    if (!cr.ok) return false;
+    prefix = (prefix << nbits) | (uint32_t)cr.bin;
+    plen += nbits;
+    if (cr.cnt <= (uint32_t)CAP) break;
+  }
+  const uint32_t lo = prefix << (SIG - plen);
+  const uint64_t hi = ((uint64_t)prefix + 1u) << (SIG - plen);
+  if (cr.cnt <= (uint32_t)CAP) {
+    uint32_t ac;
+    uint64_t am;
+    band_pass<DT, MASS>(X, lo, hi, vK, idK, nm, ac, am);
+    const int n = min(X.sh->n, CAP);
+    if (!MASS) return list_resolve_k<NT>(X, n, (int)(target - ac), v_out, id_out);
+    list_weights<NT, DT, true>(X, n, 0.f, nm, vK, idK);
+    Res R;
+    R.vK = vK;
+    R.idK = idK;
+    uint64_t km;
+    if (!list_resolve_p<NT, DT, true>(X, n, target - am, 1.f, 0.f, nm, R, km)) return false;
+    v_out = R.vP;
+    id_out = R.idP;
+    return true;
+  }
+  // one value with more than CAP copies
+  v_out = prefix;
+  if (!MASS) {
+    const int keep = (int)(target - cr.before);
+    id_out = (keep < (int)cr.cnt) ? tie_pass(X, prefix, keep, 0u, NOID) : NOID;
+  } else {
+    const uint64_t qv = fx_weight(key_value<DT>(prefix), X.c2, nm);
+    if (qv == 0) return false;
+    const uint64_t j = (target - cr.before + qv - 1) / qv;
+    id_out = (j < (uint64_t)cr.cnt) ? tie_pass(X, prefix, (int)j, vK, idK)
+                                   : ((prefix == vK) ? idK : NOID);
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Row classes
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void row_argmax(Ctx<DT>& X) {
+  const KArgs& a = *X.a;
+  uint32_t bk;
+  int bid, nf = 0;
+  argmax_stream(X, bk, bid, nf);
+  if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  if (nf) return error_row(X, ST_NONFINITE);
+  if (bk == 0u) return error_row(X, ST_EMPTY);
+  zero_outputs(X);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (a.kept_mask) a.kept_mask[(size_t)X.row * X.W + (bid >> 5)] = 1u << (bid & 31);
+    if (a.probs && a.mode == MODE_MASK) a.probs[(size_t)X.row * X.V + bid] = 1.f;
+    put_row(X, ST_OK, bid, 1, PATH_GREEDY, 0);
+  }
+  __syncthreads();
+}
+
+// Mass stream; a second stream with the row maximum as reference when the
+// first chunk's maximum was far below it (weights would overflow).
+template <int DT, bool ALLM>
+__device__ __forceinline__ ExpOut mass_stream(Ctx<DT>& X, float Kt, float vest) {
+  ExpOut E;
+  float ref = __int_as_float(0x7fffffff);
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    E = exp_stream<DT, ALLM, !ALLM>(X, Kt, vest, ref);
+    if (X.sh->timeout || E.nf || E.nleg == 0 || !((E.mx - E.ref) * X.c2 > 100.f)) break;
+    ref = E.mx;
+  }
+  return E;
+}
+
+template <int DT>
+__device__ __noinline__ void row_keepall(Ctx<DT>& X, double u, float vest) {
+  const KArgs& a = *X.a;
+  const ExpOut E = mass_stream<DT, true>(X, 0.f, vest);
+  if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  if (E.nf) return error_row(X, ST_NONFINITE);
+  if (E.nleg == 0) return error_row(X, ST_EMPTY);
+  const float nm = -E.ref * X.c2;
+  double mtot = 0.0;
+  int tok = -1;
+  if (a.mode == MODE_SAMPLE || (a.probs && a.mode == MODE_MASK))
+    tok = sample_tail(X, u, 0u, -1, nm, nullptr, mtot);
+  if (a.probs && a.mode == MODE_MASK) probs_pass(X, 0u, -1, __fdiv_rn(E.ref, X.temp), mtot);
+  if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  write_row(X, ST_OK, tok, E.nleg, PATH_ALL);
+  __syncthreads();
+}
+
+// Returns false when the list does not validate (the row then takes the
+// general path).
+template <int DT>
+__device__ __noinline__ bool row_list(Ctx<DT>& X, int K, float p, double u, float vest) {
+  const bool take_all = vest <= (float)(CAP - CAP / 8);
+  const float Kt = (float)(K + K / 4 + 64);
+  int nf = 0;
+  const uint32_t kmax = list_stream(X, Kt, vest, take_all, nf);
+  if (X.sh->timeout) {
+    error_row(X, ST_TIMEOUT, __LINE__);
+    return true;
+  }
+  const int nl = X.sh->n;
+  if (nl > CAP || (nl < K && !(take_all && nl > 0))) {
+    if (take_all && nl == 0) {
+      error_row(X, nf ? ST_NONFINITE : ST_EMPTY);
+      return true;
+    }
+    return false;
+  }
+  if (nf || kmax >= ElemT<DT>::KPINF) {
+    error_row(X, ST_NONFINITE);
+    return true;
+  }
+  const float m_z = __fdiv_rn(key_value<DT>(kmax), X.temp);
+  if (!list_finish(X, nl, min(K, nl), p, 0, m_z, u, PATH_SIGMA)) error_row(X, ST_TIMEOUT, __LINE__);
+  return true;
+}
+
+template <int DT>
+__device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, float vest) {
+  const int Kt = (K < X.V && K <= (CAP * 3) / 4) ? K + K / 4 + 64 : CAP / 2;
+  const ExpOut E = mass_stream<DT, false>(X, (float)Kt, vest);
+  if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  if (E.nf) return error_row(X, ST_NONFINITE);
+  if (E.nleg == 0) return error_row(X, ST_EMPTY);
+  const float m = E.mx;
+  const float m_z = __fdiv_rn(m, X.temp);
+  const float nm = -m * X.c2;
+  const int keff = min(K, E.nleg);
+  const bool needK = keff < E.nleg;
+  const int n = min(X.sh->n, CAP);
+  const bool list_ok = !E.ovf;
+  // row mass relative to the maximum, fixed point
+  const double zq = E.z * exp2((double)((E.ref - m) * X.c2)) * 1099511627776.0;
+
+  // 1. the whole kept set inside the sigma-truncated list
+  if (list_ok) {
+    if (needK && n >= keff) {
+      if (list_finish(X, n, keff, p, 0, m_z, u, PATH_SIGMA)) return;
+    } else if (!needK) {
+      const uint64_t Pq = (p < 1.f) ? max((uint64_t)1, (uint64_t)ceil((double)p * zq)) : 0;
+      if (p < 1.f && list_finish(X, n, 0, p, Pq, m_z, u, PATH_SIGMA)) return;
+    }
+  }
+  // 2. a weight histogram (relative to the maximum), then one band pass over
+  //    the bracket it gives
+  int b_lo, b_hi;
+  if (!needK && p < 1.f) {
+    whist_pass(X, nm, true);
+    if (wh_bracket(X, true, 0, (double)p * zq / 1099511627776.0, 0.f, b_lo, b_hi)) {
+      const BandOut bo = band_kept_pass(X, b_lo, b_hi, nm, nm);
+      const int nb = min(X.sh->n, CAP);
+      const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));
+      if (X.sh->n <= CAP && Pq > bo.above_q) {
+        list_weights<NT, DT, true>(X, nb, 0.f, nm, 0u, -1);
+        Res R;
+        R.vK = 0u;
+        R.idK = -1;
+        uint64_t km;
+        if (list_resolve_p<NT, DT, true>(X, nb, Pq - bo.above_q, 1.f, 0.f, nm, R, km))
+          return finish_band(X, nb, bo, R.vP, R.idP, m, u, PATH_FULL);
+      }
+    }
+  } else if (needK) {
+    whist_pass(X, nm, false);
+    if (wh_bracket(X, false, keff, 0.0, 0.f, b_lo, b_hi)) {
+      const BandOut bo = band_kept_pass(X, b_lo, b_hi, nm, nm);
+      const int nb = min(X.sh->n, CAP);
+      uint32_t vK;
+      int idK;
+      if (X.sh->n <= CAP && keff > bo.above_n &&
+          list_resolve_k<NT>(X, nb, keff - bo.above_n, vK, idK)) {
+        list_weights<NT, DT, true>(X, nb, 0.f, nm, vK, idK);
+        if (p >= 1.f) return finish_band(X, nb, bo, vK, idK, m, u, PATH_FULL);
+        uint64_t s = 0;
+        const float* wq = list_w(X);
+        for (int i = threadIdx.x; i < nb; i += NT) s += to_fx(wq[i]);
+        const uint64_t mk = bo.above_q + bsum_q(s, X.sh->rq[1]);
+        const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * (double)mk));
+        if (Pq > bo.above_q) {
+          Res R;
+          R.vK = vK;
+          R.idK = idK;
+          uint64_t km;
+          if (list_resolve_p<NT, DT, true>(X, nb, Pq - bo.above_q, 1.f, 0.f, nm, R, km))
+            return finish_band(X, nb, bo, R.vP, R.idP, m, u, PATH_FULL);
+        } else {
+          uint32_t vP;
+          int idP;
+          if (!descend<DT, true>(X, 0, p, vK, idK, m, vP, idP)) return error_row(X, ST_TIMEOUT, __LINE__);
+          return finish_by_pass(X, vP, idP, m, u, PATH_FULL);
+        }
+      }
+    }
+  }
+  // 3. exact radix descent
+  uint32_t vK = 0u;
+  int idK = -1;
+  if (needK && !descend<DT, false>(X, (uint64_t)keff, 1.f, 0u, -1, m, vK, idK))
+    return error_row(X, ST_TIMEOUT, __LINE__);
+  if (p < 1.f) {
+    uint32_t vP;
+    int idP;
+    if (!descend<DT, true>(X, 0, p, vK, idK, m, vP, idP)) return error_row(X, ST_TIMEOUT, __LINE__);
+    return finish_by_pass(X, vP, idP, m, u, PATH_FULL);
+  }
+  return finish_by_pass(X, vK, idK, m, u, PATH_FULL);
+}
+
+// ---------------------------------------------------------------------------
+// One row.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ void process_row(Ctx<DT>& X, int row) {
+  const KArgs& a = *X.a;
+  X.row = row;
+  X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
+  X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
+  __syncthreads();
+  // an expired wait leaves the ring's phases unknown: this CTA streams no more
+  if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+
+  float T = 0.f, p = 1.f;
+  int topk = 1;
+  if (a.mode != MODE_ARGMAX) {
+    T = a.temperature[row];
+    topk = a.top_k[row];
+    p = a.top_p[row];
+    if (!(T >= 0.f) || topk < 1 || !(p > 0.f) || !(p <= 1.f)) return error_row(X, ST_INVALID);
+  }
+  const int K = min(topk, X.V);
+  X.temp = T;
+  // (an infinite temperature keeps a tiny positive slope so that -inf still
+  //  maps to a zero weight)
+  X.c2 = (T > 0.f) ? fmaxf(1.4426950408889634f / T, 1e-30f) : 0.f;
+  if (a.mode == MODE_ARGMAX || T == 0.f || K == 1) return row_argmax(X);
+  const double u = (a.mode == MODE_SAMPLE) ? philox_uniform(a.seed[row], a.offset[row]) : 0.0;
+
+  // legal-count estimate: the bitmask's population, else V
+  float vest = (float)X.V;
+  if (X.bm) {
+    int pc = 0;
+    for (int w = threadIdx.x; w < X.W; w += NT) {
+      uint32_t b = __ldg(X.bm + w);
+      if (w == X.W - 1 && (X.V & 31)) b &= (1u << (X.V & 31)) - 1u;
+      pc += __popc(b);
+    }
+    vest = fmaxf((float)bsum_i(pc, X.sh->ri[1]), 1.f);
+  }
+  if (K >= X.V && p >= 1.f) return row_keepall(X, u, vest);
+  if (K <= KLIST && row_list(X, K, p, u, vest)) return;
+  row_general(X, K, p, u, vest);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(NT, 2) smp_kernel(const __grid_constant__ KArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  char* base = reinterpret_cast<char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  Ctx<DT> X;
+  X.a = &a;
+  X.ring = base;
+  X.lk = reinterpret_cast<uint32_t*>(base + SMEM_RING);
+  X.li = reinterpret_cast<int*>(base + SMEM_RING + CAP * 4);
+  X.wh = reinterpret_cast<uint32_t*>(base + SMEM_RING + SMEM_LIST);
+  X.sh = reinterpret_cast<Sh*>(base + SMEM_RING + SMEM_LIST + SMEM_HIST);
+  X.V = a.V;
+  X.W = a.W;
+  X.nch = (a.V + ElemT<DT>::CE - 1) / ElemT<DT>::CE;
+  X.use_tma = a.use_tma;
+  X.parity = 0u;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&X.sh->full[s], 1);
+    fence_mbar_init();
+    X.sh->timeout = 0;
+    X.sh->n = 0;
+  }
+  __syncthreads();
+  for (int row = blockIdx.x; row < a.B; row += gridDim.x) process_row(X, row);
+}
+
+}  // namespace smp

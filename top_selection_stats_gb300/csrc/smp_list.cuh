@@ -1,0 +1,485 @@
+// smp_list.cuh -- the candidate list: warp-aggregated appends during a pass,
+// radix selection on it (k-th value, tie quota by id, top-p boundary by mass)
+// and the id-order inverse-CDF draw over the kept entries.
+//
+// The list holds, in no particular order, every legal element whose key lies
+// in a band of the rank order.  Order-dependent rules -- earliest ids win
+// ties, the draw scans ids upward -- are evaluated on ids, never on list
+// positions, and every mass is a fixed-point integer, so results do not depend
+// on the append order.
+//
+// The selection runs on a thread group of G threads: one warp (G = 32,
+// warp-synchronous, no block barrier) for lists of up to GSMALL entries, the
+// whole CTA (G = NT) beyond that.
+#pragma once
+
+#include "smp_core.cuh"
+
+namespace smp {
+
+constexpr int GSMALL = 0;  // lists up to this size are resolved by one warp
+
+// After a pass the ring is idle; its bytes hold the list weights and the
+// selection scratch (histogram bins, id-segment masses, the gathered segment
+// of the draw).
+template <int DT>
+__device__ __forceinline__ float* list_w(const Ctx<DT>& X) {
+  return reinterpret_cast<float*>(X.ring);
+}
+template <int DT>
+__device__ __forceinline__ uint64_t* list_scratch(const Ctx<DT>& X) {
+  return reinterpret_cast<uint64_t*>(X.ring + CAP * 4);
+}
+
+__device__ __forceinline__ bool in_set(uint32_t k, int id, uint32_t v, int idv) {
+  return k > v || (k == v && id <= idv);
+}
+
+// Raw bits of element j (0 <= j < EPV, any j) of a vector, without indexing
+// a local array.
+template <int DT>
+__device__ __forceinline__ uint32_t elem_bits_dyn(const uint4 r, int j) {
+  if constexpr (DT == DT_F32) {
+    const uint32_t lo = (j & 1) ? r.y : r.x, hi = (j & 1) ? r.w : r.z;
+    return (j & 2) ? hi : lo;
+  } else {
+    const int q = j >> 1;
+    const uint32_t lo = (q & 1) ? r.y : r.x, hi = (q & 1) ? r.w : r.z;
+    const uint32_t w = (q & 2) ? hi : lo;
+    return (j & 1) ? (w >> 16) : (w & 0xffffu);
+  }
+}
+
+// Appends the elements flagged in cm (bit j = element j of this lane's
+// vector, ids id0 + j).  Called by all lanes of a warp.  Entries past CAP are
+// dropped; sh->n keeps counting, so n > CAP flags the overflow.  Returns the
+// largest key appended by this lane (0 if none).
+template <int DT>
+__device__ __forceinline__ uint32_t list_append(Ctx<DT>& X, const uint4 r, int id0, uint32_t cm) {
+  const int lane = threadIdx.x & 31;
+  const int cnt = __popc(cm);
+  const int inc = warp_incl_scan(cnt);
+  const int tot = __shfl_sync(0xffffffffu, inc, 31);
+  uint32_t kmax = 0u;
+  if (tot == 0) return kmax;
+  int base = 0;
+  if (lane == 31) base = atomicAdd(&X.sh->n, tot);
+  base = __shfl_sync(0xffffffffu, base, 31);
+  int pos = base + inc - cnt;
+  while (cm) {
+    const int j = __ffs(cm) - 1;
+    cm &= cm - 1u;
+    const uint32_t k = bits_key<DT>(elem_bits_dyn<DT>(r, j));
+    kmax = max(kmax, k);
+    if (pos < CAP) {
+      X.lk[pos] = k;
+      X.li[pos] = id0 + j;
+    }
+    ++pos;
+  }
+  return kmax;
+}
+
+// Per-lane append (no warp collective): the elements flagged in cm (bit j =
+// element j of the vector r, ids id0 + j).  Returns the largest key appended.
+template <int DT>
+__device__ __forceinline__ uint32_t lane_append(uint32_t* lk, int* li, int* n, const uint4 r, int id0,
+                                                uint32_t cm) {
+  uint32_t kmax = 0u;
+  int pos = atomicAdd(n, __popc(cm));
+  while (cm) {
+    const int j = __ffs(cm) - 1;
+    cm &= cm - 1u;
+    const uint32_t k = bits_key<DT>(elem_bits_dyn<DT>(r, j));
+    kmax = max(kmax, k);
+    if (pos < CAP) {
+      lk[pos] = k;
+      li[pos] = id0 + j;
+    }
+    ++pos;
+  }
+  return kmax;
+}
+
+// Bits of the elements >= tf; NaN or +inf raises nf.
+template <int DT>
+__device__ __forceinline__ uint32_t ge_bits(const uint4 r, float tf, int& nf) {
+  uint32_t cm = 0u;
+#pragma unroll
+  for (int j = 0; j < ElemT<DT>::EPV; ++j) {
+    const float x = bits_value<DT>(elem_bits<DT>(r, j));
+    if (x >= tf) cm |= 1u << j;
+    if (x != x || x == INFINITY) nf = 1;
+  }
+  return cm;
+}
+
+// ---------------------------------------------------------------------------
+// Thread groups
+// ---------------------------------------------------------------------------
+template <int G>
+__device__ __forceinline__ int gtid() {
+  return G == 32 ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
+}
+template <int G>
+__device__ __forceinline__ void gsync() {
+  if (G == 32) __syncwarp();
+  else __syncthreads();
+}
+template <int G>
+__device__ __forceinline__ uint64_t gsum_q(uint64_t v, uint64_t* s) {
+  if (G == 32) return warp_sum(v);
+  return bsum_q(v, s);
+}
+template <int G>
+__device__ __forceinline__ int gsum_i(int v, int* s) {
+  if (G == 32) return __reduce_add_sync(0xffffffffu, v);
+  return bsum_i(v, s);
+}
+template <int G>
+__device__ __forceinline__ uint32_t gmax_u(uint32_t v, uint32_t* s) {
+  if (G == 32) return __reduce_max_sync(0xffffffffu, v);
+  return bmax_u(v, s);
+}
+template <int G, class T>
+__device__ __forceinline__ T gscan_excl(T v, T* s, T& total) {
+  if (G == 32) {
+    const T inc = warp_incl_scan(v);
+    total = __shfl_sync(0xffffffffu, inc, 31);
+    return inc - v;
+  }
+  return bscan_excl<T>(v, s, total);
+}
+
+// ---------------------------------------------------------------------------
+// Radix selection over list entries, 8-bit digits from the top.
+//   SEL_COUNT : key = entry key, every entry, weight 1
+//   SEL_MASS  : key = entry key, members of S_k, weight = fixed-point mass
+//   SEL_TIEID : key = 2^24 - 1 - id, members of S_k whose key is `at`, weight 1
+// Finds the largest key value v whose weight at-or-above reaches target;
+// above = weight strictly above v, at_w / at_n = weight / count at v.  With
+// p_rel > 0 the target is ceil(p_rel * total weight) (the first round's sum).
+// ---------------------------------------------------------------------------
+enum { SEL_COUNT = 0, SEL_MASS = 1, SEL_TIEID = 2 };
+
+struct SelOut {
+  uint32_t v;
+  uint64_t above, at_w, total, target;
+  int at_n;
+  int ok;
+};
+
+template <int G, int DT, int KIND>
+__device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, float p_rel,
+                                           uint32_t vK, int idK, uint32_t at) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int SIGB = (KIND == SEL_TIEID) ? 24 : ElemT<DT>::SIG;
+  constexpr int ROUNDS = SIGB / 8;
+  uint64_t* bw = list_scratch(X);                                // [2][256] weights
+  uint32_t* bc = reinterpret_cast<uint32_t*>(bw + 512);          // [2][256] counts
+  const float* wq = list_w(X);
+  const int t = gtid<G>();
+  const int lane = threadIdx.x & 31;
+  const bool scanner = (G == 32) || (threadIdx.x < 32);
+  uint32_t prefix = 0u;
+  uint64_t above = 0;
+  SelOut o;
+  o.ok = 1;
+  o.at_w = 0;
+  o.at_n = 0;
+  o.total = 0;
+  gsync<G>();
+  for (int b = t; b < 256; b += G) {
+    bw[b] = 0;
+    bc[b] = 0u;
+  }
+  gsync<G>();
+#pragma unroll 1
+  for (int rd = 0; rd < ROUNDS; ++rd) {
+    const int shift = SIGB - 8 * (rd + 1);
+    uint64_t* w = bw + (rd & 1) * 256;
+    uint32_t* c = bc + (rd & 1) * 256;
+    uint64_t* w2 = bw + ((rd + 1) & 1) * 256;
+    uint32_t* c2 = bc + ((rd + 1) & 1) * 256;
+    for (int b = t; b < 256; b += G) {  // the other buffer, for the next round
+      w2[b] = 0;
+      c2[b] = 0u;
+    }
+#pragma unroll 1
+    for (int i = t; i < n; i += G) {
+      const uint32_t k0 = X.lk[i];
+      const int id = X.li[i];
+      bool f = true;
+      uint32_t key = k0;
+      if constexpr (KIND == SEL_MASS) f = in_set(k0, id, vK, idK);
+      if constexpr (KIND == SEL_TIEID) {
+        f = (k0 == at) && in_set(k0, id, vK, idK);
+        key = 0xffffffu - (uint32_t)id;
+      }
+      if (!f) continue;
+      if (rd > 0 && (key >> (shift + 8)) != prefix) continue;
+      const int d = (key >> shift) & 255;
+      uint64_t wgt = 1;
+      if constexpr (KIND == SEL_MASS) wgt = to_fx(wq[i]);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&w[d]), (unsigned long long)wgt);
+      atomicAdd(&c[d], 1u);
+    }
+    gsync<G>();
+    if (scanner) {
+      // lane l reads digits 255 - 8l ... 248 - 8l (descending)
+      uint64_t v[8];
+      uint64_t loc = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[q] = w[255 - 8 * lane - q];
+        loc += v[q];
+      }
+      const uint64_t inc = warp_incl_scan(loc);
+      const uint64_t tot = __shfl_sync(0xffffffffu, inc, 31);
+      if (rd == 0) {
+        o.total = tot;
+        if (p_rel > 0.f) {
+          target = (uint64_t)ceil((double)p_rel * (double)tot);
+          if (target == 0) target = 1;
+        }
+      }
+      uint64_t cum = above + inc - loc;
+      int hit = -1;
+      uint64_t hb = 0, hv = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (hit < 0 && v[q] > 0 && cum < target && cum + v[q] >= target) {
+          hit = 255 - 8 * lane - q;
+          hb = cum;
+          hv = v[q];
+        }
+        cum += v[q];
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, hit >= 0);
+      const int src = bal ? (__ffs(bal) - 1) : 0;
+      const int d = __shfl_sync(0xffffffffu, hit, src);
+      const uint64_t hb2 = __shfl_sync(0xffffffffu, hb, src);
+      const uint64_t hv2 = __shfl_sync(0xffffffffu, hv, src);
+      if (G == 32) {
+        if (bal == 0u) {
+          o.ok = 0;
+        } else {
+          prefix = (prefix << 8) | (uint32_t)d;
+          above = hb2;
+          o.at_w = hv2;
+          o.at_n = (int)c[d];
+        }
+      } else if (lane == 0) {
+        X.sh->bi[0] = bal ? d : -1;
+        X.sh->bq[0] = hb2;
+        X.sh->bq[1] = hv2;
+        X.sh->bq[2] = tot;
+        X.sh->bq[3] = target;
+        X.sh->bi[1] = bal ? (int)c[d] : 0;
+      }
+    }
+    if (G != 32) {
+      __syncthreads();
+      const int d = X.sh->bi[0];
+      if (d < 0) {
+        o.ok = 0;
+      } else {
+        prefix = (prefix << 8) | (uint32_t)d;
+        above = X.sh->bq[0];
+        o.at_w = X.sh->bq[1];
+        o.at_n = X.sh->bi[1];
+        if (rd == 0) {
+          o.total = X.sh->bq[2];
+          target = X.sh->bq[3];
+        }
+      }
+    }
+    if (!o.ok) break;
+  }
+  o.v = prefix;
+  o.above = above;
+  o.target = target;
+  return o;
+}
+
+// Resolution of a kept set inside a list (targets already net of the part
+// of the row above the list).
+struct Res {
+  uint32_t vK;
+  int idK;  // S_k = {key > vK} + {key == vK, id <= idK}
+  uint32_t vP;
+  int idP;  // S_p = S_k restricted to {key > vP} + {key == vP, id <= idP}
+};
+
+// k-th largest key inside the list (K counted from the top of the list).
+template <int G, int DT>
+__device__ bool list_resolve_k(Ctx<DT>& X, int n, int K, uint32_t& vK, int& idK) {
+  const SelOut s = list_select<G, DT, SEL_COUNT>(X, n, (uint64_t)K, 0.f, 0u, NOID, 0u);
+  if (!s.ok) return false;
+  vK = s.v;
+  const int keep = K - (int)s.above;  // ties at vK kept, earliest ids first
+  idK = NOID;
+  if (keep < s.at_n) {
+    const SelOut ti = list_select<G, DT, SEL_TIEID>(X, n, (uint64_t)keep, 0.f, 0u, NOID, vK);
+    if (!ti.ok) return false;
+    idK = (int)(0xffffffu - ti.v);
+  }
+  return true;
+}
+
+// Weight of a value relative to the row maximum.  Precise: the contract's
+// expf(fl32(x / T) - fl32(max / T)) (m_z = fl32(max / T)).  FAST: the base-2
+// hardware exponential of the row passes (nm = -max * log2(e) / T), so a band
+// list weighs its elements exactly as the pass that chose it.
+template <int DT, bool FAST>
+__device__ __forceinline__ float rel_weight(const Ctx<DT>& X, float x, float m_z, float nm) {
+  if (FAST) return fast_exp2(fmaf(x, X.c2, nm));
+  return expf(__fdiv_rn(x, X.temp) - m_z);
+}
+
+// Weights of the S_k members (others 0) into the list weight array.
+template <int G, int DT, bool FAST>
+__device__ void list_weights(Ctx<DT>& X, int n, float m_z, float nm, uint32_t vK, int idK) {
+  float* wq = list_w(X);
+  const uint32_t* lk = X.lk;
+  const int* li = X.li;
+  const float temp = X.temp, c2 = X.c2;
+  for (int i = gtid<G>(); i < n; i += G) {
+    const uint32_t k = lk[i];
+    float w = 0.f;
+    if (in_set(k, li[i], vK, idK)) {
+      const float x = key_value<DT>(k);
+      w = FAST ? fast_exp2(fmaf(x, c2, nm)) : expf(__fdiv_rn(x, temp) - m_z);
+    }
+    wq[i] = w;
+  }
+  gsync<G>();
+}
+
+// Top-p boundary inside the list: the shortest prefix (value descending, id
+// ascending) of S_k members whose mass reaches the target.  target > 0: that
+// fixed-point mass (net of the mass above the list); otherwise p times the
+// list's S_k mass.  kept_mass receives the mass of S_p inside the list.
+template <int G, int DT, bool FAST>
+__device__ bool list_resolve_p(Ctx<DT>& X, int n, uint64_t target, float p, float m_z, float nm,
+                               Res& R, uint64_t& kept_mass) {
+  const SelOut s = list_select<G, DT, SEL_MASS>(X, n, target, target ? 0.f : p, R.vK, R.idK, 0u);
+  if (!s.ok) return false;
+  R.vP = s.v;
+  const uint64_t qv = to_fx(rel_weight<DT, FAST>(X, key_value<DT>(s.v), m_z, nm));
+  if (qv == 0) return false;
+  const uint64_t need = s.target - s.above;  // > 0 by the selection
+  int j = (int)((need + qv - 1) / qv);
+  if (j > s.at_n) j = s.at_n;
+  R.idP = (s.v == R.vK) ? R.idK : NOID;
+  if (j < s.at_n) {
+    const SelOut ti = list_select<G, DT, SEL_TIEID>(X, n, (uint64_t)j, 0.f, R.vK, R.idK, s.v);
+    if (!ti.ok) return false;
+    R.idP = (int)(0xffffffu - ti.v);
+  }
+  kept_mass = s.above + (uint64_t)j * qv;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Id-order draw over the kept entries {key > vP} + {key == vP, id <= idP}:
+// fixed-point masses summed per id segment (2^sshift ids), the segment holding
+// u * Mp found by a scan, and that segment's kept entries ranked by id.
+// ---------------------------------------------------------------------------
+template <int G, int DT>
+__device__ int list_draw(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, double u) {
+  const float* wq = list_w(X);
+  uint64_t* seg = list_scratch(X);
+  const uint32_t* lk = X.lk;
+  const int* li = X.li;
+  Sh* sh = X.sh;
+  const int t = gtid<G>();
+  int sshift = 8;
+  while (((X.V - 1) >> sshift) + 1 > SEG_MAX) ++sshift;
+  const int nseg = ((X.V - 1) >> sshift) + 1;
+  const double T = u * (double)Mp;
+  gsync<G>();
+  for (int s = t; s < nseg; s += G) seg[s] = 0;
+  gsync<G>();
+  int lastk = -1;
+#pragma unroll 1
+  for (int i = t; i < n; i += G) {
+    const int id = li[i];
+    if (in_set(lk[i], id, vP, idP)) {
+      atomicAdd(reinterpret_cast<unsigned long long*>(&seg[id >> sshift]),
+                (unsigned long long)to_fx(wq[i]));
+      lastk = max(lastk, id);
+    }
+  }
+  const int last = (int)gmax_u<G>((uint32_t)(lastk + 1), sh->ru[0]) - 1;
+  gsync<G>();
+  const int spt = (nseg + G - 1) / G;
+  const int s0 = t * spt, s1 = min(nseg, s0 + spt);
+  uint64_t loc = 0;
+  for (int s = s0; s < s1; ++s) loc += seg[s];
+  uint64_t tot;
+  uint64_t cum = gscan_excl<G, uint64_t>(loc, sh->rq[0], tot);
+  int hit = -1;
+  uint64_t before = 0;
+  for (int s = s0; s < s1; ++s) {
+    const uint64_t v = seg[s];
+    if (hit < 0 && v > 0 && (double)cum <= T && (double)(cum + v) > T) {
+      hit = s;
+      before = cum;
+    }
+    cum += v;
+  }
+  // the (unique) crossing segment
+  int ss;
+  uint64_t bf;
+  if (G == 32) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, hit >= 0);
+    const int src = bal ? __ffs(bal) - 1 : 0;
+    ss = bal ? __shfl_sync(0xffffffffu, hit, src) : -1;
+    bf = __shfl_sync(0xffffffffu, before, src);
+  } else {
+    if (threadIdx.x == 0) sh->bi[0] = -1;
+    __syncthreads();
+    if (hit >= 0) {
+      sh->bi[0] = hit;
+      sh->bq[0] = before;
+    }
+    __syncthreads();
+    ss = sh->bi[0];
+    bf = sh->bq[0];
+  }
+  if (ss < 0) return last;
+  // gather the kept entries of segment ss (the segment sums are no longer needed)
+  gsync<G>();
+  uint64_t* gq = seg;
+  int* gid = reinterpret_cast<int*>(seg + GMAX);
+  if (t == 0) sh->gn = 0;
+  gsync<G>();
+#pragma unroll 1
+  for (int i = t; i < n; i += G) {
+    const int id = li[i];
+    if ((id >> sshift) == ss && in_set(lk[i], id, vP, idP)) {
+      const int slot = atomicAdd(&sh->gn, 1);
+      if (slot < GMAX) {
+        gid[slot] = id;
+        gq[slot] = to_fx(wq[i]);
+      }
+    }
+  }
+  gsync<G>();
+  const int gn = min(sh->gn, GMAX);
+  int tok = -1;
+#pragma unroll 1
+  for (int q = t; q < gn; q += G) {
+    const int my = gid[q];
+    uint64_t pre = bf;
+    for (int r = 0; r < gn; ++r)
+      if (gid[r] < my) pre += gq[r];
+    if (gq[q] > 0 && (double)pre <= T && (double)(pre + gq[q]) > T) tok = my;
+  }
+  tok = (int)gmax_u<G>((uint32_t)(tok + 1), sh->ru[1]) - 1;
+  return tok >= 0 ? tok : last;
+}
+
+}  // namespace smp

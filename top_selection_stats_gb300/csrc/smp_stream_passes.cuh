@@ -1,0 +1,423 @@
+// smp_stream_passes.cuh -- the single-pass row streams of the sampling kernel.
+//
+//   argmax_stream : greedy rows and top-k = 1: packed max test per vector, the
+//                   exact argmax (earliest id) only on vectors that beat the
+//                   warp's running maximum.
+//   list_stream   : top-k rows (k <= KLIST): sigma truncation (Qrita paper
+//                   notes, key design 1) -- a threshold t = mu + delta * sigma
+//                   from the first chunk, one packed compare per vector, and
+//                   the elements >= t appended to the candidate list.
+//   exp_stream    : rows whose kept set can be large: the softmax mass of every
+//                   legal element (base-2 hardware exponential relative to the
+//                   first chunk's maximum), the legal count and the maximum;
+//                   keep-all rows also write the kept mask and per-chunk
+//                   masses; other rows fill a sigma-truncated list and a
+//                   histogram of the weights (WHS bins per factor of two).
+#pragma once
+
+#include "smp_list.cuh"
+
+namespace smp {
+
+// Mean and deviation of the legal finite elements of a staged chunk.
+template <int DT>
+__device__ __forceinline__ void chunk_stats(Ctx<DT>& X, const char* stage, float& mu, float& sd,
+                                         int& cnt) {
+  constexpr int EPV = ElemT<DT>::EPV;
+  float s1 = 0.f, s2 = 0.f, n = 0.f;
+#pragma unroll 1
+  for (int it = 0; it < ITW; ++it) {
+    const uint4 r = load_vec(X, stage, 0, warp_vec<DT>(it));
+    float x[EPV];
+    unpack<DT>(r, x);
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) {
+      if (x[j] > -INFINITY && x[j] < INFINITY) {
+        n += 1.f;
+        s1 += x[j];
+        s2 += x[j] * x[j];
+      }
+    }
+  }
+  n = bsum_f(n, X.sh->rf[0]);
+  s1 = bsum_f(s1, X.sh->rf[1]);
+  s2 = bsum_f(s2, X.sh->rf[2]);
+  cnt = (int)n;
+  mu = n > 0.f ? s1 / n : 0.f;
+  const float var = n > 0.f ? fmaxf(s2 / n - mu * mu, 0.f) : 0.f;
+  sd = sqrtf(var);
+}
+
+// t = mu + delta(q) * sd, delta(q) = Phi^-1(1 - q) interpolated from the host
+// table over log2 q in [-24, 0] (step 1/4).  q >= 1 gives -inf.
+__device__ __forceinline__ float sigma_threshold(const KArgs& a, float mu, float sd, float q) {
+  if (!(q < 1.f)) return -INFINITY;
+  float pos = (log2f(fmaxf(q, 1e-30f)) + 24.f) * 4.f;
+  pos = fminf(fmaxf(pos, 0.f), (float)(DTAB - 1));
+  const int i = min((int)pos, DTAB - 2);
+  const float f = pos - (float)i;
+  const float d = a.delta[i] * (1.f - f) + a.delta[i + 1] * f;
+  return mu + d * sd;
+}
+
+// Threshold packed in the element type (rounded toward -inf) and its exact
+// float value; anything at or below the lowest finite value takes every
+// legal element.
+template <int DT>
+__device__ __forceinline__ void make_threshold(float t, uint32_t& t2, float& tf) {
+  const float low = key_value<DT>(ElemT<DT>::KLOW);
+  if (!(t > low)) t = low;
+  t2 = pack_down<DT>(t);
+  tf = (DT == DT_F32) ? __uint_as_float(t2) : bits_value<DT>(t2 & 0xffffu);
+}
+
+// Threshold of a sigma-truncated list from the staged first chunk.
+template <int DT>
+__device__ __forceinline__ void list_threshold(Ctx<DT>& X, const char* stage, float Kt, float vest,
+                                               uint32_t& t2, float& tf) {
+  float mu, sd;
+  int n1;
+  chunk_stats(X, stage, mu, sd, n1);
+  const float t = (n1 >= 64) ? sigma_threshold(*X.a, mu, sd, Kt / vest) : -INFINITY;
+  make_threshold<DT>(t, t2, tf);
+}
+
+// Vector vi of a staged chunk c with the legal mask applied (no context).
+template <int DT>
+__device__ __forceinline__ uint4 stage_vec(const char* stage, const uint32_t* bm, int W, int c,
+                                           int vi) {
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  uint4 r = reinterpret_cast<const uint4*>(stage)[vi];
+  if (bm) {
+    const int e = c * CE + vi * EPV;
+    const int w = e >> 5;
+    const uint32_t lb = (w < W) ? (__ldg(bm + w) >> (e & 31)) & ((1u << EPV) - 1u) : 0u;
+    if (lb != (1u << EPV) - 1u) r = apply_mask<DT>(r, lb);
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Argmax over the legal finite elements: (largest key, earliest id).
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void argmax_stream(Ctx<DT>& Xr, uint32_t& best_key, int& best_id, int& nf) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const int v0 = warp_vec<DT>(0);
+  uint32_t wkey = 0u;
+  int wid = NOID;
+  float runf = -INFINITY;
+  uint32_t run2 = ninf2<DT>();
+  int bad = 0;
+  ring_begin(X);
+  RingIt<DT> R(X);
+#pragma unroll 1
+  while (R.c < X.nch) {
+    const char* stage = R.wait(X);
+    uint4 r[ITW];
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) r[it] = load_vec(X, stage, R.c, v0 + 32 * it);
+    uint32_t hits = 0u;
+    if (R.c == 0) {
+      // seed the warp's running maximum with its first chunk: only vectors
+      // holding that maximum (or NaN) take the exact path
+      float m = -INFINITY;
+#pragma unroll
+      for (int it = 0; it < ITW; ++it) m = fmaxf(m, vmax_nan_f<DT>(r[it]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (m > -INFINITY) {
+        runf = nextafterf(m, -INFINITY);  // elements >= m pass the strict test
+        run2 = pack_down<DT>(runf);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) hits |= any_gt<DT>(r[it], run2, runf) ? (1u << it) : 0u;
+    if (__any_sync(0xffffffffu, hits != 0u)) {
+      uint32_t lk = 0u;
+      int lid = NOID;
+#pragma unroll 1
+      for (int it = 0; it < ITW; ++it) {
+        if (!((hits >> it) & 1u)) continue;
+        const int vi = v0 + 32 * it;
+        const uint4 rv = load_vec(X, stage, R.c, vi);
+        const int id0 = R.c * CE + vi * EPV;
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) {
+          const uint32_t b = elem_bits<DT>(rv, j);
+          const float x = bits_value<DT>(b);
+          if (x != x || x == INFINITY) {
+            bad = 1;
+          } else if (x > runf) {
+            const uint32_t k = bits_key<DT>(b);
+            if (k > lk) {
+              lk = k;
+              lid = id0 + j;
+            }
+          }
+        }
+      }
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, lk);
+      if (mk > wkey) {
+        wid = (int)__reduce_min_sync(0xffffffffu, (uint32_t)((lk == mk) ? lid : NOID));
+        wkey = mk;
+        runf = key_value<DT>(mk);
+        run2 = pack_down<DT>(runf);
+      }
+    }
+    R.release(X);
+  }
+  best_key = bmax_u(wkey, X.sh->ru[0]);
+  best_id = (int)bmin_u((uint32_t)((wkey == best_key) ? wid : NOID), X.sh->ru[1]);
+  nf = bsum_i(bad, X.sh->ri[0]);
+}
+
+// ---------------------------------------------------------------------------
+// Sigma-truncated list.  Kt is the number of candidates aimed at; take_all
+// puts every legal element in the list.  Once the list overflows the rest of
+// the row is only drained.  Returns the largest key appended (0: none); nf
+// counts NaN / +inf seen in legal slots.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ uint32_t list_stream(Ctx<DT>& Xr, float Kt, float vest, bool take_all,
+                                             int& nf) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  if (threadIdx.x == 0) X.sh->n = 0;
+  const int v0 = warp_vec<DT>(0);
+  uint32_t t2;
+  float tf;
+  make_threshold<DT>(-INFINITY, t2, tf);
+  uint32_t kmax = 0u;
+  int bad = 0;
+  ring_begin(X);
+  RingIt<DT> R(X);
+#pragma unroll 1
+  while (R.c < X.nch) {
+    const char* stage = R.wait(X);
+    if (R.c == 0 && !take_all) list_threshold(X, stage, Kt, vest, t2, tf);
+    uint4 r[ITW];
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) r[it] = load_vec(X, stage, R.c, v0 + 32 * it);
+    uint32_t hits = 0u;
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) hits |= any_ge<DT>(r[it], t2, tf) ? (1u << it) : 0u;
+    // once the list overflowed the row falls back: the pass only drains
+    if (hits && X.sh->n <= CAP) {
+#pragma unroll 1
+      for (int it = 0; it < ITW; ++it) {
+        if (!((hits >> it) & 1u)) continue;
+        const int vi = v0 + 32 * it;
+        const uint4 rv = load_vec(X, stage, R.c, vi);
+        const uint32_t cm = ge_bits<DT>(rv, tf, bad);
+        if (cm) kmax = max(kmax, lane_append<DT>(X.lk, X.li, &X.sh->n, rv, R.c * CE + vi * EPV, cm));
+      }
+    }
+    R.release(X);
+  }
+  nf = bsum_i(bad, X.sh->ri[0]);
+  return bmax_u(kmax, X.sh->ru[0]);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax-mass stream.  Weights 2^((x - ref) * log2(e) / T) with ref the first
+// chunk's maximum (or ref_in when given).  ALLM (keep-all rows): kept mask
+// words written on the fly, per-chunk per-warp masses in sh->cmass.  EMIT: a
+// sigma-truncated list with Kt candidates aimed at.  The maximum, the NaN /
+// +inf flag and the -inf test ride on packed extrema accumulated per thread.
+// ---------------------------------------------------------------------------
+struct ExpOut {
+  double z;    // sum of weights (relative to ref)
+  float ref;   // reference value
+  float mx;    // maximum legal value
+  int nleg;    // legal finite count
+  int nf;      // NaN / +inf seen
+  int ovf;     // list overflow (EMIT)
+};
+
+// Sum of the EPV weights of a vector: a tree (short dependency chains).
+template <int EPV>
+__device__ __forceinline__ float tree_sum(const float (&w)[EPV]) {
+  if constexpr (EPV == 8) {
+    return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+  } else {
+    return (w[0] + w[1]) + (w[2] + w[3]);
+  }
+}
+
+template <int DT, bool ALLM, bool EMIT>
+__device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, float ref_in) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  constexpr uint32_t FULLB = (1u << EPV) - 1u;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int v0 = warp_vec<DT>(0);
+  uint32_t* mrow = (ALLM && X.a->kept_mask) ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
+  if (threadIdx.x == 0) X.sh->n = 0;
+  uint32_t t2 = p_pinf<DT>();
+  float tf = INFINITY;
+  float ref = ref_in, nref = 0.f;
+  const float c2 = X.c2;
+  double tz = 0.0;
+  uint32_t amax = p_ninf<DT>();
+  int nleg = 0;
+  ring_begin(X);
+  RingIt<DT> R(X);
+#pragma unroll 1
+  while (R.c < X.nch) {
+    const int c = R.c;
+    const char* stage = R.wait(X);
+    if (c == 0) {
+      if (ref_in != ref_in) {  // reference = the first chunk's maximum
+        float m = -INFINITY;
+#pragma unroll 1
+        for (int it = 0; it < ITW; ++it) {
+          float x[EPV];
+          unpack<DT>(load_vec(X, stage, 0, v0 + 32 * it), x);
+#pragma unroll
+          for (int j = 0; j < EPV; ++j)
+            if (x[j] < INFINITY) m = fmaxf(m, x[j]);
+        }
+        ref = bmax_f(m, X.sh->rf[0]);
+        if (!(ref > -INFINITY)) ref = 0.f;
+      }
+      nref = -ref * c2;
+      if (EMIT) list_threshold(X, stage, Kt, vest, t2, tf);
+    }
+    float cs = 0.f;
+    uint32_t hits = 0u, cmin = p_pinf<DT>();
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) {
+      const uint4 r = load_vec(X, stage, c, v0 + 32 * it);
+      const uint32_t m2 = vmax2<DT>(r);
+      amax = pmax<DT>(amax, m2);
+      cmin = pmin<DT>(cmin, vmin2<DT>(r));
+      if (EMIT && p_any_ge<DT>(m2, t2, tf)) hits |= 1u << it;
+      float x[EPV], w[EPV];
+      unpack<DT>(r, x);
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) w[j] = fast_exp2(fmaf(x[j], c2, nref));  // -inf -> 0
+      cs += tree_sum<EPV>(w);
+    }
+    // legal count and kept-mask words: every slot legal unless the chunk
+    // holds -inf somewhere in this warp
+    const bool neg = !(p2f_min<DT>(cmin) > -INFINITY);
+    if (!__any_sync(0xffffffffu, neg)) {
+      nleg += EPV * ITW;
+      if (ALLM && mrow) {
+#pragma unroll
+        for (int it = 0; it < ITW; ++it) {
+          const int wi = (c * CE + (v0 + 32 * it) * EPV) >> 5;
+          if ((lane & (32 / EPV - 1)) == 0 && wi < X.W) mrow[wi] = 0xffffffffu;
+        }
+      }
+    } else {
+#pragma unroll 1
+      for (int it = 0; it < ITW; ++it) {
+        const int vi = v0 + 32 * it;
+        uint32_t kb = FULLB;
+        if (neg) {
+          float x[EPV];
+          unpack<DT>(load_vec(X, stage, c, vi), x);
+          kb = 0u;
+#pragma unroll
+          for (int j = 0; j < EPV; ++j)
+            if (x[j] > -INFINITY) kb |= 1u << j;
+        }
+        nleg += __popc(kb);
+        if (ALLM && mrow) {
+          uint32_t wv;
+          int wi;
+          if constexpr (EPV == 8) {
+            wv = kb << (8 * (lane & 3));
+            wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+            wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+            wi = ((lane & 3) == 0) ? ((c * CE + vi * EPV) >> 5) : -1;
+          } else {
+            wv = kb << (4 * (lane & 7));
+            wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+            wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+            wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
+            wi = ((lane & 7) == 0) ? ((c * CE + vi * EPV) >> 5) : -1;
+          }
+          if (wi >= 0 && wi < X.W) mrow[wi] = wv;
+        }
+      }
+    }
+    if (EMIT && hits && X.sh->n <= CAP) {
+      int dummy = 0;
+#pragma unroll 1
+      for (int it = 0; it < ITW; ++it) {
+        if (!((hits >> it) & 1u)) continue;
+        const int vi = v0 + 32 * it;
+        const uint4 rv = load_vec(X, stage, c, vi);
+        const uint32_t cm = ge_bits<DT>(rv, tf, dummy);
+        if (cm) lane_append<DT>(X.lk, X.li, &X.sh->n, rv, c * CE + vi * EPV, cm);
+      }
+    }
+    tz += (double)cs;
+    if (ALLM) {
+      const float ws = warp_sum(cs);
+      if (lane == 0) X.sh->cmass[c][warp] = ws;
+    }
+    R.release(X);
+  }
+  const float tmax = p2f_max<DT>(amax);
+  ExpOut o;
+  o.z = bsum_d(tz, X.sh->rd[0]);
+  o.ref = ref;
+  o.nf = bsum_i((tmax < INFINITY) ? 0 : 1, X.sh->ri[1]);  // NaN or +inf in a legal slot
+  o.mx = bmax_f(o.nf ? -INFINITY : tmax, X.sh->rf[0]);
+  o.nleg = bsum_i(nleg, X.sh->ri[0]);
+  o.ovf = X.sh->n > CAP;
+  return o;
+}
+
+// ---------------------------------------------------------------------------
+// Weight-histogram pass: legal elements binned by a = (x - m) * log2(e) / T
+// (nm = -m * log2(e) / T), WHS bins per factor of two.  hmass: each element
+// adds 2^11 * 2^f, f = (1 - frac(y)) / WHS its weight's excess over the bin's
+// lower edge (2^f by its quadratic expansion, error < 2e-5); else 1.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void whist_pass(Ctx<DT>& Xr, float nm, bool hmass) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV;
+  uint32_t* wh = X.wh;
+  for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
+  const int v0 = warp_vec<DT>(0);
+  const float c2 = X.c2;
+  ring_begin(X);
+  RingIt<DT> R(X);
+#pragma unroll 1
+  while (R.c < X.nch) {
+    const char* stage = R.wait(X);
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      float x[EPV];
+      unpack<DT>(load_vec(X, stage, R.c, v0 + 32 * it), x);
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) {
+        if (!(x[j] > -INFINITY)) continue;
+        const float y = fmaf(fmaf(x[j], c2, nm), -(float)WHS, (float)WHOFF);
+        const float fy = floorf(y);
+        const int b = min(max((int)fy, 0), WBINS - 1);
+        uint32_t add = 1u;
+        if (hmass) {
+          const float f = (b == (int)fy) ? (1.f - (y - fy)) * (1.f / WHS) : 0.f;
+          add = (uint32_t)fmaf(f, fmaf(f, 491.96f, 1419.57f), 2048.5f);
+        }
+        atomicAdd(&wh[b], add);
+      }
+    }
+    R.release(X);
+  }
+  __syncthreads();
+}
+
+}  // namespace smp
