@@ -100,36 +100,36 @@ __device__ __noinline__ bool wh_bracket(Ctx<DT>& Xr, bool pmode, int K, double P
   const uint32_t* wh = X.wh;
   constexpr int BPT = WBINS / NT;
   const int t = threadIdx.x;
-  double v[BPT];
-  double s = 0.0;
+  float v[BPT];
+  float s = 0.f;
 #pragma unroll
   for (int q = 0; q < BPT; ++q) {
     const int b = t * BPT + q;
     // P mode: wh[b] / 2^11 counts the bin's elements in units of its lower
     // edge weight 2^((WHOFF - b - 1) / WHS); the clamped end bins are bounded
     // by amax above and 0 below
-    v[q] = (double)wh[b];
+    v[q] = (float)wh[b];
     if (pmode) {
-      const double lo_w = (b == WBINS - 1) ? 0.0 : exp2((double)(WHOFF - b - 1) / WHS);
-      v[q] = (b == 0) ? v[q] / 2048.0 * exp2((double)fmaxf(amax, (float)WHOFF / WHS))
-                      : v[q] / 2048.0 * lo_w;
+      const float lo_w = (b == WBINS - 1) ? 0.f : exp2f((float)(WHOFF - b - 1) * (1.f / WHS));
+      v[q] = (b == 0) ? v[q] * (1.f / 2048.f) * exp2f(fmaxf(amax, (float)WHOFF / WHS))
+                      : v[q] * (1.f / 2048.f) * lo_w;
     }
     s += v[q];
   }
-  double tot;
-  double cum = bscan_excl<double>(s, X.sh->rd[0], tot);
+  float tot;
+  float cum = bscan_excl<float>(s, X.sh->rf[0], tot);
   if (t == 0) {
     X.sh->bi[0] = WBINS;
     X.sh->bi[1] = -1;
   }
   __syncthreads();
-  const double lo_t = pmode ? PZ * (1.0 - 1e-3) : (double)K;
-  const double hi_t = pmode ? PZ * (1.0 + 1e-3) : (double)K;
+  const float lo_t = pmode ? (float)(PZ * (1.0 - 1e-3)) : (float)K;
+  const float hi_t = pmode ? (float)(PZ * (1.0 + 1e-3)) : (float)K;
 #pragma unroll
   for (int q = 0; q < BPT; ++q) {
     const int b = t * BPT + q;
-    if (v[q] > 0.0 && cum + v[q] >= lo_t) atomicMin(&X.sh->bi[0], b);
-    if (v[q] > 0.0 && cum < hi_t) atomicMax(&X.sh->bi[1], b);
+    if (v[q] > 0.f && cum + v[q] >= lo_t) atomicMin(&X.sh->bi[0], b);
+    if (v[q] > 0.f && cum < hi_t) atomicMax(&X.sh->bi[1], b);
     cum += v[q];
   }
   __syncthreads();
@@ -139,15 +139,14 @@ __device__ __noinline__ bool wh_bracket(Ctx<DT>& Xr, bool pmode, int K, double P
     __syncthreads();
     return false;
   }
-  double n = 0.0;
+  int n = 0;
 #pragma unroll
   for (int q = 0; q < BPT; ++q) {
     const int b = t * BPT + q;
-    if (b >= b_lo && b <= b_hi) n += pmode ? (double)wh[b] / 2048.0 : v[q];
+    if (b >= b_lo && b <= b_hi) n += pmode ? (int)(wh[b] >> 11) + 1 : (int)wh[b];
   }
-  n = bsum_d(n, X.sh->rd[1]);
-  (void)amax;
-  return n <= (double)CAP;
+  n = bsum_i(n, X.sh->ri[1]);
+  return n <= CAP;
 }
 
 // ---------------------------------------------------------------------------
@@ -159,7 +158,7 @@ __device__ __noinline__ bool wh_bracket(Ctx<DT>& Xr, bool pmode, int K, double P
 // ---------------------------------------------------------------------------
 struct BandOut {
   int above_n;
-  uint64_t above_q;
+  uint64_t above_q;  // fixed-point mass above the bracket (from the per-cell sums)
 };
 template <int DT>
 __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, float nref, float nm) {
@@ -171,7 +170,7 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
   const float c2 = X.c2;
   if (threadIdx.x == 0) X.sh->n = 0;
   int nk = 0;
-  uint64_t aq = 0;
+  double ta = 0.0;
   ring_begin(X);
 #pragma unroll 1
   for (int c = 0; c < X.nch; ++c) {
@@ -191,9 +190,7 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
         const int b = wbin(x[j], c2, nref);
         if (b < b_lo) {
           kb |= 1u << j;
-          const float w = fast_exp2(fmaf(x[j], c2, nm));
-          cs += w;
-          aq += to_fx(w);
+          cs += fast_exp2(fmaf(x[j], c2, nm));
         } else if (b <= b_hi) {
           cm |= 1u << j;
         }
@@ -204,11 +201,12 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
     }
     const float ws = warp_sum(cs);
     if (lane == 0) X.sh->cmass[c][warp] = ws;
+    ta += (double)cs;
     warp_release(X, c);
   }
   BandOut o;
   o.above_n = bsum_i(nk, X.sh->ri[0]);
-  o.above_q = bsum_q(aq, X.sh->rq[1]);
+  o.above_q = (uint64_t)(bsum_d(ta, X.sh->rd[0]) * 1099511627776.0);
   return o;
 }
 

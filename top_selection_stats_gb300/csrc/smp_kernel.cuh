@@ -117,7 +117,7 @@ __device__ bool list_solve(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float
 template <int DT>
 __device__ __noinline__ bool list_finish(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float m_z,
                                          double u, int path) {
-  __syncthreads();
+  list_range(X, n);
   zero_outputs(X);
   __syncthreads();
   bool ok;
@@ -231,6 +231,7 @@ __device__ __noinline__ bool descend(Ctx<DT>& X, uint64_t target, float p, uint3
     uint64_t am;
     band_pass<DT, MASS>(X, lo, hi, vK, idK, nm, ac, am);
     const int n = min(X.sh->n, CAP);
+    list_range(X, n);
     if (!MASS) return list_resolve_k<NT>(X, n, (int)(target - ac), v_out, id_out);
     list_weights<NT, DT, true>(X, n, 0.f, nm, vK, idK);
     Res R;
@@ -343,7 +344,10 @@ __device__ __noinline__ bool row_list(Ctx<DT>& X, int K, float p, double u, floa
 
 template <int DT>
 __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, float vest) {
-  const int Kt = (K < X.V && K <= (CAP * 3) / 4) ? K + K / 4 + 64 : CAP / 2;
+  // list target: the top-k set plus margin, or (no top-k boundary expected)
+  // 512 -- top-p sets are short unless the row is flat, and flat rows take
+  // the histogram bracket anyway
+  const int Kt = (K < X.V && (float)K < vest && K <= (CAP * 3) / 4) ? K + K / 4 + 64 : 512;
   const ExpOut E = mass_stream<DT, false>(X, (float)Kt, vest);
   if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
   if (E.nf) return error_row(X, ST_NONFINITE);
@@ -362,9 +366,10 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
   if (list_ok) {
     if (needK && n >= keff) {
       if (list_finish(X, n, keff, p, 0, m_z, u, PATH_SIGMA)) return;
-    } else if (!needK) {
-      const uint64_t Pq = (p < 1.f) ? max((uint64_t)1, (uint64_t)ceil((double)p * zq)) : 0;
-      if (p < 1.f && list_finish(X, n, 0, p, Pq, m_z, u, PATH_SIGMA)) return;
+    } else if (!needK && p < 1.f && E.lmass >= (double)p * E.z * (1.0 - 1e-4)) {
+      // the list (a rank prefix of the legal set) carries p of the row's mass
+      const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));
+      if (list_finish(X, n, 0, p, Pq, m_z, u, PATH_SIGMA)) return;
     }
   }
   // 2. a weight histogram (relative to the maximum), then one band pass over
@@ -375,6 +380,7 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
     if (wh_bracket(X, true, 0, (double)p * zq / 1099511627776.0, 0.f, b_lo, b_hi)) {
       const BandOut bo = band_kept_pass(X, b_lo, b_hi, nm, nm);
       const int nb = min(X.sh->n, CAP);
+      list_range(X, nb);
       const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));
       if (X.sh->n <= CAP && Pq > bo.above_q) {
         list_weights<NT, DT, true>(X, nb, 0.f, nm, 0u, -1);
@@ -391,6 +397,7 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
     if (wh_bracket(X, false, keff, 0.0, 0.f, b_lo, b_hi)) {
       const BandOut bo = band_kept_pass(X, b_lo, b_hi, nm, nm);
       const int nb = min(X.sh->n, CAP);
+      list_range(X, nb);
       uint32_t vK;
       int idK;
       if (X.sh->n <= CAP && keff > bo.above_n &&

@@ -101,6 +101,35 @@ __device__ __forceinline__ uint32_t lane_append(uint32_t* lk, int* li, int* n, c
   return kmax;
 }
 
+// Bits of the elements >= t (packed compares; NaN compares false); a NaN in
+// the vector raises nf (+inf is kept and caught by the list's largest key).
+template <int DT>
+__device__ __forceinline__ uint32_t ge_mask(const uint4 r, uint32_t t2, float tf, int& nf) {
+  if constexpr (DT == DT_F32) {
+    const float a = __uint_as_float(r.x), b = __uint_as_float(r.y), c = __uint_as_float(r.z),
+                d = __uint_as_float(r.w);
+    if (a != a || b != b || c != c || d != d) nf = 1;
+    return (a >= tf ? 1u : 0u) | (b >= tf ? 2u : 0u) | (c >= tf ? 4u : 0u) | (d >= tf ? 8u : 0u);
+  } else {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    uint32_t cm = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t m;
+      if constexpr (DT == DT_BF16)
+        m = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[q]),
+                        *reinterpret_cast<const __nv_bfloat162*>(&t2));
+      else
+        m = __hge2_mask(*reinterpret_cast<const __half2*>(&w[q]),
+                        *reinterpret_cast<const __half2*>(&t2));
+      cm |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * q);
+    }
+    const float mx = p2f_max<DT>(vmax2<DT>(r));
+    if (mx != mx) nf = 1;
+    return cm;
+  }
+}
+
 // Bits of the elements >= tf; NaN or +inf raises nf.
 template <int DT>
 __device__ __forceinline__ uint32_t ge_bits(const uint4 r, float tf, int& nf) {
@@ -174,8 +203,12 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
                                            uint32_t vK, int idK, uint32_t at) {
   LocalCtx<DT> lc_(Xr);
   Ctx<DT>& X = lc_.v;
-  constexpr int SIGB = (KIND == SEL_TIEID) ? 24 : ElemT<DT>::SIG;
-  constexpr int ROUNDS = SIGB / 8;
+  // Digits are taken over the list's own key range [kbase, kbase + 2^SIGB):
+  // the keys of a candidate list cluster, and digits of the full key width
+  // would pile them onto a few bins (serialised shared atomics).
+  const uint32_t kbase = (KIND == SEL_TIEID) ? 0u : X.sh->bu[4];
+  const int SIGB = (KIND == SEL_TIEID) ? 24 : max(8, 32 - __clz((int)(X.sh->bu[5] - kbase)));
+  const int ROUNDS = (SIGB + 7) / 8;
   uint64_t* bw = list_scratch(X);                                // [2][256] weights
   uint32_t* bc = reinterpret_cast<uint32_t*>(bw + 512);          // [2][256] counts
   const float* wq = list_w(X);
@@ -197,7 +230,11 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
   gsync<G>();
 #pragma unroll 1
   for (int rd = 0; rd < ROUNDS; ++rd) {
-    const int shift = SIGB - 8 * (rd + 1);
+    const int shift = max(SIGB - 8 * (rd + 1), 0);  // = SIGB - 8 rd - wr
+    // round rd takes the next wr bits below the prefix (the last round the
+    // remaining low bits)
+    const int wr = min(8, SIGB - 8 * rd);
+    const uint32_t dmask = (1u << wr) - 1u;
     uint64_t* w = bw + (rd & 1) * 256;
     uint32_t* c = bc + (rd & 1) * 256;
     uint64_t* w2 = bw + ((rd + 1) & 1) * 256;
@@ -211,15 +248,15 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
       const uint32_t k0 = X.lk[i];
       const int id = X.li[i];
       bool f = true;
-      uint32_t key = k0;
+      uint32_t key = k0 - kbase;
       if constexpr (KIND == SEL_MASS) f = in_set(k0, id, vK, idK);
       if constexpr (KIND == SEL_TIEID) {
         f = (k0 == at) && in_set(k0, id, vK, idK);
         key = 0xffffffu - (uint32_t)id;
       }
       if (!f) continue;
-      if (rd > 0 && (key >> (shift + 8)) != prefix) continue;
-      const int d = (key >> shift) & 255;
+      if (rd > 0 && (key >> (shift + wr)) != prefix) continue;
+      const int d = (key >> shift) & dmask;
       uint64_t wgt = 1;
       if constexpr (KIND == SEL_MASS) wgt = to_fx(wq[i]);
       atomicAdd(reinterpret_cast<unsigned long long*>(&w[d]), (unsigned long long)wgt);
@@ -265,7 +302,7 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
         if (bal == 0u) {
           o.ok = 0;
         } else {
-          prefix = (prefix << 8) | (uint32_t)d;
+          prefix = (prefix << wr) | (uint32_t)d;
           above = hb2;
           o.at_w = hv2;
           o.at_n = (int)c[d];
@@ -285,7 +322,7 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
       if (d < 0) {
         o.ok = 0;
       } else {
-        prefix = (prefix << 8) | (uint32_t)d;
+        prefix = (prefix << wr) | (uint32_t)d;
         above = X.sh->bq[0];
         o.at_w = X.sh->bq[1];
         o.at_n = X.sh->bi[1];
@@ -297,10 +334,31 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
     }
     if (!o.ok) break;
   }
-  o.v = prefix;
+  o.v = (KIND == SEL_TIEID) ? prefix : prefix + kbase;
   o.above = above;
   o.target = target;
   return o;
+}
+
+// Key range of the list entries (sh->bu[4], sh->bu[5]): the radix digits of
+// list_select are taken inside it.  All threads of the CTA call it.
+template <int DT>
+__device__ __noinline__ void list_range(Ctx<DT>& Xr, int n) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t k = X.lk[i];
+    lo = min(lo, k);
+    hi = max(hi, k);
+  }
+  lo = bmin_u(lo, X.sh->ru[0]);
+  hi = bmax_u(hi, X.sh->ru[1]);
+  if (threadIdx.x == 0) {
+    X.sh->bu[4] = (n > 0) ? lo : 0u;
+    X.sh->bu[5] = (n > 0) ? hi : 0u;
+  }
+  __syncthreads();
 }
 
 // Resolution of a kept set inside a list (targets already net of the part

@@ -212,7 +212,7 @@ __device__ __noinline__ uint32_t list_stream(Ctx<DT>& Xr, float Kt, float vest, 
         if (!((hits >> it) & 1u)) continue;
         const int vi = v0 + 32 * it;
         const uint4 rv = load_vec(X, stage, R.c, vi);
-        const uint32_t cm = ge_bits<DT>(rv, tf, bad);
+        const uint32_t cm = ge_mask<DT>(rv, t2, tf, bad);
         if (cm) kmax = max(kmax, lane_append<DT>(X.lk, X.li, &X.sh->n, rv, R.c * CE + vi * EPV, cm));
       }
     }
@@ -236,6 +236,7 @@ struct ExpOut {
   int nleg;    // legal finite count
   int nf;      // NaN / +inf seen
   int ovf;     // list overflow (EMIT)
+  double lmass;  // mass of the list's elements (EMIT, relative to ref)
 };
 
 // Sum of the EPV weights of a vector: a tree (short dependency chains).
@@ -263,6 +264,7 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   float ref = ref_in, nref = 0.f;
   const float c2 = X.c2;
   double tz = 0.0;
+  float lm = 0.f;
   uint32_t amax = p_ninf<DT>();
   int nleg = 0;
   ring_begin(X);
@@ -355,8 +357,14 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
         if (!((hits >> it) & 1u)) continue;
         const int vi = v0 + 32 * it;
         const uint4 rv = load_vec(X, stage, c, vi);
-        const uint32_t cm = ge_bits<DT>(rv, tf, dummy);
-        if (cm) lane_append<DT>(X.lk, X.li, &X.sh->n, rv, c * CE + vi * EPV, cm);
+        const uint32_t cm = ge_mask<DT>(rv, t2, tf, dummy);
+        if (!cm) continue;
+        lane_append<DT>(X.lk, X.li, &X.sh->n, rv, c * CE + vi * EPV, cm);
+        float x[EPV];
+        unpack<DT>(rv, x);
+#pragma unroll
+        for (int j = 0; j < EPV; ++j)
+          if ((cm >> j) & 1u) lm += fast_exp2(fmaf(x[j], c2, nref));
       }
     }
     tz += (double)cs;
@@ -374,6 +382,7 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   o.mx = bmax_f(o.nf ? -INFINITY : tmax, X.sh->rf[0]);
   o.nleg = bsum_i(nleg, X.sh->ri[0]);
   o.ovf = X.sh->n > CAP;
+  o.lmass = EMIT ? bsum_d((double)lm, X.sh->rd[1]) : 0.0;
   return o;
 }
 
