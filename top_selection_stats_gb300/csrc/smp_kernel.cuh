@@ -86,19 +86,20 @@ __device__ bool list_solve(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float
   R.vK = R.vP = vK;
   R.idK = R.idP = idK;
   uint64_t mp = 0;
+  int nk = 0;
   if (p < 1.f) {
-    if (!list_resolve_p<G, DT, false>(X, n, Pq, p, m_z, 0.f, R, mp)) return false;
+    if (!list_resolve_p<G, DT, false>(X, n, Pq, p, m_z, 0.f, R, mp, &nk)) return false;
   } else {
     const float* wq = list_w(X);
     uint64_t s = 0;
     for (int i = gtid<G>(); i < n; i += G) s += to_fx(wq[i]);
     mp = gsum_q<G>(s, X.sh->rq[1]);
+    nk = (K > 0) ? K : n;
   }
-  int nk = 0;
-  for (int i = gtid<G>(); i < n; i += G) nk += in_set(lk[i], li[i], R.vP, R.idP) ? 1 : 0;
-  nk = gsum_i<G>(nk, X.sh->ri[0]);
   int tok = -1;
-  if (a.mode == MODE_SAMPLE) tok = list_draw<G>(X, n, R.vP, R.idP, mp, u);
+  if (a.mode == MODE_SAMPLE)
+    tok = (G == NT && nk <= NT) ? list_draw_small(X, n, R.vP, R.idP, mp, u)
+                                : list_draw<G>(X, n, R.vP, R.idP, mp, u);
   const float* wq = list_w(X);
   const double inv = 1099511627776.0 / (double)mp;
   for (int i = gtid<G>(); i < n; i += G) {
@@ -116,8 +117,13 @@ __device__ bool list_solve(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float
 // the same verdict.
 template <int DT>
 __device__ __noinline__ bool list_finish(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float m_z,
-                                         double u, int path) {
-  list_range(X, n);
+                                         double u, int path, uint32_t kbase, uint32_t kmax) {
+  // every list entry has kbase <= key <= kmax (the stream's threshold and its
+  // largest append)
+  if (threadIdx.x == 0) {
+    X.sh->bu[4] = kbase;
+    X.sh->bu[5] = max(kmax, kbase);
+  }
   zero_outputs(X);
   __syncthreads();
   bool ok;
@@ -283,12 +289,12 @@ __device__ __noinline__ void row_argmax(Ctx<DT>& X) {
 // Mass stream; a second stream with the row maximum as reference when the
 // first chunk's maximum was far below it (weights would overflow).
 template <int DT, bool ALLM>
-__device__ __forceinline__ ExpOut mass_stream(Ctx<DT>& X, float Kt, float vest) {
+__device__ __forceinline__ ExpOut mass_stream(Ctx<DT>& X, float Kt, float vest, float p_hist) {
   ExpOut E;
   float ref = __int_as_float(0x7fffffff);
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
-    E = exp_stream<DT, ALLM, !ALLM>(X, Kt, vest, ref);
+    E = exp_stream<DT, ALLM, !ALLM>(X, Kt, vest, ref, p_hist);
     if (X.sh->timeout || E.nf || E.nleg == 0 || !((E.mx - E.ref) * X.c2 > 100.f)) break;
     ref = E.mx;
   }
@@ -298,7 +304,7 @@ __device__ __forceinline__ ExpOut mass_stream(Ctx<DT>& X, float Kt, float vest) 
 template <int DT>
 __device__ __noinline__ void row_keepall(Ctx<DT>& X, double u, float vest) {
   const KArgs& a = *X.a;
-  const ExpOut E = mass_stream<DT, true>(X, 0.f, vest);
+  const ExpOut E = mass_stream<DT, true>(X, 0.f, vest, 0.f);
   if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
   if (E.nf) return error_row(X, ST_NONFINITE);
   if (E.nleg == 0) return error_row(X, ST_EMPTY);
@@ -320,7 +326,8 @@ __device__ __noinline__ bool row_list(Ctx<DT>& X, int K, float p, double u, floa
   const bool take_all = vest <= (float)(CAP - CAP / 8);
   const float Kt = (float)(K + K / 4 + 64);
   int nf = 0;
-  const uint32_t kmax = list_stream(X, Kt, vest, take_all, nf);
+  uint32_t tkey;
+  const uint32_t kmax = list_stream(X, Kt, vest, take_all, nf, tkey);
   if (X.sh->timeout) {
     error_row(X, ST_TIMEOUT, __LINE__);
     return true;
@@ -338,7 +345,8 @@ __device__ __noinline__ bool row_list(Ctx<DT>& X, int K, float p, double u, floa
     return true;
   }
   const float m_z = __fdiv_rn(key_value<DT>(kmax), X.temp);
-  if (!list_finish(X, nl, min(K, nl), p, 0, m_z, u, PATH_SIGMA)) error_row(X, ST_TIMEOUT, __LINE__);
+  if (!list_finish(X, nl, min(K, nl), p, 0, m_z, u, PATH_SIGMA, tkey, kmax))
+    error_row(X, ST_TIMEOUT, __LINE__);
   return true;
 }
 
@@ -348,7 +356,10 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
   // 512 -- top-p sets are short unless the row is flat, and flat rows take
   // the histogram bracket anyway
   const int Kt = (K < X.V && (float)K < vest && K <= (CAP * 3) / 4) ? K + K / 4 + 64 : 512;
-  const ExpOut E = mass_stream<DT, false>(X, (float)Kt, vest);
+  // a top-p row without top-k boundary may build its weight histogram in the
+  // stream (when the first chunk predicts a kept set beyond the list)
+  const bool g1 = !((float)K < vest) && p < 1.f;
+  const ExpOut E = mass_stream<DT, false>(X, (float)Kt, vest, g1 ? p : 0.f);
   if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
   if (E.nf) return error_row(X, ST_NONFINITE);
   if (E.nleg == 0) return error_row(X, ST_EMPTY);
@@ -365,20 +376,29 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
   // 1. the whole kept set inside the sigma-truncated list
   if (list_ok) {
     if (needK && n >= keff) {
-      if (list_finish(X, n, keff, p, 0, m_z, u, PATH_SIGMA)) return;
+      if (list_finish(X, n, keff, p, 0, m_z, u, PATH_SIGMA, E.tkey, E.lkmax)) return;
     } else if (!needK && p < 1.f && E.lmass >= (double)p * E.z * (1.0 - 1e-4)) {
       // the list (a rank prefix of the legal set) carries p of the row's mass
       const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));
-      if (list_finish(X, n, 0, p, Pq, m_z, u, PATH_SIGMA)) return;
+      if (list_finish(X, n, 0, p, Pq, m_z, u, PATH_SIGMA, E.tkey, E.lkmax)) return;
     }
   }
   // 2. a weight histogram (relative to the maximum), then one band pass over
   //    the bracket it gives
   int b_lo, b_hi;
   if (!needK && p < 1.f) {
-    whist_pass(X, nm, true);
-    if (wh_bracket(X, true, 0, (double)p * zq / 1099511627776.0, 0.f, b_lo, b_hi)) {
-      const BandOut bo = band_kept_pass(X, b_lo, b_hi, nm, nm);
+    // bins relative to the stream's reference when it built the histogram,
+    // else a histogram pass relative to the maximum
+    const float nref = E.hist ? -E.ref * X.c2 : nm;
+    bool br;
+    if (E.hist) {
+      br = wh_bracket(X, true, 0, (double)p * E.z, (m - E.ref) * X.c2, b_lo, b_hi);
+    } else {
+      whist_pass(X, nm, true);
+      br = wh_bracket(X, true, 0, (double)p * zq / 1099511627776.0, 0.f, b_lo, b_hi);
+    }
+    if (br) {
+      const BandOut bo = band_kept_pass(X, b_lo, b_hi, nref, nm);
       const int nb = min(X.sh->n, CAP);
       list_range(X, nb);
       const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));

@@ -194,6 +194,7 @@ enum { SEL_COUNT = 0, SEL_MASS = 1, SEL_TIEID = 2 };
 struct SelOut {
   uint32_t v;
   uint64_t above, at_w, total, target;
+  int above_n;  // entries strictly above v
   int at_n;
   int ok;
 };
@@ -217,6 +218,7 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
   const bool scanner = (G == 32) || (threadIdx.x < 32);
   uint32_t prefix = 0u;
   uint64_t above = 0;
+  int above_n = 0;
   SelOut o;
   o.ok = 1;
   o.at_w = 0;
@@ -266,13 +268,18 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
     if (scanner) {
       // lane l reads digits 255 - 8l ... 248 - 8l (descending)
       uint64_t v[8];
+      uint32_t cv[8];
       uint64_t loc = 0;
+      uint32_t locc = 0u;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         v[q] = w[255 - 8 * lane - q];
+        cv[q] = c[255 - 8 * lane - q];
         loc += v[q];
+        locc += cv[q];
       }
       const uint64_t inc = warp_incl_scan(loc);
+      uint32_t cumc = (uint32_t)above_n + warp_incl_scan(locc) - locc;
       const uint64_t tot = __shfl_sync(0xffffffffu, inc, 31);
       if (rd == 0) {
         o.total = tot;
@@ -284,26 +291,31 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
       uint64_t cum = above + inc - loc;
       int hit = -1;
       uint64_t hb = 0, hv = 0;
+      uint32_t hc = 0u;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (hit < 0 && v[q] > 0 && cum < target && cum + v[q] >= target) {
           hit = 255 - 8 * lane - q;
           hb = cum;
           hv = v[q];
+          hc = cumc;
         }
         cum += v[q];
+        cumc += cv[q];
       }
       const uint32_t bal = __ballot_sync(0xffffffffu, hit >= 0);
       const int src = bal ? (__ffs(bal) - 1) : 0;
       const int d = __shfl_sync(0xffffffffu, hit, src);
       const uint64_t hb2 = __shfl_sync(0xffffffffu, hb, src);
       const uint64_t hv2 = __shfl_sync(0xffffffffu, hv, src);
+      const uint32_t hc2 = __shfl_sync(0xffffffffu, hc, src);
       if (G == 32) {
         if (bal == 0u) {
           o.ok = 0;
         } else {
           prefix = (prefix << wr) | (uint32_t)d;
           above = hb2;
+          above_n = (int)hc2;
           o.at_w = hv2;
           o.at_n = (int)c[d];
         }
@@ -314,6 +326,7 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
         X.sh->bq[2] = tot;
         X.sh->bq[3] = target;
         X.sh->bi[1] = bal ? (int)c[d] : 0;
+        X.sh->bi[3] = (int)hc2;
       }
     }
     if (G != 32) {
@@ -324,6 +337,7 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
       } else {
         prefix = (prefix << wr) | (uint32_t)d;
         above = X.sh->bq[0];
+        above_n = X.sh->bi[3];
         o.at_w = X.sh->bq[1];
         o.at_n = X.sh->bi[1];
         if (rd == 0) {
@@ -336,6 +350,7 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
   }
   o.v = (KIND == SEL_TIEID) ? prefix : prefix + kbase;
   o.above = above;
+  o.above_n = above_n;
   o.target = target;
   return o;
 }
@@ -421,7 +436,7 @@ __device__ void list_weights(Ctx<DT>& X, int n, float m_z, float nm, uint32_t vK
 // list's S_k mass.  kept_mass receives the mass of S_p inside the list.
 template <int G, int DT, bool FAST>
 __device__ bool list_resolve_p(Ctx<DT>& X, int n, uint64_t target, float p, float m_z, float nm,
-                               Res& R, uint64_t& kept_mass) {
+                               Res& R, uint64_t& kept_mass, int* kept_n = nullptr) {
   const SelOut s = list_select<G, DT, SEL_MASS>(X, n, target, target ? 0.f : p, R.vK, R.idK, 0u);
   if (!s.ok) return false;
   R.vP = s.v;
@@ -437,6 +452,7 @@ __device__ bool list_resolve_p(Ctx<DT>& X, int n, uint64_t target, float p, floa
     R.idP = (int)(0xffffffu - ti.v);
   }
   kept_mass = s.above + (uint64_t)j * qv;
+  if (kept_n) *kept_n = s.above_n + j;
   return true;
 }
 
@@ -538,6 +554,55 @@ __device__ int list_draw(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, d
   }
   tok = (int)gmax_u<G>((uint32_t)(tok + 1), sh->ru[1]) - 1;
   return tok >= 0 ? tok : last;
+}
+
+// Id-order draw over a short kept set (at most NT entries): the kept entries
+// are compacted, ranked by id, laid out in id order and prefix-summed.
+template <int DT>
+__device__ int list_draw_small(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, double u) {
+  const float* wq = list_w(X);
+  const uint32_t* lk = X.lk;
+  const int* li = X.li;
+  Sh* sh = X.sh;
+  uint64_t* gq = list_scratch(X);            // compacted masses   [NT]
+  uint64_t* sq = gq + NT;                    // id-ordered masses  [NT]
+  int* gid = reinterpret_cast<int*>(sq + NT);  // compacted ids  [NT]
+  int* sid = gid + NT;                         // id-ordered ids [NT]
+  const int t = threadIdx.x;
+  const double T = u * (double)Mp;
+  __syncthreads();
+  if (t == 0) {
+    sh->gn = 0;
+    sh->bi[6] = -1;
+  }
+  __syncthreads();
+  for (int i = t; i < n; i += NT) {
+    const int id = li[i];
+    if (in_set(lk[i], id, vP, idP)) {
+      const int slot = atomicAdd(&sh->gn, 1);
+      if (slot < NT) {
+        gid[slot] = id;
+        gq[slot] = to_fx(wq[i]);
+      }
+    }
+  }
+  __syncthreads();
+  const int m = min(sh->gn, NT);
+  if (t < m) {
+    const int my = gid[t];
+    int r = 0;
+    for (int j = 0; j < m; ++j) r += (gid[j] < my) ? 1 : 0;
+    sq[r] = gq[t];
+    sid[r] = my;
+  }
+  __syncthreads();
+  const uint64_t v = (t < m) ? sq[t] : 0;
+  uint64_t tot;
+  const uint64_t ex = bscan_excl<uint64_t>(v, sh->rq[0], tot);
+  if (t < m && v > 0 && (double)ex <= T && (double)(ex + v) > T) sh->bi[6] = sid[t];
+  __syncthreads();
+  const int tok = sh->bi[6];
+  return tok >= 0 ? tok : ((m > 0) ? sid[m - 1] : -1);
 }
 
 }  // namespace smp

@@ -178,11 +178,11 @@ __device__ __noinline__ void argmax_stream(Ctx<DT>& Xr, uint32_t& best_key, int&
 // Sigma-truncated list.  Kt is the number of candidates aimed at; take_all
 // puts every legal element in the list.  Once the list overflows the rest of
 // the row is only drained.  Returns the largest key appended (0: none); nf
-// counts NaN / +inf seen in legal slots.
+// counts NaN / +inf seen in legal slots; tkey is the threshold's key.
 // ---------------------------------------------------------------------------
 template <int DT>
 __device__ __noinline__ uint32_t list_stream(Ctx<DT>& Xr, float Kt, float vest, bool take_all,
-                                             int& nf) {
+                                             int& nf, uint32_t& tkey) {
   LocalCtx<DT> lc_(Xr);
   Ctx<DT>& X = lc_.v;
   constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
@@ -219,6 +219,7 @@ __device__ __noinline__ uint32_t list_stream(Ctx<DT>& Xr, float Kt, float vest, 
     R.release(X);
   }
   nf = bsum_i(bad, X.sh->ri[0]);
+  tkey = bits_key<DT>((DT == DT_F32) ? t2 : (t2 & 0xffffu));  // every entry's key is >= tkey
   return bmax_u(kmax, X.sh->ru[0]);
 }
 
@@ -237,6 +238,8 @@ struct ExpOut {
   int nf;      // NaN / +inf seen
   int ovf;     // list overflow (EMIT)
   double lmass;  // mass of the list's elements (EMIT, relative to ref)
+  uint32_t tkey, lkmax;  // the list threshold's key and the largest key listed (EMIT)
+  int hist;              // the weight histogram (relative to ref) was built
 };
 
 // Sum of the EPV weights of a vector: a tree (short dependency chains).
@@ -250,7 +253,8 @@ __device__ __forceinline__ float tree_sum(const float (&w)[EPV]) {
 }
 
 template <int DT, bool ALLM, bool EMIT>
-__device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, float ref_in) {
+__device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, float ref_in,
+                                          float p_hist) {
   LocalCtx<DT> lc_(Xr);
   Ctx<DT>& X = lc_.v;
   constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
@@ -265,6 +269,9 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   const float c2 = X.c2;
   double tz = 0.0;
   float lm = 0.f;
+  uint32_t lkm = 0u;
+  bool hist = false;
+  uint32_t* wh = X.wh;
   uint32_t amax = p_ninf<DT>();
   int nleg = 0;
   ring_begin(X);
@@ -288,7 +295,34 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
         if (!(ref > -INFINITY)) ref = 0.f;
       }
       nref = -ref * c2;
-      if (EMIT) list_threshold(X, stage, Kt, vest, t2, tf);
+      if (EMIT) {
+        list_threshold(X, stage, Kt, vest, t2, tf);
+        if (p_hist > 0.f) {
+          // top-p row: if the first chunk's mass at or above the list
+          // threshold is below p of its mass, the kept set will not fit the
+          // list -- build the weight histogram on the way (bins relative to
+          // ref, excess-weighted counts)
+          float z0 = 0.f, m0 = 0.f;
+#pragma unroll 1
+          for (int it = 0; it < ITW; ++it) {
+            float x[EPV];
+            unpack<DT>(load_vec(X, stage, 0, v0 + 32 * it), x);
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) {
+              const float w = fast_exp2(fmaf(x[j], c2, nref));
+              z0 += w;
+              if (x[j] >= tf) m0 += w;
+            }
+          }
+          z0 = bsum_f(z0, X.sh->rf[1]);
+          m0 = bsum_f(m0, X.sh->rf[2]);
+          hist = m0 < p_hist * z0;
+          if (hist) {
+            for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
+            __syncthreads();
+          }
+        }
+      }
     }
     float cs = 0.f;
     uint32_t hits = 0u, cmin = p_pinf<DT>();
@@ -304,6 +338,17 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
 #pragma unroll
       for (int j = 0; j < EPV; ++j) w[j] = fast_exp2(fmaf(x[j], c2, nref));  // -inf -> 0
       cs += tree_sum<EPV>(w);
+      if (EMIT && hist) {
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) {
+          if (!(x[j] > -INFINITY)) continue;
+          const float y = fmaf(fmaf(x[j], c2, nref), -(float)WHS, (float)WHOFF);
+          const float fy = floorf(y);
+          const int b = min(max((int)fy, 0), WBINS - 1);
+          const float f = (b == (int)fy) ? (1.f - (y - fy)) * (1.f / WHS) : 0.f;
+          atomicAdd(&wh[b], (uint32_t)fmaf(f, fmaf(f, 491.96f, 1419.57f), 2048.5f));
+        }
+      }
     }
     // legal count and kept-mask words: every slot legal unless the chunk
     // holds -inf somewhere in this warp
@@ -359,7 +404,7 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
         const uint4 rv = load_vec(X, stage, c, vi);
         const uint32_t cm = ge_mask<DT>(rv, t2, tf, dummy);
         if (!cm) continue;
-        lane_append<DT>(X.lk, X.li, &X.sh->n, rv, c * CE + vi * EPV, cm);
+        lkm = max(lkm, lane_append<DT>(X.lk, X.li, &X.sh->n, rv, c * CE + vi * EPV, cm));
         float x[EPV];
         unpack<DT>(rv, x);
 #pragma unroll
@@ -383,6 +428,9 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   o.nleg = bsum_i(nleg, X.sh->ri[0]);
   o.ovf = X.sh->n > CAP;
   o.lmass = EMIT ? bsum_d((double)lm, X.sh->rd[1]) : 0.0;
+  o.tkey = bits_key<DT>((DT == DT_F32) ? t2 : (t2 & 0xffffu));
+  o.lkmax = EMIT ? bmax_u(lkm, X.sh->ru[0]) : 0u;
+  o.hist = hist ? 1 : 0;
   return o;
 }
 
