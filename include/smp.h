@@ -87,13 +87,16 @@ typedef struct {
 
 /* Create a handle bound to CUDA device `device` for calls with B <=
  * max_batch and V <= max_vocab.  Queries the device, configures the kernels
- * (cluster size, shared memory) and builds the host-side sigma-truncation
+ * (shared memory, CTAs per SM) and builds the host-side sigma-truncation
  * table (Qrita paper notes, key design 1 and "training strategy": delta =
- * Phi^-1(1 - k/V) from a precomputed table).  Allocates no device memory.
+ * Phi^-1(1 - k/V) from a precomputed table).  Allocates the handle's one
+ * device workspace (about 1.7 MB: the job board on which rows with very flat
+ * top-p sets share their second pass across CTAs); calls allocate nothing.
+ * Calls on one handle must not run concurrently (issue them on one stream).
  * Returns SMP_OK, SMP_ERR_INVALID_PARAM or SMP_ERR_CUDA. */
 int smp_create(smp_handle* h, int device, int max_batch, int max_vocab);
 
-/* Release a handle (NULL is accepted). */
+/* Release a handle and its workspace (NULL is accepted). */
 int smp_destroy(smp_handle h);
 
 /* Kept set of every row: after temperature, mask, top-k and top-p (steps

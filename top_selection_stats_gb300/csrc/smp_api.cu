@@ -33,6 +33,7 @@ struct smp_ctx {
   int grid_max;
   float delta[DTAB];
   int32_t* row_info;
+  Board* board;  // job board: zeroed at creation, reset by each launch's last CTA
 };
 
 namespace {
@@ -114,6 +115,7 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   a.kept_count = kept_count;
   a.probs = probs;
   a.row_info = h->row_info;
+  a.board = h->board;
   a.mode = mode;
   const size_t es = (size_t)esize_of(dt);
   a.use_tma = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
@@ -177,11 +179,23 @@ int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
     return SMP_ERR_CUDA;
   }
   h->grid_max = per_sm * h->sm_count;
+  h->board = nullptr;
+  if (cudaMalloc(&h->board, sizeof(Board)) != cudaSuccess ||
+      cudaMemset(h->board, 0, sizeof(Board)) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->board) cudaFree(h->board);
+    delete h;
+    return SMP_ERR_CUDA;
+  }
   *out = h;
   return SMP_OK;
 }
 
 int smp_destroy(smp_handle h) {
+  if (h) {
+    DeviceGuard guard(h->device);
+    if (h->board) cudaFree(h->board);
+  }
   delete h;
   return SMP_OK;
 }

@@ -26,6 +26,23 @@ constexpr int SEG_MAX = 3072;       // id segments of the list sampler
 constexpr int GMAX = 512;           // ids per segment, at most
 constexpr int NOID = 0x7fffffff;
 
+// Job board (device workspace owned by the handle): rows whose kept set is
+// decided by a weight-histogram bracket publish their band pass as one task
+// per chunk; CTAs that have finished their own rows claim and run tasks.
+constexpr int MAXJOBS = 32;
+struct JobHdr {
+  int ready, row, b_lo, b_hi;
+  float nref, nm, c2, pad;
+  int claimed, done, list_n, above_n;
+};
+struct Board {
+  int njobs, ctas_done, exits, pad;
+  JobHdr hdr[MAXJOBS];
+  float cmass[MAXJOBS][MAXCH * NWARP];
+  uint32_t lk[MAXJOBS][CAP];
+  int li[MAXJOBS][CAP];
+};
+
 struct KArgs {
   const void* logits;
   long long ld;
@@ -44,6 +61,7 @@ struct KArgs {
   int* row_info;
   int mode;
   int use_tma;  // rows are 16-byte aligned: stage them with bulk copies
+  Board* board;  // job board (zeroed between launches), or null
   float delta[DTAB];
 };
 

@@ -160,6 +160,21 @@ struct BandOut {
   int above_n;
   uint64_t above_q;  // fixed-point mass above the bracket (from the per-cell sums)
 };
+
+// Fixed-point mass of the per-(chunk, warp) cells in sh->cmass: each chunk's
+// cells summed in warp order and converted on its own, so the total does not
+// depend on which CTA computed which chunk.
+template <int DT>
+__device__ uint64_t cells_fixed_mass(Ctx<DT>& X) {
+  uint64_t s = 0;
+  for (int c = threadIdx.x; c < X.nch; c += NT) {
+    double m = 0.0;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) m += (double)X.sh->cmass[c][w];
+    s += (uint64_t)(m * 1099511627776.0);
+  }
+  return bsum_q(s, X.sh->rq[1]);
+}
 template <int DT>
 __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, float nref, float nm) {
   LocalCtx<DT> lc_(Xr);
@@ -170,7 +185,6 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
   const float c2 = X.c2;
   if (threadIdx.x == 0) X.sh->n = 0;
   int nk = 0;
-  double ta = 0.0;
   ring_begin(X);
 #pragma unroll 1
   for (int c = 0; c < X.nch; ++c) {
@@ -201,13 +215,82 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
     }
     const float ws = warp_sum(cs);
     if (lane == 0) X.sh->cmass[c][warp] = ws;
-    ta += (double)cs;
     warp_release(X, c);
   }
   BandOut o;
   o.above_n = bsum_i(nk, X.sh->ri[0]);
-  o.above_q = (uint64_t)(bsum_d(ta, X.sh->rd[0]) * 1099511627776.0);
+  o.above_q = 0;
   return o;
+}
+
+// ---------------------------------------------------------------------------
+// One chunk of a published band pass (job j of the board), run by the whole
+// CTA -- the row's owner or a helper between rows: the same classification
+// as band_kept_pass, with the bracket elements appended to the job's list,
+// the cell masses stored in the job and the counts added to its header.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const KArgs& a = *X.a;
+  Board* bd = a.board;
+  volatile JobHdr* H = &bd->hdr[j];
+  const int row = H->row, b_lo = H->b_lo, b_hi = H->b_hi;
+  const float nref = H->nref, nm = H->nm, c2 = H->c2;
+  X.row = row;
+  X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
+  X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
+  X.c2 = c2;
+  uint32_t* mrow = a.kept_mask ? a.kept_mask + (size_t)row * X.W : nullptr;
+  __syncthreads();
+  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
+  const char* stage = ring_wait(X, c);
+  float cs = 0.f;
+  int nk = 0;
+#pragma unroll 1
+  for (int it = 0; it < ITW; ++it) {
+    const int vi = warp_vec<DT>(it);
+    const uint4 r = load_vec(X, stage, c, vi);
+    const int id0 = c * CE + vi * EPV;
+    float x[EPV];
+    unpack<DT>(r, x);
+    uint32_t kb = 0u, cm = 0u;
+#pragma unroll
+    for (int q = 0; q < EPV; ++q) {
+      if (!(x[q] > -INFINITY)) continue;
+      const int b = wbin(x[q], c2, nref);
+      if (b < b_lo) {
+        kb |= 1u << q;
+        cs += fast_exp2(fmaf(x[q], c2, nm));
+      } else if (b <= b_hi) {
+        cm |= 1u << q;
+      }
+    }
+    nk += __popc(kb);
+    put_mask_word<DT>(X, mrow, kb, id0);
+    if (cm) {
+      int pos = atomicAdd((int*)&H->list_n, __popc(cm));
+      while (cm) {
+        const int q = __ffs(cm) - 1;
+        cm &= cm - 1u;
+        if (pos < CAP) {
+          bd->lk[j][pos] = bits_key<DT>(elem_bits_dyn<DT>(r, q));
+          bd->li[j][pos] = id0 + q;
+        }
+        ++pos;
+      }
+    }
+  }
+  const float ws = warp_sum(cs);
+  if (lane == 0) bd->cmass[j][c * NWARP + warp] = ws;
+  nk = __reduce_add_sync(0xffffffffu, nk);
+  if (lane == 0 && nk) atomicAdd((int*)&H->above_n, nk);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd((int*)&H->done, 1);
 }
 
 // ---------------------------------------------------------------------------

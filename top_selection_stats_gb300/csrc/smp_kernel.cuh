@@ -197,6 +197,160 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
 }
 
 // ---------------------------------------------------------------------------
+// Job board.  The owner of a bracketed row publishes its band pass (one task
+// per chunk), runs tasks itself, waits (bounded) for the tasks others
+// claimed, and gathers the list, the cell masses and the count above the
+// bracket.  No wait depends on a helper starting: a task is only waited for
+// once some CTA has claimed it.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ int publish_job(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm) {
+  Board* bd = X.a->board;
+  if (!bd) return -1;
+  if (threadIdx.x == 0) {
+    int j = atomicAdd(&bd->njobs, 1);
+    if (j < MAXJOBS) {
+      JobHdr* H = &bd->hdr[j];
+      H->row = X.row;
+      H->b_lo = b_lo;
+      H->b_hi = b_hi;
+      H->nref = nref;
+      H->nm = nm;
+      H->c2 = X.c2;
+      __threadfence();
+      atomicExch(&H->ready, 1);
+    } else {
+      j = -1;
+    }
+    X.sh->bi[0] = j;
+  }
+  __syncthreads();
+  const int j = X.sh->bi[0];
+  __syncthreads();
+  return j;
+}
+
+// Runs tasks of job j until all are claimed, then waits for the claimed ones;
+// returns the list length (-1 if a bounded wait expired).
+template <int DT>
+__device__ __noinline__ int run_job(Ctx<DT>& X, int j, BandOut& bo) {
+  Board* bd = X.a->board;
+  volatile JobHdr* H = &bd->hdr[j];
+#pragma unroll 1
+  while (true) {
+    if (threadIdx.x == 0) X.sh->bi[0] = atomicAdd((int*)&H->claimed, 1);
+    __syncthreads();
+    const int t = X.sh->bi[0];
+    __syncthreads();
+    if (t >= X.nch) break;
+    band_task(X, j, t);
+  }
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    int ok = 1;
+    while (H->done < X.nch) {
+      if (clock64() - t0 > 4000000000ll) {
+        ok = 0;
+        break;
+      }
+      __nanosleep(200);
+    }
+    __threadfence();
+    X.sh->bi[0] = ok;
+    X.sh->bi[1] = H->list_n;
+    X.sh->bi[2] = H->above_n;
+  }
+  __syncthreads();
+  const int ok = X.sh->bi[0], ln = X.sh->bi[1];
+  bo.above_n = X.sh->bi[2];
+  bo.above_q = 0;
+  if (!ok) {
+    if (threadIdx.x == 0) X.sh->timeout = 1;
+    __syncthreads();
+    return -1;
+  }
+  const int n = min(ln, CAP);
+  for (int i = threadIdx.x; i < n; i += NT) {
+    X.lk[i] = bd->lk[j][i];
+    X.li[i] = bd->li[j][i];
+  }
+  for (int f = threadIdx.x; f < X.nch * NWARP; f += NT)
+    X.sh->cmass[f / NWARP][f % NWARP] = bd->cmass[j][f];
+  if (threadIdx.x == 0) X.sh->n = ln;
+  __syncthreads();
+  return ln;
+}
+
+// Band pass over a weight-histogram bracket, shared on the job board when a
+// slot is free, else run by this CTA alone.  Returns the list length.
+template <int DT>
+__device__ int band_any(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm, BandOut& bo) {
+  const int j = publish_job(X, b_lo, b_hi, nref, nm);
+  int ln;
+  if (j >= 0) {
+    ln = run_job(X, j, bo);
+  } else {
+    bo = band_kept_pass(X, b_lo, b_hi, nref, nm);
+    ln = X.sh->n;
+  }
+  if (ln >= 0) bo.above_q = cells_fixed_mass(X);
+  return ln;
+}
+
+// After its own rows, a CTA runs published tasks until every CTA has finished
+// its rows (so no job can still appear); the last CTA out resets the board.
+template <int DT>
+__device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
+  Board* bd = X.a->board;
+  if (!bd) return;
+  if (threadIdx.x == 0) atomicAdd(&bd->ctas_done, 1);
+  const long long t0 = clock64();
+#pragma unroll 1
+  while (true) {
+    if (threadIdx.x == 0) {
+      volatile Board* vb = bd;
+      int jj = -1, tt = -1, stop = 0;
+      const int nj = min(vb->njobs, MAXJOBS);
+      for (int q = 0; q < nj && jj < 0; ++q) {
+        if (!vb->hdr[q].ready || vb->hdr[q].claimed >= X.nch) continue;
+        const int t = atomicAdd(&bd->hdr[q].claimed, 1);
+        if (t < X.nch) {
+          jj = q;
+          tt = t;
+        }
+      }
+      __threadfence();  // the job's header is read after its ready flag
+      if (jj < 0) {
+        if (vb->ctas_done >= (int)gridDim.x || clock64() - t0 > 4000000000ll) stop = 1;
+        else __nanosleep(400);
+      }
+      X.sh->bi[0] = jj;
+      X.sh->bi[1] = tt;
+      X.sh->bi[2] = stop;
+    }
+    __syncthreads();
+    const int jj = X.sh->bi[0], tt = X.sh->bi[1], stop = X.sh->bi[2];
+    __syncthreads();
+    if (stop) break;
+    if (jj >= 0) band_task(X, jj, tt);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&bd->exits, 1) == (int)gridDim.x - 1) {
+      const int nj = min(bd->njobs, MAXJOBS);
+      for (int q = 0; q < nj; ++q) {
+        JobHdr* H = &bd->hdr[q];
+        H->ready = H->claimed = H->done = H->list_n = H->above_n = 0;
+      }
+      bd->njobs = 0;
+      bd->ctas_done = 0;
+      bd->exits = 0;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Radix descent to a boundary.  COUNT (MASS = false): the target-th largest
 // legal element (ties: earliest ids).  MASS: the top-p boundary of S_k (vK,
 // idK) for mass p * M_k, M_k taken from the first histogram.  Returns false if
@@ -398,11 +552,13 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
       br = wh_bracket(X, true, 0, (double)p * zq / 1099511627776.0, 0.f, b_lo, b_hi);
     }
     if (br) {
-      const BandOut bo = band_kept_pass(X, b_lo, b_hi, nref, nm);
-      const int nb = min(X.sh->n, CAP);
+      BandOut bo;
+      const int ln = band_any(X, b_lo, b_hi, nref, nm, bo);
+      if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+      const int nb = min(max(ln, 0), CAP);
       list_range(X, nb);
       const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));
-      if (X.sh->n <= CAP && Pq > bo.above_q) {
+      if (ln >= 0 && ln <= CAP && Pq > bo.above_q) {
         list_weights<NT, DT, true>(X, nb, 0.f, nm, 0u, -1);
         Res R;
         R.vK = 0u;
@@ -415,12 +571,14 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
   } else if (needK) {
     whist_pass(X, nm, false);
     if (wh_bracket(X, false, keff, 0.0, 0.f, b_lo, b_hi)) {
-      const BandOut bo = band_kept_pass(X, b_lo, b_hi, nm, nm);
-      const int nb = min(X.sh->n, CAP);
+      BandOut bo;
+      const int ln = band_any(X, b_lo, b_hi, nm, nm, bo);
+      if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+      const int nb = min(max(ln, 0), CAP);
       list_range(X, nb);
       uint32_t vK;
       int idK;
-      if (X.sh->n <= CAP && keff > bo.above_n &&
+      if (ln >= 0 && ln <= CAP && keff > bo.above_n &&
           list_resolve_k<NT>(X, nb, keff - bo.above_n, vK, idK)) {
         list_weights<NT, DT, true>(X, nb, 0.f, nm, vK, idK);
         if (p >= 1.f) return finish_band(X, nb, bo, vK, idK, m, u, PATH_FULL);
@@ -529,6 +687,7 @@ __global__ void __launch_bounds__(NT, 2) smp_kernel(const __grid_constant__ KArg
   }
   __syncthreads();
   for (int row = blockIdx.x; row < a.B; row += gridDim.x) process_row(X, row);
+  help_and_exit(X);
 }
 
 }  // namespace smp
