@@ -124,6 +124,33 @@ int smp_argmax(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, 
                const uint32_t* bitmask, int32_t* tokens, int32_t* row_status,
                smp_stream stream);
 
+/* smp_sample without a handle and without any device allocation.  The pages
+ * this library follows have no counterpart: it exists for callers that may
+ * not call cudaMalloc.  One example is a plugin inside a serving runtime that
+ * reserves nearly all device memory for its KV cache at start-up and hands
+ * out memory only through its own pool.  Another is a stateless hook with
+ * nowhere to keep a handle between calls.
+ * Arguments, outputs and statuses are those of smp_sample.  The call runs on
+ * the CURRENT CUDA device.  The caller passes every input and output.
+ * Scratch: the job board that smp_create would allocate is instead a static
+ * device array of 1,705,728 bytes.  Every device that loads the library
+ * holds it until the process exits.
+ * Set-up: the first call on each device does the set-up, with that device
+ * current.  It configures the kernels, looks up the array's device address
+ * and clears the array on `stream`.  Make that first call before any stream
+ * capture.
+ * Limit: V may be at most 128 staging chunks, that is 786,432 tokens for fp32
+ * and 1,572,864 for bf16/fp16.  Larger V returns SMP_ERR_CAPACITY and
+ * launches nothing.  B has no limit of its own.
+ * Sharing: all calls on a device share the one array.  Each launch leaves
+ * the board cleared when it ends.  Calls that overlap on the GPU race on it,
+ * so issue them in order, e.g. on one stream.  Calls through a handle use
+ * that handle's own workspace and do not race with these. */
+int smp_sample_noalloc(const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                       const uint32_t* bitmask, const smp_row_params* params, int32_t* tokens,
+                       int32_t* row_status, uint32_t* kept_mask, int32_t* kept_count,
+                       smp_stream stream);
+
 /* Optional per-row diagnostics for subsequent calls on this handle: when
  * row_info is not NULL, each call writes int32 [B][4] to it (DEVICE memory
  * owned by the caller, at least max_batch*4 entries): {path, band size,

@@ -7,8 +7,8 @@ kernels.  There is no fallback: if the library is missing, calls raise.
 """
 from .binding import (SMP_OK, SMP_ERR_EMPTY, SMP_ERR_NONFINITE, SMP_ERR_INVALID_PARAM,
                       SMP_ERR_TIMEOUT, SMP_ERR_CUDA, SMP_ERR_CAPACITY, PATH_NAMES, Sampler,
-                      SmpError, lib_path, load_library)
+                      SmpError, lib_path, load_library, sample_noalloc)
 
-__all__ = ["Sampler", "SmpError", "load_library", "lib_path", "SMP_OK", "SMP_ERR_EMPTY",
-           "SMP_ERR_NONFINITE", "SMP_ERR_INVALID_PARAM", "SMP_ERR_TIMEOUT", "SMP_ERR_CUDA",
+__all__ = ["Sampler", "SmpError", "load_library", "lib_path", "sample_noalloc", "SMP_OK",
+           "SMP_ERR_EMPTY", "SMP_ERR_NONFINITE", "SMP_ERR_INVALID_PARAM", "SMP_ERR_TIMEOUT", "SMP_ERR_CUDA",
            "SMP_ERR_CAPACITY", "PATH_NAMES"]

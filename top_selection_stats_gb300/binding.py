@@ -15,7 +15,7 @@ PATH_NAMES = {0: "error", 1: "greedy", 2: "all", 3: "sigma", 4: "full"}
 _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_F16}
 
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
-           "smp_set_row_info", "smp_plan", "smp_status_string")
+           "smp_sample_noalloc", "smp_set_row_info", "smp_plan", "smp_status_string")
 
 
 class SmpError(RuntimeError):
@@ -51,6 +51,8 @@ def load_library(path=None):
     L.smp_sample.argtypes = [P, P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams), P, P,
                              P, P, P]
     L.smp_argmax.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P]
+    L.smp_sample_noalloc.argtypes = [P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams), P,
+                                     P, P, P, P]
     L.smp_set_row_info.argtypes = [P, P]
     L.smp_plan.argtypes = [P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
@@ -194,3 +196,34 @@ class Sampler:
                                  _ptr(bitmask), _ptr(tokens), _ptr(status), self._stream())
         _check(rc, "smp_argmax")
         return dict(tokens=tokens, status=status)
+
+
+def sample_noalloc(logits, temperature, top_k, top_p, seed, offset, tokens, status,
+                   bitmask=None, V=None, kept_mask=None, kept_count=None, lib=None):
+    """smp_sample_noalloc: sampling with no handle and no device allocation.
+
+    For callers that may not allocate device memory.  The library allocates
+    nothing here, and neither does this wrapper: the caller passes every
+    output (tokens, status and, optionally, kept_mask and kept_count).  The
+    call runs on the current stream of the device that holds ``logits``.
+    Tensor layouts are those of ``Sampler.sample``.
+    """
+    L = lib or load_library()
+    if logits.dtype not in _DTYPES:
+        raise ValueError(f"unsupported logits dtype {logits.dtype}")
+    dev = logits.device
+    ts = (logits, bitmask, temperature, top_k, top_p, seed, offset, tokens, status, kept_mask,
+          kept_count)
+    for t in ts:
+        if t is not None and (not t.is_cuda or t.device != dev or not t.is_contiguous()):
+            raise ValueError(f"every tensor must be contiguous and on {dev}")
+    B, ld = logits.shape
+    V = ld if V is None else V
+    params = RowParams(*(t.data_ptr() for t in (temperature, top_k, top_p, seed, offset)))
+    with torch.cuda.device(dev):
+        stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+        rc = L.smp_sample_noalloc(_ptr(logits), _DTYPES[logits.dtype], B, V, ld, _ptr(bitmask),
+                                  ctypes.byref(params), _ptr(tokens), _ptr(status),
+                                  _ptr(kept_mask), _ptr(kept_count), stream)
+    _check(rc, "smp_sample_noalloc")
+    return dict(tokens=tokens, status=status, kept_mask=kept_mask, kept_count=kept_count)

@@ -4,6 +4,7 @@
 // call allocates, copies to the host or synchronises.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -255,3 +256,103 @@ const char* smp_status_string(int code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// smp_sample_noalloc: the sampling call without a handle, for callers that may
+// not allocate device memory.  Its only scratch is the job board (the handle
+// calls take theirs from the handle's workspace); here it is the file-scope
+// array below, which the CUDA runtime places on every device that loads this
+// library and keeps until the process exits.  On the host the array's name
+// denotes a host-side shadow object, not device memory, so the per-device
+// set-up asks the runtime for its device address and passes that to the
+// kernel.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t NOALLOC_SCRATCH_BYTES = (sizeof(Board) + 255) / 256 * 256;
+static_assert(NOALLOC_SCRATCH_BYTES == 1705728, "the scratch size is stated in smp.h");
+constexpr int NOALLOC_MAX_DEVICES = 64;
+}  // namespace
+
+static __device__ __align__(256) unsigned char smp_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex noalloc_mutex;
+smp_ctx noalloc_dev[NOALLOC_MAX_DEVICES];
+bool noalloc_ready[NOALLOC_MAX_DEVICES];
+
+// Once per device, with that device current: the kernels' shared-memory
+// attribute and the resident grid (as smp_create computes them), the sigma
+// table, the scratch's device address, and a clear of the scratch on the
+// caller's stream.  The board must start at zero; every launch's last CTA
+// leaves it at zero again, so later calls need no clear of their own.
+int noalloc_setup(int dev, cudaStream_t st, smp_ctx** out) {
+  std::lock_guard<std::mutex> lock(noalloc_mutex);
+  smp_ctx& c = noalloc_dev[dev];
+  if (!noalloc_ready[dev]) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SMP_ERR_CUDA;
+    }
+    int per_sm = 1 << 30;
+    for (int dt : {DT_F32, DT_BF16, DT_F16}) {
+      const void* k = kernel_for(dt);
+      int nb = 0;
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, NT, SMEM_TOTAL) != cudaSuccess) {
+        cudaGetLastError();
+        return SMP_ERR_CUDA;
+      }
+      per_sm = nb < per_sm ? nb : per_sm;
+    }
+    if (per_sm < 1) return SMP_ERR_CUDA;
+    Board* board = nullptr;
+    if (cudaGetSymbolAddress((void**)&board, smp_noalloc_scratch) != cudaSuccess ||
+        cudaMemsetAsync(board, 0, NOALLOC_SCRATCH_BYTES, st) != cudaSuccess) {
+      cudaGetLastError();
+      return SMP_ERR_CUDA;
+    }
+    c.device = dev;
+    c.max_batch = INT_MAX;
+    c.max_vocab = INT_MAX;
+    c.sm_count = prop.multiProcessorCount;
+    c.smem_optin = (int)prop.sharedMemPerBlockOptin;
+    c.smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
+    c.grid_max = per_sm * c.sm_count;
+    for (int i = 0; i < DTAB; ++i) c.delta[i] = (float)upper_quantile(std::pow(2.0, -24.0 + 0.25 * i));
+    c.row_info = nullptr;
+    c.board = board;
+    noalloc_ready[dev] = true;
+  }
+  *out = &c;
+  return SMP_OK;
+}
+
+}  // namespace
+
+extern "C" int smp_sample_noalloc(const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                                  const uint32_t* bitmask, const smp_row_params* params,
+                                  int32_t* tokens, int32_t* row_status, uint32_t* kept_mask,
+                                  int32_t* kept_count, smp_stream stream) {
+  const int dt = (int)dtype;
+  if (!logits || !params || !tokens || !row_status) return SMP_ERR_INVALID_PARAM;
+  if (dt != DT_F32 && dt != DT_BF16 && dt != DT_F16) return SMP_ERR_INVALID_PARAM;
+  if (B < 0 || V < 1 || ld < V) return SMP_ERR_INVALID_PARAM;
+  // the board's per-job chunk-mass table covers MAXCH staging chunks of a row
+  if ((long long)V > (long long)MAXCH * chunk_elems(dt)) return SMP_ERR_CAPACITY;
+  if (B == 0) return SMP_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SMP_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return SMP_ERR_CAPACITY;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  smp_ctx* c = nullptr;
+  const int rc = noalloc_setup(dev, st, &c);
+  if (rc != SMP_OK) return rc;
+  return launch(c, MODE_SAMPLE, logits, dt, B, V, ld, bitmask, params, tokens, row_status,
+                kept_mask, kept_count, nullptr, stream);
+}
