@@ -133,7 +133,7 @@ int smp_argmax(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, 
  * Arguments, outputs and statuses are those of smp_sample.  The call runs on
  * the CURRENT CUDA device.  The caller passes every input and output.
  * Scratch: the job board that smp_create would allocate is instead a static
- * device array of 1,705,728 bytes.  Every device that loads the library
+ * device array of 2,001,664 bytes.  Every device that loads the library
  * holds it until the process exits.
  * Set-up: the first call on each device does the set-up, with that device
  * current.  It configures the kernels, looks up the array's device address

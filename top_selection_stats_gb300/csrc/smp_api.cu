@@ -122,8 +122,10 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   a.use_tma = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
   std::memcpy(a.delta, h->delta, sizeof(a.delta));
 
-  // one CTA per row, at most two resident per SM; CTAs loop over rows
-  const int grid = B < h->grid_max ? B : h->grid_max;
+  // one CTA per row, at most two resident per SM; CTAs loop over rows.  With
+  // a job board the whole resident grid is launched: CTAs without a row take
+  // chunk tasks of the slow rows from the start.
+  const int grid = (B < h->grid_max && !h->board) ? B : h->grid_max;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (dt) {
@@ -269,7 +271,7 @@ const char* smp_status_string(int code) {
 // ---------------------------------------------------------------------------
 namespace {
 constexpr size_t NOALLOC_SCRATCH_BYTES = (sizeof(Board) + 255) / 256 * 256;
-static_assert(NOALLOC_SCRATCH_BYTES == 1705728, "the scratch size is stated in smp.h");
+static_assert(NOALLOC_SCRATCH_BYTES == 2001664, "the scratch size is stated in smp.h");
 constexpr int NOALLOC_MAX_DEVICES = 64;
 }  // namespace
 

@@ -26,21 +26,37 @@ constexpr int SEG_MAX = 3072;       // id segments of the list sampler
 constexpr int GMAX = 512;           // ids per segment, at most
 constexpr int NOID = 0x7fffffff;
 
-// Job board (device workspace owned by the handle): rows whose kept set is
-// decided by a weight-histogram bracket publish their band pass as one task
-// per chunk; CTAs that have finished their own rows claim and run tasks.
+// Weight histogram of the mass stream: bin = floor(HOFF - HS * a) with a =
+// (x - ref) * log2(e) / T, clamped to [0, WBINS): HS bins per factor of two.
+constexpr int WBINS = 2048;
+constexpr int WHS = 16;
+constexpr int WHOFF = 256;
+
+// Job board (device workspace owned by the handle).  A row that would pass
+// over its chunks on its own for long publishes the pass as a job, one task
+// per chunk (chunks c0 .. c0 + ntask - 1): the mass stream of a row whose
+// kept set is predicted to be large (kind JOB_STREAM), and the band pass over
+// a weight-histogram bracket (JOB_BAND).  CTAs without a row of their own, or
+// done with theirs, claim and run tasks; the owner runs tasks too and waits
+// (bounded) only for tasks already claimed.
 constexpr int MAXJOBS = 32;
+constexpr int JOB_BAND = 0, JOB_STREAM = 1;
 struct JobHdr {
-  int ready, row, b_lo, b_hi;
-  float nref, nm, c2, pad;
+  int ready, row, kind, ntask;
+  int c0, b_lo, b_hi, pad0;
+  float nref, nm, c2, pad1;
   int claimed, done, list_n, above_n;
+  uint32_t mxk;  // stream: largest key of the tasks' chunks
+  int nleg, nf, pad2;
 };
 struct Board {
   int njobs, ctas_done, exits, pad;
   JobHdr hdr[MAXJOBS];
-  float cmass[MAXJOBS][MAXCH * NWARP];
-  uint32_t lk[MAXJOBS][CAP];
+  float cmass[MAXJOBS][MAXCH * NWARP];  // band: per-(chunk, warp) masses above the bracket
+  uint32_t lk[MAXJOBS][CAP];            // band: bracket elements (key, id)
   int li[MAXJOBS][CAP];
+  uint32_t wh[MAXJOBS][WBINS];          // stream: weight histogram of the tasks' chunks
+  double zc[MAXJOBS][MAXCH];            // stream: mass of each task's chunk
 };
 
 struct KArgs {
@@ -80,17 +96,12 @@ struct Sh {
   int nf;                     // NaN / +inf seen in a legal slot
   int timeout;                // a bounded wait expired
   int gn;                     // gathered entries of the sampled segment
+  int tn;                     // list entries of the current board task
   int bi[8];                  // broadcast ints
   uint32_t bu[8];             // broadcast keys
   uint64_t bq[4];             // broadcast masses
   double bd[4];               // broadcast doubles
 };
-
-// Weight histogram of the mass stream: bin = floor(HOFF - HS * a) with a =
-// (x - ref) * log2(e) / T, clamped to [0, WBINS): HS bins per factor of two.
-constexpr int WBINS = 2048;
-constexpr int WHS = 16;
-constexpr int WHOFF = 256;
 
 constexpr int SMEM_RING = NSTAGE * STAGE_BYTES;
 constexpr int SMEM_LIST = CAP * 8;

@@ -225,9 +225,10 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
 
 // ---------------------------------------------------------------------------
 // One chunk of a published band pass (job j of the board), run by the whole
-// CTA -- the row's owner or a helper between rows: the same classification
-// as band_kept_pass, with the bracket elements appended to the job's list,
-// the cell masses stored in the job and the counts added to its header.
+// CTA -- the row's owner or a helper: the same classification as
+// band_kept_pass.  Bracket elements collect in this CTA's list area first and
+// are then copied behind one reservation in the job's list; the cell masses
+// go to the job and the counts to its header.
 // ---------------------------------------------------------------------------
 template <int DT>
 __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
@@ -245,6 +246,7 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
   X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
   X.c2 = c2;
   uint32_t* mrow = a.kept_mask ? a.kept_mask + (size_t)row * X.W : nullptr;
+  if (threadIdx.x == 0) X.sh->tn = 0;
   __syncthreads();
   if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
   const char* stage = ring_wait(X, c);
@@ -271,23 +273,22 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
     }
     nk += __popc(kb);
     put_mask_word<DT>(X, mrow, kb, id0);
-    if (cm) {
-      int pos = atomicAdd((int*)&H->list_n, __popc(cm));
-      while (cm) {
-        const int q = __ffs(cm) - 1;
-        cm &= cm - 1u;
-        if (pos < CAP) {
-          bd->lk[j][pos] = bits_key<DT>(elem_bits_dyn<DT>(r, q));
-          bd->li[j][pos] = id0 + q;
-        }
-        ++pos;
-      }
-    }
+    if (cm) lane_append<DT>(X.lk, X.li, &X.sh->tn, r, id0, cm);
   }
   const float ws = warp_sum(cs);
   if (lane == 0) bd->cmass[j][c * NWARP + warp] = ws;
   nk = __reduce_add_sync(0xffffffffu, nk);
   if (lane == 0 && nk) atomicAdd((int*)&H->above_n, nk);
+  __syncthreads();
+  const int n = X.sh->tn;
+  if (threadIdx.x == 0) X.sh->bi[4] = n ? atomicAdd((int*)&H->list_n, n) : 0;
+  __syncthreads();
+  const int base = X.sh->bi[4];
+  const int ncopy = min(min(n, CAP), CAP - base);
+  for (int i = threadIdx.x; i < ncopy; i += NT) {
+    bd->lk[j][base + i] = X.lk[i];
+    bd->li[j][base + i] = X.li[i];
+  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) atomicAdd((int*)&H->done, 1);

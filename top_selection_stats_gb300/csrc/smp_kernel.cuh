@@ -197,85 +197,57 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
 }
 
 // ---------------------------------------------------------------------------
-// Job board.  The owner of a bracketed row publishes its band pass (one task
+// Band jobs.  The owner of a bracketed row publishes its band pass (one task
 // per chunk), runs tasks itself, waits (bounded) for the tasks others
 // claimed, and gathers the list, the cell masses and the count above the
-// bracket.  No wait depends on a helper starting: a task is only waited for
-// once some CTA has claimed it.
+// bracket.
 // ---------------------------------------------------------------------------
-template <int DT>
-__device__ int publish_job(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm) {
-  Board* bd = X.a->board;
-  if (!bd) return -1;
-  if (threadIdx.x == 0) {
-    int j = atomicAdd(&bd->njobs, 1);
-    if (j < MAXJOBS) {
-      JobHdr* H = &bd->hdr[j];
-      H->row = X.row;
-      H->b_lo = b_lo;
-      H->b_hi = b_hi;
-      H->nref = nref;
-      H->nm = nm;
-      H->c2 = X.c2;
-      __threadfence();
-      atomicExch(&H->ready, 1);
-    } else {
-      j = -1;
-    }
-    X.sh->bi[0] = j;
+// Copies n16 16-byte words from global (written by other CTAs: read at L2)
+// to shared memory, at most PER per thread, loads first.
+template <int PER>
+__device__ __forceinline__ void gather16(uint4* dst, const uint4* src, int n16) {
+  uint4 v[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int i = threadIdx.x + q * NT;
+    if (i < n16) v[q] = __ldcg(src + i);
   }
-  __syncthreads();
-  const int j = X.sh->bi[0];
-  __syncthreads();
-  return j;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int i = threadIdx.x + q * NT;
+    if (i < n16) dst[i] = v[q];
+  }
 }
 
-// Runs tasks of job j until all are claimed, then waits for the claimed ones;
-// returns the list length (-1 if a bounded wait expired).
+// Runs tasks of band job j until all are claimed, waits for the claimed ones
+// and gathers the job; returns the list length (-1 if a bounded wait expired).
 template <int DT>
 __device__ __noinline__ int run_job(Ctx<DT>& X, int j, BandOut& bo) {
   Board* bd = X.a->board;
-  volatile JobHdr* H = &bd->hdr[j];
 #pragma unroll 1
-  while (true) {
-    if (threadIdx.x == 0) X.sh->bi[0] = atomicAdd((int*)&H->claimed, 1);
-    __syncthreads();
-    const int t = X.sh->bi[0];
-    __syncthreads();
-    if (t >= X.nch) break;
-    band_task(X, j, t);
-  }
-  if (threadIdx.x == 0) {
-    const long long t0 = clock64();
-    int ok = 1;
-    while (H->done < X.nch) {
-      if (clock64() - t0 > 4000000000ll) {
-        ok = 0;
-        break;
-      }
-      __nanosleep(200);
-    }
-    __threadfence();
-    X.sh->bi[0] = ok;
-    X.sh->bi[1] = H->list_n;
-    X.sh->bi[2] = H->above_n;
-  }
-  __syncthreads();
-  const int ok = X.sh->bi[0], ln = X.sh->bi[1];
-  bo.above_n = X.sh->bi[2];
+  for (int t = claim_task(X, j); t < X.nch; t = claim_task(X, j)) band_task(X, j, t);
+  if (!wait_job(X, j, X.nch)) return -1;
+  volatile JobHdr* H = &bd->hdr[j];
+  const int ln = H->list_n;
+  bo.above_n = H->above_n;
   bo.above_q = 0;
-  if (!ok) {
-    if (threadIdx.x == 0) X.sh->timeout = 1;
-    __syncthreads();
-    return -1;
+  // list and cell masses: 16-byte loads, each batch issued before its stores
+  const int n4 = (min(ln, CAP) + 3) / 4;
+  gather16<CAP / 4 / NT>(reinterpret_cast<uint4*>(X.lk), reinterpret_cast<const uint4*>(bd->lk[j]), n4);
+  gather16<CAP / 4 / NT>(reinterpret_cast<uint4*>(X.li), reinterpret_cast<const uint4*>(bd->li[j]), n4);
+  const int nc = X.nch * NWARP;
+  constexpr int PC = (MAXCH * NWARP) / NT;
+  float cm[PC];
+#pragma unroll
+  for (int q = 0; q < PC; ++q) {
+    const int f = threadIdx.x + q * NT;
+    cm[q] = (f < nc) ? __ldcg(&bd->cmass[j][f]) : 0.f;
   }
-  const int n = min(ln, CAP);
-  for (int i = threadIdx.x; i < n; i += NT) {
-    X.lk[i] = bd->lk[j][i];
-    X.li[i] = bd->li[j][i];
+#pragma unroll
+  for (int q = 0; q < PC; ++q) {
+    const int f = threadIdx.x + q * NT;
+    if (f < nc) X.sh->cmass[f / NWARP][f % NWARP] = cm[q];
   }
-  for (int f = threadIdx.x; f < X.nch * NWARP; f += NT)
-    X.sh->cmass[f / NWARP][f % NWARP] = bd->cmass[j][f];
   if (threadIdx.x == 0) X.sh->n = ln;
   __syncthreads();
   return ln;
@@ -285,7 +257,7 @@ __device__ __noinline__ int run_job(Ctx<DT>& X, int j, BandOut& bo) {
 // slot is free, else run by this CTA alone.  Returns the list length.
 template <int DT>
 __device__ int band_any(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm, BandOut& bo) {
-  const int j = publish_job(X, b_lo, b_hi, nref, nm);
+  const int j = publish_job(X, JOB_BAND, 0, X.nch, b_lo, b_hi, nref, nm);
   int ln;
   if (j >= 0) {
     ln = run_job(X, j, bo);
@@ -312,27 +284,31 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
       int jj = -1, tt = -1, stop = 0;
       const int nj = min(vb->njobs, MAXJOBS);
       for (int q = 0; q < nj && jj < 0; ++q) {
-        if (!vb->hdr[q].ready || vb->hdr[q].claimed >= X.nch) continue;
+        if (!vb->hdr[q].ready || vb->hdr[q].claimed >= vb->hdr[q].ntask) continue;
         const int t = atomicAdd(&bd->hdr[q].claimed, 1);
-        if (t < X.nch) {
+        if (t < vb->hdr[q].ntask) {
           jj = q;
-          tt = t;
+          tt = vb->hdr[q].c0 + t;
         }
       }
       __threadfence();  // the job's header is read after its ready flag
       if (jj < 0) {
         if (vb->ctas_done >= (int)gridDim.x || clock64() - t0 > 4000000000ll) stop = 1;
-        else __nanosleep(400);
+        else __nanosleep(200);
       }
       X.sh->bi[0] = jj;
       X.sh->bi[1] = tt;
       X.sh->bi[2] = stop;
+      X.sh->bi[3] = (jj >= 0) ? vb->hdr[jj].kind : 0;
     }
     __syncthreads();
-    const int jj = X.sh->bi[0], tt = X.sh->bi[1], stop = X.sh->bi[2];
+    const int jj = X.sh->bi[0], tt = X.sh->bi[1], stop = X.sh->bi[2], kind = X.sh->bi[3];
     __syncthreads();
     if (stop) break;
-    if (jj >= 0) band_task(X, jj, tt);
+    if (jj >= 0) {
+      if (kind == JOB_STREAM) stream_task(X, jj, tt);
+      else band_task(X, jj, tt);
+    }
   }
   if (threadIdx.x == 0) {
     __threadfence();
@@ -341,6 +317,8 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
       for (int q = 0; q < nj; ++q) {
         JobHdr* H = &bd->hdr[q];
         H->ready = H->claimed = H->done = H->list_n = H->above_n = 0;
+        H->mxk = 0u;
+        H->nleg = H->nf = 0;
       }
       bd->njobs = 0;
       bd->ctas_done = 0;

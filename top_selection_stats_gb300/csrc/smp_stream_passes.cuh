@@ -252,6 +252,158 @@ __device__ __forceinline__ float tree_sum(const float (&w)[EPV]) {
   }
 }
 
+// Excess-weighted weight-histogram entry of a legal element x (nref = -ref *
+// log2(e) / T): bin floor(WHOFF - WHS * a), a = x * log2(e) / T + nref,
+// clamped to [0, WBINS); the element adds 2^11 * 2^f, f = (1 - frac) / WHS
+// its weight's excess over the bin's lower edge (2^f by its quadratic
+// expansion, error < 2e-5).  Clamped elements add 2^11.
+__device__ __forceinline__ void whist_add(uint32_t* wh, float x, float c2, float nref) {
+  const float y = fmaf(fmaf(x, c2, nref), -(float)WHS, (float)WHOFF);
+  const float fy = floorf(y);
+  const int b = min(max((int)fy, 0), WBINS - 1);
+  const float f = (b == (int)fy) ? (1.f - (y - fy)) * (1.f / WHS) : 0.f;
+  atomicAdd(&wh[b], (uint32_t)fmaf(f, fmaf(f, 491.96f, 1419.57f), 2048.5f));
+}
+
+// ---------------------------------------------------------------------------
+// Job board primitives.  publish_job writes a job's header for this CTA's row
+// (fenced before the ready flag) and returns its slot, or -1 without a board
+// or a free slot.  claim_task hands out the next task index of job j to the
+// whole CTA (>= ntask: none left).  wait_job waits, bounded, until every
+// claimed task of job j is done; a helper only claims tasks it then runs, so
+// no wait depends on a CTA that has not started one.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ int publish_job(Ctx<DT>& X, int kind, int c0, int ntask, int b_lo, int b_hi,
+                           float nref, float nm) {
+  Board* bd = X.a->board;
+  if (!bd) return -1;
+  if (threadIdx.x == 0) {
+    const int j = atomicAdd(&bd->njobs, 1);
+    X.sh->bi[0] = (j < MAXJOBS) ? j : -1;
+  }
+  __syncthreads();
+  const int j = X.sh->bi[0];
+  __syncthreads();
+  if (j < 0) return -1;
+  if (kind == JOB_STREAM)
+    for (int b = threadIdx.x; b < WBINS; b += NT) bd->wh[j][b] = 0u;
+  if (threadIdx.x == 0) {
+    JobHdr* H = &bd->hdr[j];
+    H->row = X.row;
+    H->kind = kind;
+    H->c0 = c0;
+    H->ntask = ntask;
+    H->b_lo = b_lo;
+    H->b_hi = b_hi;
+    H->nref = nref;
+    H->nm = nm;
+    H->c2 = X.c2;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) atomicExch(&bd->hdr[j].ready, 1);
+  return j;
+}
+
+template <int DT>
+__device__ __forceinline__ int claim_task(Ctx<DT>& X, int j) {
+  if (threadIdx.x == 0) X.sh->bi[0] = atomicAdd(&X.a->board->hdr[j].claimed, 1);
+  __syncthreads();
+  const int t = X.sh->bi[0];
+  __syncthreads();
+  return t;
+}
+
+template <int DT>
+__device__ bool wait_job(Ctx<DT>& X, int j, int ntask) {
+  if (threadIdx.x == 0) {
+    volatile JobHdr* H = &X.a->board->hdr[j];
+    const long long t0 = clock64();
+    int ok = 1;
+    while (H->done < ntask) {
+      if (clock64() - t0 > 4000000000ll) {
+        ok = 0;
+        break;
+      }
+      __nanosleep(100);
+    }
+    __threadfence();
+    X.sh->bi[0] = ok;
+    if (!ok) X.sh->timeout = 1;
+  }
+  __syncthreads();
+  const bool ok = X.sh->bi[0] != 0;
+  __syncthreads();
+  return ok;
+}
+
+// ---------------------------------------------------------------------------
+// One chunk of a published mass stream (job j), run by the whole CTA: the
+// chunk's mass relative to the owner's reference, its legal count, largest
+// value and NaN / +inf flag, and its weight histogram (built in this CTA's
+// histogram area, then added to the job's).  The arithmetic is exp_stream's,
+// so a chunk contributes the same whichever CTA runs it.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  constexpr int EPV = ElemT<DT>::EPV;
+  const KArgs& a = *X.a;
+  Board* bd = a.board;
+  volatile JobHdr* H = &bd->hdr[j];
+  const int row = H->row;
+  const float nref = H->nref, c2 = H->c2;
+  X.row = row;
+  X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
+  X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
+  X.c2 = c2;
+  uint32_t* wh = X.wh;
+  for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
+  __syncthreads();
+  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
+  const char* stage = ring_wait(X, c);
+  const int v0 = warp_vec<DT>(0);
+  float cs = 0.f;
+  uint32_t amax = p_ninf<DT>();
+  int nleg = 0;
+#pragma unroll
+  for (int it = 0; it < ITW; ++it) {
+    const uint4 r = load_vec(X, stage, c, v0 + 32 * it);
+    amax = pmax<DT>(amax, vmax2<DT>(r));
+    float x[EPV], w[EPV];
+    unpack<DT>(r, x);
+#pragma unroll
+    for (int q = 0; q < EPV; ++q) w[q] = fast_exp2(fmaf(x[q], c2, nref));  // -inf -> 0
+    cs += tree_sum<EPV>(w);
+#pragma unroll
+    for (int q = 0; q < EPV; ++q) {
+      if (!(x[q] > -INFINITY)) continue;
+      ++nleg;
+      whist_add(wh, x[q], c2, nref);
+    }
+  }
+  const float tmax = p2f_max<DT>(amax);
+  const double zc = bsum_d((double)cs, X.sh->rd[0]);  // (its barrier also ends the histogram)
+  for (int b = threadIdx.x; b < WBINS; b += NT) {
+    const uint32_t v = wh[b];
+    if (v) atomicAdd(&bd->wh[j][b], v);
+  }
+  const int nf = bsum_i((tmax < INFINITY) ? 0 : 1, X.sh->ri[1]);
+  const float mx = bmax_f(nf ? -INFINITY : tmax, X.sh->rf[0]);
+  nleg = bsum_i(nleg, X.sh->ri[0]);
+  if (threadIdx.x == 0) {
+    bd->zc[j][c] = zc;
+    if (nf) atomicOr((int*)&H->nf, 1);
+    else if (mx > -INFINITY) atomicMax((unsigned int*)&H->mxk, fkey(mx));
+    if (nleg) atomicAdd((int*)&H->nleg, nleg);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd((int*)&H->done, 1);
+}
+
 template <int DT, bool ALLM, bool EMIT>
 __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, float ref_in,
                                           float p_hist) {
@@ -274,6 +426,7 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   uint32_t* wh = X.wh;
   uint32_t amax = p_ninf<DT>();
   int nleg = 0;
+  int js = -1;  // board slot of the shared rest of the stream
   ring_begin(X);
   RingIt<DT> R(X);
 #pragma unroll 1
@@ -320,6 +473,12 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
           if (hist) {
             for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
             __syncthreads();
+            // such a row is slow to stream (every element is histogrammed):
+            // chunks 2.. go to the job board and this CTA streams 0 and 1
+            if (X.nch > 2) {
+              js = publish_job(X, JOB_STREAM, 2, X.nch - 2, 0, 0, nref, 0.f);
+              if (js >= 0) X.nch = 2;
+            }
           }
         }
       }
@@ -342,11 +501,7 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
 #pragma unroll
         for (int j = 0; j < EPV; ++j) {
           if (!(x[j] > -INFINITY)) continue;
-          const float y = fmaf(fmaf(x[j], c2, nref), -(float)WHS, (float)WHOFF);
-          const float fy = floorf(y);
-          const int b = min(max((int)fy, 0), WBINS - 1);
-          const float f = (b == (int)fy) ? (1.f - (y - fy)) * (1.f / WHS) : 0.f;
-          atomicAdd(&wh[b], (uint32_t)fmaf(f, fmaf(f, 491.96f, 1419.57f), 2048.5f));
+          whist_add(wh, x[j], c2, nref);
         }
       }
     }
@@ -427,6 +582,33 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   o.mx = bmax_f(o.nf ? -INFINITY : tmax, X.sh->rf[0]);
   o.nleg = bsum_i(nleg, X.sh->ri[0]);
   o.ovf = X.sh->n > CAP;
+  if (EMIT && js >= 0) {
+    // the shared rest of the stream: this CTA's histogram joins the job's,
+    // the CTA runs tasks, waits for the claimed ones, then merges the job
+    // (chunk masses summed in chunk order: independent of who ran what)
+    Board* bd = X.a->board;
+    for (int b = threadIdx.x; b < WBINS; b += NT) {
+      const uint32_t v = wh[b];
+      if (v) atomicAdd(&bd->wh[js][b], v);
+    }
+    __syncthreads();
+    const int nt = Xr.nch - 2;
+#pragma unroll 1
+    for (int t = claim_task(X, js); t < nt; t = claim_task(X, js)) stream_task(X, js, 2 + t);
+    if (wait_job(X, js, nt)) {
+      volatile JobHdr* H = &bd->hdr[js];
+      const double zt = bsum_d((threadIdx.x < nt) ? __ldcg(&bd->zc[js][2 + threadIdx.x]) : 0.0,
+                               X.sh->rd[1]);
+      for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = __ldcg(&bd->wh[js][b]);
+      o.z += zt;
+      o.nleg += H->nleg;
+      o.nf |= H->nf;
+      const uint32_t mk = H->mxk;
+      o.mx = o.nf ? -INFINITY : fmaxf(o.mx, mk ? key_to_float(mk) : -INFINITY);
+    }
+    o.ovf = 1;  // the list saw chunks 0 and 1 only
+    __syncthreads();
+  }
   o.lmass = EMIT ? bsum_d((double)lm, X.sh->rd[1]) : 0.0;
   o.tkey = bits_key<DT>((DT == DT_F32) ? t2 : (t2 & 0xffffu));
   o.lkmax = EMIT ? bmax_u(lkm, X.sh->ru[0]) : 0u;
