@@ -90,8 +90,9 @@ typedef struct {
  * (shared memory, CTAs per SM) and builds the host-side sigma-truncation
  * table (Qrita paper notes, key design 1 and "training strategy": delta =
  * Phi^-1(1 - k/V) from a precomputed table).  Allocates the handle's one
- * device workspace (about 1.7 MB: the job board on which rows with very flat
- * top-p sets share their second pass across CTAs); calls allocate nothing.
+ * device workspace (1,968,896 bytes: the job board on which rows with large
+ * top-p sets share their passes over the row across CTAs); calls allocate
+ * nothing.
  * Calls on one handle must not run concurrently (issue them on one stream).
  * Returns SMP_OK, SMP_ERR_INVALID_PARAM or SMP_ERR_CUDA. */
 int smp_create(smp_handle* h, int device, int max_batch, int max_vocab);
@@ -133,7 +134,7 @@ int smp_argmax(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, 
  * Arguments, outputs and statuses are those of smp_sample.  The call runs on
  * the CURRENT CUDA device.  The caller passes every input and output.
  * Scratch: the job board that smp_create would allocate is instead a static
- * device array of 2,001,664 bytes.  Every device that loads the library
+ * device array of 1,968,896 bytes.  Every device that loads the library
  * holds it until the process exits.
  * Set-up: the first call on each device does the set-up, with that device
  * current.  It configures the kernels, looks up the array's device address

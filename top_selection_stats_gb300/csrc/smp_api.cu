@@ -271,7 +271,7 @@ const char* smp_status_string(int code) {
 // ---------------------------------------------------------------------------
 namespace {
 constexpr size_t NOALLOC_SCRATCH_BYTES = (sizeof(Board) + 255) / 256 * 256;
-static_assert(NOALLOC_SCRATCH_BYTES == 2001664, "the scratch size is stated in smp.h");
+static_assert(NOALLOC_SCRATCH_BYTES == 1968896, "the scratch size is stated in smp.h");
 constexpr int NOALLOC_MAX_DEVICES = 64;
 }  // namespace
 

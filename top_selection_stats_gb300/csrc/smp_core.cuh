@@ -33,30 +33,37 @@ constexpr int WHS = 16;
 constexpr int WHOFF = 256;
 
 // Job board (device workspace owned by the handle).  A row that would pass
-// over its chunks on its own for long publishes the pass as a job, one task
-// per chunk (chunks c0 .. c0 + ntask - 1): the mass stream of a row whose
-// kept set is predicted to be large (kind JOB_STREAM), and the band pass over
-// a weight-histogram bracket (JOB_BAND).  CTAs without a row of their own, or
-// done with theirs, claim and run tasks; the owner runs tasks too and waits
-// (bounded) only for tasks already claimed.
+// over its chunks on its own for long publishes the pass as a job: the mass
+// stream of a row whose kept set is predicted to be large (kind JOB_STREAM),
+// and the band pass over a weight-histogram bracket (JOB_BAND).  The owner
+// keeps streaming the row from the front through its ring; CTAs without a row
+// of their own, or done with theirs, take single chunks from the back.  One
+// 64-bit word holds both ends (front << 32 | back + ENDS_OFF): the owner adds
+// 1 << 32 and owns chunk `front` if front < back; a helper adds -1 and owns
+// chunk back - 1 if that is >= front.  Once the owner's claim fails, chunks
+// [front, nch) are exactly the helpers' ones, and it waits (bounded) for
+// that many tasks.  ENDS_OFF keeps failed helper claims from borrowing into
+// the front half.
 constexpr int MAXJOBS = 32;
 constexpr int JOB_BAND = 0, JOB_STREAM = 1;
+constexpr uint32_t ENDS_OFF = 1u << 20;
 struct JobHdr {
-  int ready, row, kind, ntask;
-  int c0, b_lo, b_hi, pad0;
-  float nref, nm, c2, pad1;
-  int claimed, done, list_n, above_n;
-  uint32_t mxk;  // stream: largest key of the tasks' chunks
-  int nleg, nf, pad2;
+  unsigned long long ends;
+  int ready, row, kind, nch;
+  int b_lo, b_hi, done, list_n;
+  float nref, nm, c2;
+  int above_n;
+  uint32_t mxk;  // stream: largest key of the helpers' chunks
+  int nleg, nf, pad[3];
 };
+static_assert(sizeof(JobHdr) % 16 == 0, "job headers keep the board's arrays aligned");
 struct Board {
   int njobs, ctas_done, exits, pad;
   JobHdr hdr[MAXJOBS];
-  float cmass[MAXJOBS][MAXCH * NWARP];  // band: per-(chunk, warp) masses above the bracket
-  uint32_t lk[MAXJOBS][CAP];            // band: bracket elements (key, id)
+  float cmass[MAXJOBS][MAXCH * NWARP];  // per-(chunk, warp) masses of the helpers' chunks
+  uint32_t lk[MAXJOBS][CAP];            // band: the helpers' bracket elements (key, id)
   int li[MAXJOBS][CAP];
-  uint32_t wh[MAXJOBS][WBINS];          // stream: weight histogram of the tasks' chunks
-  double zc[MAXJOBS][MAXCH];            // stream: mass of each task's chunk
+  uint32_t wh[MAXJOBS][WBINS];          // stream: weight histogram of the helpers' chunks
 };
 
 struct KArgs {
@@ -96,7 +103,6 @@ struct Sh {
   int nf;                     // NaN / +inf seen in a legal slot
   int timeout;                // a bounded wait expired
   int gn;                     // gathered entries of the sampled segment
-  int tn;                     // list entries of the current board task
   int bi[8];                  // broadcast ints
   uint32_t bu[8];             // broadcast keys
   uint64_t bq[4];             // broadcast masses

@@ -175,83 +175,17 @@ __device__ uint64_t cells_fixed_mass(Ctx<DT>& X) {
   }
   return bsum_q(s, X.sh->rq[1]);
 }
+// Band classification of one staged chunk (the body of every band pass, the
+// same arithmetic whichever CTA runs the chunk): bracket elements go to this
+// CTA's list (sh->n), elements above the bracket get their kept-mask bits and
+// count (nk) and add their weights relative to the row maximum (nm) to the
+// returned per-thread mass.
 template <int DT>
-__device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, float nref, float nm) {
-  LocalCtx<DT> lc_(Xr);
-  Ctx<DT>& X = lc_.v;
+__device__ __forceinline__ float band_chunk(Ctx<DT>& X, const char* stage, int c, int b_lo,
+                                            int b_hi, float c2, float nref, float nm,
+                                            uint32_t* mrow, int& nk) {
   constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t* mrow = X.a->kept_mask ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
-  const float c2 = X.c2;
-  if (threadIdx.x == 0) X.sh->n = 0;
-  int nk = 0;
-  ring_begin(X);
-#pragma unroll 1
-  for (int c = 0; c < X.nch; ++c) {
-    const char* stage = warp_wait(X, c);
-    float cs = 0.f;
-#pragma unroll 1
-    for (int it = 0; it < ITW; ++it) {
-      const int vi = warp_vec<DT>(it);
-      const uint4 r = load_vec(X, stage, c, vi);
-      const int id0 = c * CE + vi * EPV;
-      float x[EPV];
-      unpack<DT>(r, x);
-      uint32_t kb = 0u, cm = 0u;
-#pragma unroll
-      for (int j = 0; j < EPV; ++j) {
-        if (!(x[j] > -INFINITY)) continue;
-        const int b = wbin(x[j], c2, nref);
-        if (b < b_lo) {
-          kb |= 1u << j;
-          cs += fast_exp2(fmaf(x[j], c2, nm));
-        } else if (b <= b_hi) {
-          cm |= 1u << j;
-        }
-      }
-      nk += __popc(kb);
-      put_mask_word<DT>(X, mrow, kb, id0);
-      if (__any_sync(0xffffffffu, cm != 0u)) list_append(X, r, id0, cm);
-    }
-    const float ws = warp_sum(cs);
-    if (lane == 0) X.sh->cmass[c][warp] = ws;
-    warp_release(X, c);
-  }
-  BandOut o;
-  o.above_n = bsum_i(nk, X.sh->ri[0]);
-  o.above_q = 0;
-  return o;
-}
-
-// ---------------------------------------------------------------------------
-// One chunk of a published band pass (job j of the board), run by the whole
-// CTA -- the row's owner or a helper: the same classification as
-// band_kept_pass.  Bracket elements collect in this CTA's list area first and
-// are then copied behind one reservation in the job's list; the cell masses
-// go to the job and the counts to its header.
-// ---------------------------------------------------------------------------
-template <int DT>
-__device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
-  LocalCtx<DT> lc_(Xr);
-  Ctx<DT>& X = lc_.v;
-  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const KArgs& a = *X.a;
-  Board* bd = a.board;
-  volatile JobHdr* H = &bd->hdr[j];
-  const int row = H->row, b_lo = H->b_lo, b_hi = H->b_hi;
-  const float nref = H->nref, nm = H->nm, c2 = H->c2;
-  X.row = row;
-  X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
-  X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
-  X.c2 = c2;
-  uint32_t* mrow = a.kept_mask ? a.kept_mask + (size_t)row * X.W : nullptr;
-  if (threadIdx.x == 0) X.sh->tn = 0;
-  __syncthreads();
-  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
-  const char* stage = ring_wait(X, c);
   float cs = 0.f;
-  int nk = 0;
 #pragma unroll 1
   for (int it = 0; it < ITW; ++it) {
     const int vi = warp_vec<DT>(it);
@@ -273,14 +207,98 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
     }
     nk += __popc(kb);
     put_mask_word<DT>(X, mrow, kb, id0);
-    if (cm) lane_append<DT>(X.lk, X.li, &X.sh->tn, r, id0, cm);
+    if (__any_sync(0xffffffffu, cm != 0u)) list_append(X, r, id0, cm);
   }
-  const float ws = warp_sum(cs);
+  return cs;
+}
+
+// The band pass of a row alone (no board slot): every chunk through the ring.
+template <int DT>
+__device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, float nref, float nm) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* mrow = X.a->kept_mask ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
+  if (threadIdx.x == 0) X.sh->n = 0;
+  int nk = 0;
+  ring_begin(X);
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    const char* stage = warp_wait(X, c);
+    const float ws = warp_sum(band_chunk<DT>(X, stage, c, b_lo, b_hi, X.c2, nref, nm, mrow, nk));
+    if (lane == 0) X.sh->cmass[c][warp] = ws;
+    warp_release(X, c);
+  }
+  BandOut o;
+  o.above_n = bsum_i(nk, X.sh->ri[0]);
+  o.above_q = 0;
+  return o;
+}
+
+// The owner's side of a band job (slot j): the band pass over the chunks this
+// CTA claims from the front (two-stage ring, one block barrier per chunk).
+// Returns the first helper chunk; the list (sh->n entries), the cells and
+// above_n cover the owner's chunks.
+template <int DT>
+__device__ __noinline__ int band_owner_pass(Ctx<DT>& Xr, int j, int b_lo, int b_hi, float nref,
+                                            float nm, int& above_n) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* mrow = X.a->kept_mask ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
+  if (threadIdx.x == 0) X.sh->n = 0;
+  int nk = 0;
+  OwnerClaims<DT> oc;
+  oc.start(X, &X.a->board->hdr[j], X.nch);
+  ring_begin(X);  // chunks 0 and 1 are the owner's
+#pragma unroll 1
+  for (int c = 0; c < X.nch; ++c) {
+    if (c >= 2 && !oc.owns(X, c)) break;
+    const char* stage = ring_wait(X, c);
+    const float ws = warp_sum(band_chunk<DT>(X, stage, c, b_lo, b_hi, X.c2, nref, nm, mrow, nk));
+    if (lane == 0) X.sh->cmass[c][warp] = ws;
+    __syncthreads();
+    oc.decide(X, c + 2);
+  }
+  if (threadIdx.x == 0) X.sh->bi[1] = oc.first;
+  above_n = bsum_i(nk, X.sh->ri[0]);
+  const int first = X.sh->bi[1];
+  __syncthreads();
+  return first;
+}
+
+// ---------------------------------------------------------------------------
+// One chunk of a published band pass (job j), run by a helper: band_chunk
+// into this CTA's list area, then the entries are copied behind one
+// reservation in the job's list; the cells go to the job and the count to
+// its header.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const KArgs& a = *X.a;
+  Board* bd = a.board;
+  volatile JobHdr* H = &bd->hdr[j];
+  const int row = H->row, b_lo = H->b_lo, b_hi = H->b_hi;
+  const float nref = H->nref, nm = H->nm, c2 = H->c2;
+  X.row = row;
+  X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
+  X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
+  X.c2 = c2;
+  uint32_t* mrow = a.kept_mask ? a.kept_mask + (size_t)row * X.W : nullptr;
+  if (threadIdx.x == 0) X.sh->n = 0;
+  __syncthreads();
+  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
+  const char* stage = ring_wait(X, c);
+  int nk = 0;
+  const float ws = warp_sum(band_chunk<DT>(X, stage, c, b_lo, b_hi, c2, nref, nm, mrow, nk));
   if (lane == 0) bd->cmass[j][c * NWARP + warp] = ws;
   nk = __reduce_add_sync(0xffffffffu, nk);
   if (lane == 0 && nk) atomicAdd((int*)&H->above_n, nk);
   __syncthreads();
-  const int n = X.sh->tn;
+  const int n = X.sh->n;
   if (threadIdx.x == 0) X.sh->bi[4] = n ? atomicAdd((int*)&H->list_n, n) : 0;
   __syncthreads();
   const int base = X.sh->bi[4];

@@ -202,52 +202,50 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
 // claimed, and gathers the list, the cell masses and the count above the
 // bracket.
 // ---------------------------------------------------------------------------
-// Copies n16 16-byte words from global (written by other CTAs: read at L2)
-// to shared memory, at most PER per thread, loads first.
-template <int PER>
-__device__ __forceinline__ void gather16(uint4* dst, const uint4* src, int n16) {
-  uint4 v[PER];
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int i = threadIdx.x + q * NT;
-    if (i < n16) v[q] = __ldcg(src + i);
-  }
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int i = threadIdx.x + q * NT;
-    if (i < n16) dst[i] = v[q];
-  }
-}
-
-// Runs tasks of band job j until all are claimed, waits for the claimed ones
-// and gathers the job; returns the list length (-1 if a bounded wait expired).
+// The owner's side of band job j: its band pass from the front, a bounded wait
+// for the helpers' chunks, then their list entries (after the owner's), cells
+// and count.  Returns the list length (-1 if a bounded wait expired).
 template <int DT>
-__device__ __noinline__ int run_job(Ctx<DT>& X, int j, BandOut& bo) {
+__device__ __noinline__ int run_job(Ctx<DT>& X, int j, int b_lo, int b_hi, float nref, float nm,
+                                    BandOut& bo) {
   Board* bd = X.a->board;
-#pragma unroll 1
-  for (int t = claim_task(X, j); t < X.nch; t = claim_task(X, j)) band_task(X, j, t);
-  if (!wait_job(X, j, X.nch)) return -1;
+  int own_above = 0;
+  const int first = band_owner_pass(X, j, b_lo, b_hi, nref, nm, own_above);
+  if (!wait_job(X, j, X.nch - first)) return -1;
   volatile JobHdr* H = &bd->hdr[j];
-  const int ln = H->list_n;
-  bo.above_n = H->above_n;
+  const int n_own = X.sh->n;
+  const int n_h = H->list_n;
+  bo.above_n = own_above + H->above_n;
   bo.above_q = 0;
-  // list and cell masses: 16-byte loads, each batch issued before its stores
-  const int n4 = (min(ln, CAP) + 3) / 4;
-  gather16<CAP / 4 / NT>(reinterpret_cast<uint4*>(X.lk), reinterpret_cast<const uint4*>(bd->lk[j]), n4);
-  gather16<CAP / 4 / NT>(reinterpret_cast<uint4*>(X.li), reinterpret_cast<const uint4*>(bd->li[j]), n4);
-  const int nc = X.nch * NWARP;
-  constexpr int PC = (MAXCH * NWARP) / NT;
-  float cm[PC];
+  const int ln = n_own + n_h;
+  if (ln <= CAP) {
+    // helpers' entries: loads batched ahead of the stores
+    constexpr int PB = 8;
+#pragma unroll 1
+    for (int i0 = 0; i0 < n_h; i0 += NT * PB) {
+      uint32_t k[PB];
+      int id[PB];
 #pragma unroll
-  for (int q = 0; q < PC; ++q) {
-    const int f = threadIdx.x + q * NT;
-    cm[q] = (f < nc) ? __ldcg(&bd->cmass[j][f]) : 0.f;
-  }
+      for (int q = 0; q < PB; ++q) {
+        const int i = i0 + q * NT + threadIdx.x;
+        if (i < n_h) {
+          k[q] = __ldcg(&bd->lk[j][i]);
+          id[q] = __ldcg(&bd->li[j][i]);
+        }
+      }
 #pragma unroll
-  for (int q = 0; q < PC; ++q) {
-    const int f = threadIdx.x + q * NT;
-    if (f < nc) X.sh->cmass[f / NWARP][f % NWARP] = cm[q];
+      for (int q = 0; q < PB; ++q) {
+        const int i = i0 + q * NT + threadIdx.x;
+        if (i < n_h) {
+          X.lk[n_own + i] = k[q];
+          X.li[n_own + i] = id[q];
+        }
+      }
+    }
   }
+  for (int f = first * NWARP + threadIdx.x; f < X.nch * NWARP; f += NT)
+    X.sh->cmass[f / NWARP][f % NWARP] = __ldcg(&bd->cmass[j][f]);
+  __syncthreads();
   if (threadIdx.x == 0) X.sh->n = ln;
   __syncthreads();
   return ln;
@@ -257,10 +255,10 @@ __device__ __noinline__ int run_job(Ctx<DT>& X, int j, BandOut& bo) {
 // slot is free, else run by this CTA alone.  Returns the list length.
 template <int DT>
 __device__ int band_any(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm, BandOut& bo) {
-  const int j = publish_job(X, JOB_BAND, 0, X.nch, b_lo, b_hi, nref, nm);
+  const int j = publish_job(X, JOB_BAND, X.nch, b_lo, b_hi, nref, nm);
   int ln;
   if (j >= 0) {
-    ln = run_job(X, j, bo);
+    ln = run_job(X, j, b_lo, b_hi, nref, nm, bo);
   } else {
     bo = band_kept_pass(X, b_lo, b_hi, nref, nm);
     ln = X.sh->n;
@@ -279,27 +277,46 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
   const long long t0 = clock64();
 #pragma unroll 1
   while (true) {
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
+      // warp 0 looks at every job slot at once (lane q: slot q), then tries
+      // the open ones from a slot that depends on the CTA, so that helpers
+      // spread over the jobs
+      static_assert(MAXJOBS <= 32, "one lane per job slot");
       volatile Board* vb = bd;
-      int jj = -1, tt = -1, stop = 0;
+      const int lane = threadIdx.x;
       const int nj = min(vb->njobs, MAXJOBS);
-      for (int q = 0; q < nj && jj < 0; ++q) {
-        if (!vb->hdr[q].ready || vb->hdr[q].claimed >= vb->hdr[q].ntask) continue;
-        const int t = atomicAdd(&bd->hdr[q].claimed, 1);
-        if (t < vb->hdr[q].ntask) {
-          jj = q;
-          tt = vb->hdr[q].c0 + t;
+      bool open = false;
+      if (lane < nj && vb->hdr[lane].ready) {
+        const unsigned long long e = vb->hdr[lane].ends;
+        open = ends_front(e) < ends_back(e);
+      }
+      const uint32_t m = __ballot_sync(0xffffffffu, open);
+      int jj = -1, tt = -1, stop = 0;
+      if (lane == 0) {
+        const int rot = (int)(blockIdx.x % 32u);
+        const uint32_t rm = (m >> rot) | (rot ? (m << (32 - rot)) : 0u);
+        uint32_t left = rm;
+        while (left && jj < 0) {
+          const int q = (__ffs(left) - 1 + rot) & 31;
+          left &= left - 1u;
+          // a chunk from the back of the row (see JobHdr)
+          const unsigned long long old = atomicAdd(&bd->hdr[q].ends, ~0ull);
+          const int d = ends_back(old) - 1;
+          if (d >= ends_front(old)) {
+            jj = q;
+            tt = d;
+          }
         }
+        __threadfence();  // the job's header is read after its ready flag
+        if (jj < 0 && !m) {
+          if (vb->ctas_done >= (int)gridDim.x || clock64() - t0 > 4000000000ll) stop = 1;
+          else __nanosleep(200);
+        }
+        X.sh->bi[0] = jj;
+        X.sh->bi[1] = tt;
+        X.sh->bi[2] = stop;
+        X.sh->bi[3] = (jj >= 0) ? vb->hdr[jj].kind : 0;
       }
-      __threadfence();  // the job's header is read after its ready flag
-      if (jj < 0) {
-        if (vb->ctas_done >= (int)gridDim.x || clock64() - t0 > 4000000000ll) stop = 1;
-        else __nanosleep(200);
-      }
-      X.sh->bi[0] = jj;
-      X.sh->bi[1] = tt;
-      X.sh->bi[2] = stop;
-      X.sh->bi[3] = (jj >= 0) ? vb->hdr[jj].kind : 0;
     }
     __syncthreads();
     const int jj = X.sh->bi[0], tt = X.sh->bi[1], stop = X.sh->bi[2], kind = X.sh->bi[3];
@@ -316,7 +333,8 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
       const int nj = min(bd->njobs, MAXJOBS);
       for (int q = 0; q < nj; ++q) {
         JobHdr* H = &bd->hdr[q];
-        H->ready = H->claimed = H->done = H->list_n = H->above_n = 0;
+        H->ends = 0ull;  // reads as closed until the next publish
+        H->ready = H->done = H->list_n = H->above_n = 0;
         H->mxk = 0u;
         H->nleg = H->nf = 0;
       }

@@ -206,14 +206,36 @@ __device__ __noinline__ uint32_t list_stream(Ctx<DT>& Xr, float Kt, float vest, 
 #pragma unroll
     for (int it = 0; it < ITW; ++it) hits |= any_ge<DT>(r[it], t2, tf) ? (1u << it) : 0u;
     // once the list overflowed the row falls back: the pass only drains
-    if (hits && X.sh->n <= CAP) {
-#pragma unroll 1
+    // (one reservation per warp and chunk; the vectors are still in registers)
+    if (__any_sync(0xffffffffu, hits != 0u) && X.sh->n <= CAP) {
+      uint32_t cms[ITW];
+      int cnt = 0;
+#pragma unroll
       for (int it = 0; it < ITW; ++it) {
-        if (!((hits >> it) & 1u)) continue;
-        const int vi = v0 + 32 * it;
-        const uint4 rv = load_vec(X, stage, R.c, vi);
-        const uint32_t cm = ge_mask<DT>(rv, t2, tf, bad);
-        if (cm) kmax = max(kmax, lane_append<DT>(X.lk, X.li, &X.sh->n, rv, R.c * CE + vi * EPV, cm));
+        cms[it] = ((hits >> it) & 1u) ? ge_mask<DT>(r[it], t2, tf, bad) : 0u;
+        cnt += __popc(cms[it]);
+      }
+      const int inc = warp_incl_scan(cnt);
+      const int tot = __shfl_sync(0xffffffffu, inc, 31);
+      int base = 0;
+      if ((threadIdx.x & 31) == 31 && tot) base = atomicAdd(&X.sh->n, tot);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + inc - cnt;
+#pragma unroll
+      for (int it = 0; it < ITW; ++it) {
+        uint32_t cm = cms[it];
+        const int id0 = R.c * CE + (v0 + 32 * it) * EPV;
+        while (cm) {
+          const int j = __ffs(cm) - 1;
+          cm &= cm - 1u;
+          const uint32_t k = bits_key<DT>(elem_bits_dyn<DT>(r[it], j));
+          kmax = max(kmax, k);
+          if (pos < CAP) {
+            X.lk[pos] = k;
+            X.li[pos] = id0 + j;
+          }
+          ++pos;
+        }
       }
     }
     R.release(X);
@@ -267,15 +289,19 @@ __device__ __forceinline__ void whist_add(uint32_t* wh, float x, float c2, float
 
 // ---------------------------------------------------------------------------
 // Job board primitives.  publish_job writes a job's header for this CTA's row
-// (fenced before the ready flag) and returns its slot, or -1 without a board
-// or a free slot.  claim_task hands out the next task index of job j to the
-// whole CTA (>= ntask: none left).  wait_job waits, bounded, until every
-// claimed task of job j is done; a helper only claims tasks it then runs, so
-// no wait depends on a CTA that has not started one.
+// (fenced before the ready flag; the owner keeps chunks 0 and 1) and returns
+// its slot, or -1 without a board or a free slot.  OwnerClaims walks the
+// owner's claims from the front, one chunk ahead of the ring.  wait_job
+// waits, bounded, until n helper tasks of job j are done.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int ends_front(unsigned long long e) { return (int)(e >> 32); }
+__device__ __forceinline__ int ends_back(unsigned long long e) {
+  return (int)(uint32_t)e - (int)ENDS_OFF;
+}
+
 template <int DT>
-__device__ int publish_job(Ctx<DT>& X, int kind, int c0, int ntask, int b_lo, int b_hi,
-                           float nref, float nm) {
+__device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, float nref,
+                           float nm) {
   Board* bd = X.a->board;
   if (!bd) return -1;
   if (threadIdx.x == 0) {
@@ -290,10 +316,10 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int c0, int ntask, int b_lo, in
     for (int b = threadIdx.x; b < WBINS; b += NT) bd->wh[j][b] = 0u;
   if (threadIdx.x == 0) {
     JobHdr* H = &bd->hdr[j];
+    H->ends = (2ull << 32) | (unsigned long long)((uint32_t)nch + ENDS_OFF);
     H->row = X.row;
     H->kind = kind;
-    H->c0 = c0;
-    H->ntask = ntask;
+    H->nch = nch;
     H->b_lo = b_lo;
     H->b_hi = b_hi;
     H->nref = nref;
@@ -306,22 +332,50 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int c0, int ntask, int b_lo, in
   return j;
 }
 
+// The owner's claims (thread 0 holds the pending one).  decide(d) resolves
+// the claim of chunk d, issues d into stage d % NSTAGE when it is the
+// owner's, claims d + 1, and leaves the answer in sh->bi[6 + d % 2] for the
+// other threads (read after the next block barrier).  After the first failed
+// claim, `first` is the first helper chunk.
 template <int DT>
-__device__ __forceinline__ int claim_task(Ctx<DT>& X, int j) {
-  if (threadIdx.x == 0) X.sh->bi[0] = atomicAdd(&X.a->board->hdr[j].claimed, 1);
-  __syncthreads();
-  const int t = X.sh->bi[0];
-  __syncthreads();
-  return t;
-}
+struct OwnerClaims {
+  JobHdr* H;
+  unsigned long long pend;
+  int live, first;
+  __device__ __forceinline__ void start(Ctx<DT>& X, JobHdr* h, int nch) {
+    H = h;
+    live = 1;
+    first = nch;
+    if (threadIdx.x == 0) pend = atomicAdd(&H->ends, 1ull << 32);
+  }
+  __device__ __forceinline__ void decide(Ctx<DT>& X, int d) {
+    if (threadIdx.x != 0) return;
+    int own = 0;
+    if (live) {
+      const int f = ends_front(pend);
+      if (f < ends_back(pend)) {
+        own = 1;
+        issue_chunk(X, d, d % NSTAGE);
+        pend = atomicAdd(&H->ends, 1ull << 32);
+      } else {
+        live = 0;
+        first = f;
+      }
+    }
+    X.sh->bi[6 + (d & 1)] = own;
+  }
+  __device__ __forceinline__ bool owns(const Ctx<DT>& X, int d) const {
+    return X.sh->bi[6 + (d & 1)] != 0;
+  }
+};
 
 template <int DT>
-__device__ bool wait_job(Ctx<DT>& X, int j, int ntask) {
+__device__ bool wait_job(Ctx<DT>& X, int j, int n) {
   if (threadIdx.x == 0) {
     volatile JobHdr* H = &X.a->board->hdr[j];
     const long long t0 = clock64();
     int ok = 1;
-    while (H->done < ntask) {
+    while (H->done < n) {
       if (clock64() - t0 > 4000000000ll) {
         ok = 0;
         break;
@@ -338,36 +392,16 @@ __device__ bool wait_job(Ctx<DT>& X, int j, int ntask) {
   return ok;
 }
 
-// ---------------------------------------------------------------------------
-// One chunk of a published mass stream (job j), run by the whole CTA: the
-// chunk's mass relative to the owner's reference, its legal count, largest
-// value and NaN / +inf flag, and its weight histogram (built in this CTA's
-// histogram area, then added to the job's).  The arithmetic is exp_stream's,
-// so a chunk contributes the same whichever CTA runs it.
-// ---------------------------------------------------------------------------
+// Mass (returned: this thread's float sum), legal count, packed maximum and
+// weight-histogram entries of one staged chunk: the body of a shared mass
+// stream, the same arithmetic whichever CTA runs the chunk.
 template <int DT>
-__device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
-  LocalCtx<DT> lc_(Xr);
-  Ctx<DT>& X = lc_.v;
+__device__ __forceinline__ float mass_hist_chunk(const Ctx<DT>& X, const char* stage, int c,
+                                                 float c2, float nref, uint32_t* wh,
+                                                 uint32_t& amax, int& nleg) {
   constexpr int EPV = ElemT<DT>::EPV;
-  const KArgs& a = *X.a;
-  Board* bd = a.board;
-  volatile JobHdr* H = &bd->hdr[j];
-  const int row = H->row;
-  const float nref = H->nref, c2 = H->c2;
-  X.row = row;
-  X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
-  X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
-  X.c2 = c2;
-  uint32_t* wh = X.wh;
-  for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
-  __syncthreads();
-  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
-  const char* stage = ring_wait(X, c);
   const int v0 = warp_vec<DT>(0);
   float cs = 0.f;
-  uint32_t amax = p_ninf<DT>();
-  int nleg = 0;
 #pragma unroll
   for (int it = 0; it < ITW; ++it) {
     const uint4 r = load_vec(X, stage, c, v0 + 32 * it);
@@ -384,17 +418,46 @@ __device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
       whist_add(wh, x[q], c2, nref);
     }
   }
+  return cs;
+}
+
+// ---------------------------------------------------------------------------
+// One chunk of a published mass stream (job j), run by a helper: its
+// per-warp masses, legal count, largest value, NaN / +inf flag and weight
+// histogram (built in this CTA's histogram area, then added to the job's).
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const KArgs& a = *X.a;
+  Board* bd = a.board;
+  volatile JobHdr* H = &bd->hdr[j];
+  const int row = H->row;
+  const float nref = H->nref, c2 = H->c2;
+  X.row = row;
+  X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
+  X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
+  X.c2 = c2;
+  uint32_t* wh = X.wh;
+  for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
+  __syncthreads();
+  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
+  const char* stage = ring_wait(X, c);
+  uint32_t amax = p_ninf<DT>();
+  int nleg = 0;
+  const float cs = mass_hist_chunk<DT>(X, stage, c, c2, nref, wh, amax, nleg);
+  const float ws = warp_sum(cs);
+  if ((threadIdx.x & 31) == 0) bd->cmass[j][c * NWARP + (threadIdx.x >> 5)] = ws;
   const float tmax = p2f_max<DT>(amax);
-  const double zc = bsum_d((double)cs, X.sh->rd[0]);  // (its barrier also ends the histogram)
+  const int nf = bsum_i((tmax < INFINITY) ? 0 : 1, X.sh->ri[1]);  // (its barrier ends the histogram)
   for (int b = threadIdx.x; b < WBINS; b += NT) {
     const uint32_t v = wh[b];
     if (v) atomicAdd(&bd->wh[j][b], v);
   }
-  const int nf = bsum_i((tmax < INFINITY) ? 0 : 1, X.sh->ri[1]);
   const float mx = bmax_f(nf ? -INFINITY : tmax, X.sh->rf[0]);
   nleg = bsum_i(nleg, X.sh->ri[0]);
   if (threadIdx.x == 0) {
-    bd->zc[j][c] = zc;
     if (nf) atomicOr((int*)&H->nf, 1);
     else if (mx > -INFINITY) atomicMax((unsigned int*)&H->mxk, fkey(mx));
     if (nleg) atomicAdd((int*)&H->nleg, nleg);
@@ -419,7 +482,6 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   float tf = INFINITY;
   float ref = ref_in, nref = 0.f;
   const float c2 = X.c2;
-  double tz = 0.0;
   float lm = 0.f;
   uint32_t lkm = 0u;
   bool hist = false;
@@ -474,10 +536,11 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
             for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
             __syncthreads();
             // such a row is slow to stream (every element is histogrammed):
-            // chunks 2.. go to the job board and this CTA streams 0 and 1
+            // it goes on the job board, this CTA streams from the front and
+            // helpers take chunks from the back (this loop ends after chunk 0)
             if (X.nch > 2) {
-              js = publish_job(X, JOB_STREAM, 2, X.nch - 2, 0, 0, nref, 0.f);
-              if (js >= 0) X.nch = 2;
+              js = publish_job(X, JOB_STREAM, X.nch, 0, 0, nref, 0.f);
+              if (js >= 0) X.nch = 1;
             }
           }
         }
@@ -567,47 +630,69 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
           if ((cm >> j) & 1u) lm += fast_exp2(fmaf(x[j], c2, nref));
       }
     }
-    tz += (double)cs;
-    if (ALLM) {
+    const float ws = warp_sum(cs);
+    if (lane == 0) X.sh->cmass[c][warp] = ws;
+    R.release(X);
+  }
+  const int nch = Xr.nch;
+  int helpers = 0;  // chunks of the shared stream that helpers ran
+  if (EMIT && js >= 0) {
+    // the owner's side of the shared stream: chunk 1 is in flight, chunks
+    // from 2 on are the owner's while its claims succeed
+    Board* bd = X.a->board;
+    OwnerClaims<DT> oc;
+    oc.start(X, &bd->hdr[js], nch);
+    __syncthreads();  // every warp is done with chunk 0: its stage takes chunk 2
+    oc.decide(X, 2);
+#pragma unroll 1
+    for (int c = 1; c < nch; ++c) {
+      if (c >= 2 && !oc.owns(X, c)) break;
+      const char* stage = ring_wait(X, c);
+      const float cs = mass_hist_chunk<DT>(X, stage, c, c2, nref, wh, amax, nleg);
       const float ws = warp_sum(cs);
       if (lane == 0) X.sh->cmass[c][warp] = ws;
+      __syncthreads();
+      oc.decide(X, c + 2);
     }
-    R.release(X);
+    if (threadIdx.x == 0) X.sh->bi[0] = oc.first;
+    __syncthreads();
+    const int first = X.sh->bi[0];
+    helpers = nch - first;
+    if (wait_job(X, js, helpers)) {
+      for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] += __ldcg(&bd->wh[js][b]);
+      for (int f = first * NWARP + threadIdx.x; f < nch * NWARP; f += NT)
+        X.sh->cmass[f / NWARP][f % NWARP] = __ldcg(&bd->cmass[js][f]);
+    }
+    __syncthreads();
   }
   const float tmax = p2f_max<DT>(amax);
   ExpOut o;
-  o.z = bsum_d(tz, X.sh->rd[0]);
+  // row mass: the per-(chunk, warp) cells summed in chunk order, the same
+  // whether or not the stream was shared (the barrier: every warp's cells of
+  // its last chunk are written)
+  __syncthreads();
+  double zc = 0.0;
+  if (threadIdx.x < nch) {
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) zc += (double)X.sh->cmass[threadIdx.x][w];
+  }
+  o.z = bsum_d(zc, X.sh->rd[0]);
   o.ref = ref;
   o.nf = bsum_i((tmax < INFINITY) ? 0 : 1, X.sh->ri[1]);  // NaN or +inf in a legal slot
   o.mx = bmax_f(o.nf ? -INFINITY : tmax, X.sh->rf[0]);
   o.nleg = bsum_i(nleg, X.sh->ri[0]);
   o.ovf = X.sh->n > CAP;
   if (EMIT && js >= 0) {
-    // the shared rest of the stream: this CTA's histogram joins the job's,
-    // the CTA runs tasks, waits for the claimed ones, then merges the job
-    // (chunk masses summed in chunk order: independent of who ran what)
-    Board* bd = X.a->board;
-    for (int b = threadIdx.x; b < WBINS; b += NT) {
-      const uint32_t v = wh[b];
-      if (v) atomicAdd(&bd->wh[js][b], v);
-    }
-    __syncthreads();
-    const int nt = Xr.nch - 2;
-#pragma unroll 1
-    for (int t = claim_task(X, js); t < nt; t = claim_task(X, js)) stream_task(X, js, 2 + t);
-    if (wait_job(X, js, nt)) {
-      volatile JobHdr* H = &bd->hdr[js];
-      const double zt = bsum_d((threadIdx.x < nt) ? __ldcg(&bd->zc[js][2 + threadIdx.x]) : 0.0,
-                               X.sh->rd[1]);
-      for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = __ldcg(&bd->wh[js][b]);
-      o.z += zt;
+    // the helpers' counts, flags and maximum (their cells and histogram
+    // were merged above)
+    volatile JobHdr* H = &X.a->board->hdr[js];
+    if (helpers > 0) {
       o.nleg += H->nleg;
       o.nf |= H->nf;
       const uint32_t mk = H->mxk;
       o.mx = o.nf ? -INFINITY : fmaxf(o.mx, mk ? key_to_float(mk) : -INFINITY);
     }
-    o.ovf = 1;  // the list saw chunks 0 and 1 only
-    __syncthreads();
+    o.ovf = 1;  // the list saw chunk 0 only
   }
   o.lmass = EMIT ? bsum_d((double)lm, X.sh->rd[1]) : 0.0;
   o.tkey = bits_key<DT>((DT == DT_F32) ? t2 : (t2 & 0xffffu));
