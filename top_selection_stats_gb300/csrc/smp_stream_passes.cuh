@@ -613,21 +613,44 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
         }
       }
     }
-    if (EMIT && hits && X.sh->n <= CAP) {
+    if (EMIT && __any_sync(0xffffffffu, hits != 0u) && X.sh->n <= CAP) {
+      // one list reservation per warp and chunk
       int dummy = 0;
-#pragma unroll 1
+      uint32_t cms[ITW];
+      int cnt = 0;
+#pragma unroll
       for (int it = 0; it < ITW; ++it) {
-        if (!((hits >> it) & 1u)) continue;
+        cms[it] = ((hits >> it) & 1u)
+                      ? ge_mask<DT>(load_vec(X, stage, c, v0 + 32 * it), t2, tf, dummy)
+                      : 0u;
+        cnt += __popc(cms[it]);
+      }
+      const int inc = warp_incl_scan(cnt);
+      const int tot = __shfl_sync(0xffffffffu, inc, 31);
+      int base = 0;
+      if (lane == 31 && tot) base = atomicAdd(&X.sh->n, tot);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + inc - cnt;
+#pragma unroll
+      for (int it = 0; it < ITW; ++it) {
+        uint32_t cm = cms[it];
+        if (!cm) continue;
         const int vi = v0 + 32 * it;
         const uint4 rv = load_vec(X, stage, c, vi);
-        const uint32_t cm = ge_mask<DT>(rv, t2, tf, dummy);
-        if (!cm) continue;
-        lkm = max(lkm, lane_append<DT>(X.lk, X.li, &X.sh->n, rv, c * CE + vi * EPV, cm));
-        float x[EPV];
-        unpack<DT>(rv, x);
-#pragma unroll
-        for (int j = 0; j < EPV; ++j)
-          if ((cm >> j) & 1u) lm += fast_exp2(fmaf(x[j], c2, nref));
+        const int id0 = c * CE + vi * EPV;
+        while (cm) {
+          const int j = __ffs(cm) - 1;
+          cm &= cm - 1u;
+          const uint32_t b = elem_bits_dyn<DT>(rv, j);
+          const uint32_t k = bits_key<DT>(b);
+          lkm = max(lkm, k);
+          lm += fast_exp2(fmaf(bits_value<DT>(b), c2, nref));
+          if (pos < CAP) {
+            X.lk[pos] = k;
+            X.li[pos] = id0 + j;
+          }
+          ++pos;
+        }
       }
     }
     const float ws = warp_sum(cs);
