@@ -91,6 +91,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// 64-bit add into shared memory as two native 32-bit atomics: the low word's
+// wrap-around (seen by exactly the add that caused it) carries into the high
+// word, so after a barrier the pair reads as the exact 64-bit sum.  (A 64-bit
+// shared atomicAdd is a compare-and-swap loop, which serialises badly when
+// many lanes hit one bin.)
+__device__ __forceinline__ void smem_add_u64(uint64_t* p, uint64_t v) {
+  uint32_t* q = reinterpret_cast<uint32_t*>(p);
+  const uint32_t lo = (uint32_t)v;
+  const uint32_t hi = (uint32_t)(v >> 32);
+  const uint32_t old = atomicAdd(q, lo);
+  const uint32_t up = hi + ((old + lo < old) ? 1u : 0u);
+  if (up) atomicAdd(q + 1, up);
+}
+
 // --------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): round function and key
 // schedule from the paper.  key = (lo32 seed, hi32 seed), counter = (lo32

@@ -360,7 +360,7 @@ __device__ __noinline__ void hist_pass(Ctx<DT>& Xr, uint32_t prefix, int plen, i
         if (top == prefix) {
           const int d = (int)((k >> shift) & (uint32_t)(nb - 1));
           atomicAdd(&hc[d], 1u);
-          if (MASS) atomicAdd(reinterpret_cast<unsigned long long*>(&hm[d]), (unsigned long long)w);
+          if (MASS) smem_add_u64(&hm[d], w);
         } else {
           ++ac;
           am += w;

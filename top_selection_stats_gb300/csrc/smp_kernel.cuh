@@ -182,8 +182,7 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
     if (!in_set(lk[i], id, vF, idF)) continue;
     ++nk;
     if (a.kept_mask) atomicOr(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
-    atomicAdd(reinterpret_cast<unsigned long long*>(&extra[cell_of<DT>(id)]),
-              (unsigned long long)to_fx(wq[i]));
+    smem_add_u64(&extra[cell_of<DT>(id)], to_fx(wq[i]));
   }
   nk = bsum_i(nk, X.sh->ri[1]) + bo.above_n;
   double mtot = 0.0;

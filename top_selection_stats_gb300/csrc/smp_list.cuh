@@ -259,9 +259,8 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
       if (!f) continue;
       if (rd > 0 && (key >> (shift + wr)) != prefix) continue;
       const int d = (key >> shift) & dmask;
-      uint64_t wgt = 1;
-      if constexpr (KIND == SEL_MASS) wgt = to_fx(wq[i]);
-      atomicAdd(reinterpret_cast<unsigned long long*>(&w[d]), (unsigned long long)wgt);
+      // counts and (SEL_MASS) fixed-point masses; the other kinds weigh by count
+      if constexpr (KIND == SEL_MASS) smem_add_u64(&w[d], to_fx(wq[i]));
       atomicAdd(&c[d], 1u);
     }
     gsync<G>();
@@ -273,8 +272,8 @@ __device__ __noinline__ SelOut list_select(Ctx<DT>& Xr, int n, uint64_t target, 
       uint32_t locc = 0u;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        v[q] = w[255 - 8 * lane - q];
         cv[q] = c[255 - 8 * lane - q];
+        v[q] = (KIND == SEL_MASS) ? w[255 - 8 * lane - q] : (uint64_t)cv[q];
         loc += v[q];
         locc += cv[q];
       }
@@ -481,8 +480,7 @@ __device__ int list_draw(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, d
   for (int i = t; i < n; i += G) {
     const int id = li[i];
     if (in_set(lk[i], id, vP, idP)) {
-      atomicAdd(reinterpret_cast<unsigned long long*>(&seg[id >> sshift]),
-                (unsigned long long)to_fx(wq[i]));
+      smem_add_u64(&seg[id >> sshift], to_fx(wq[i]));
       lastk = max(lastk, id);
     }
   }
