@@ -442,7 +442,23 @@ __device__ __forceinline__ float fast_exp2(float v) {
   return r;
 }
 // Fixed-point mass of a weight in [0, 1]: w * 2^FX, truncated.
-__device__ __forceinline__ uint64_t to_fx(float w) { return __float2ull_rz(w * 1099511627776.0f); }
+// Built from the float's fields with integer operations (the float -> 64-bit
+// integer conversion runs on a slow pipe); equal to truncating w * 2^FX.
+__device__ __forceinline__ uint64_t to_fx(float w) {
+  const uint32_t b = __float_as_uint(w);
+  const int ex = (int)(b >> 23) - (127 + 23 - FX);  // weight of the significand's unit bit
+  const uint64_t m = (uint64_t)((b & 0x7fffffu) | 0x800000u);
+  if ((b >> 31) || (b >> 23) == 0u) return 0ull;  // negative, zero or subnormal
+  if (ex > 63 - 24) return ~0ull;                  // beyond 2^64 (never a weight)
+  return ex >= 0 ? (m << ex) : (ex > -24 ? (m >> -ex) : 0ull);
+}
+// floor(max(y, -1)) as an int for y < 2^22 by one round-down add of 1.5 *
+// 2^23 (no float -> int conversion, which runs at an eighth of the ALU rate);
+// y >= 2^22 (or +inf) gives at least 2^22, NaN gives -1, so callers that clamp
+// to [0, n) with n <= 2^22 get the clamped floor.
+__device__ __forceinline__ int floor_small(float y) {
+  return __float_as_int(__fadd_rd(fmaxf(y, -1.f), 12582912.0f)) - 0x4B400000;
+}
 
 // ---------------------------------------------------------------------------
 // Deterministic block reductions: warp trees, then every thread adds the

@@ -44,7 +44,7 @@ __device__ __forceinline__ uint64_t fx_weight(float x, float c2, float nm) {
 // Weight-histogram bin of x (nref = -ref * log2(e) / T, as in the mass stream).
 __device__ __forceinline__ int wbin(float x, float c2, float nref) {
   const float a = fmaf(x, c2, nref);
-  return min(max(__float2int_rd(fmaf(a, -(float)WHS, (float)WHOFF)), 0), WBINS - 1);
+  return min(max(floor_small(fmaf(a, -(float)WHS, (float)WHOFF)), 0), WBINS - 1);
 }
 
 // Writes the kept-mask word of 32 consecutive elements held by 4 (16-bit) or

@@ -274,17 +274,27 @@ __device__ __forceinline__ float tree_sum(const float (&w)[EPV]) {
   }
 }
 
-// Excess-weighted weight-histogram entry of a legal element x (nref = -ref *
-// log2(e) / T): bin floor(WHOFF - WHS * a), a = x * log2(e) / T + nref,
-// clamped to [0, WBINS); the element adds 2^11 * 2^f, f = (1 - frac) / WHS
-// its weight's excess over the bin's lower edge (2^f by its quadratic
-// expansion, error < 2e-5).  Clamped elements add 2^11.
+// Excess-weighted weight-histogram entry for y = WHOFF - WHS * a, a = (x - ref)
+// * log2(e) / T: bin floor(y) clamped to [0, WBINS); the element adds 2^11 *
+// 2^f, f = (1 - frac(y)) / WHS its weight's excess over the bin's lower edge
+// (2^f by its quadratic expansion, error < 2e-5).  Clamped elements add 2^11.
+// Floors are taken by round-down adds of a power-of-two constant, not by
+// float -> int conversions (a slower pipe).
+__device__ __forceinline__ void whist_entry(float y, int& b, uint32_t& add) {
+  // t = 1.5 * 2^23 + floor(y) for -1 <= y < 2^22 (y below -1 clamps to bin 0)
+  const float t = __fadd_rd(fmaxf(y, -1.f), 12582912.0f);
+  const int fyi = __float_as_int(t) - 0x4B400000;
+  b = min(max(fyi, 0), WBINS - 1);
+  const float fy = __fsub_rn(t, 12582912.0f);
+  const float f = (b == fyi) ? (1.f - (y - fy)) * (1.f / WHS) : 0.f;
+  const float v = fmaf(f, fmaf(f, 491.96f, 1419.57f), 2048.5f);  // in [2048.5, 2143)
+  add = (uint32_t)(__float_as_int(__fadd_rd(v, 8388608.0f)) - 0x4B000000);
+}
 __device__ __forceinline__ void whist_add(uint32_t* wh, float x, float c2, float nref) {
-  const float y = fmaf(fmaf(x, c2, nref), -(float)WHS, (float)WHOFF);
-  const float fy = floorf(y);
-  const int b = min(max((int)fy, 0), WBINS - 1);
-  const float f = (b == (int)fy) ? (1.f - (y - fy)) * (1.f / WHS) : 0.f;
-  atomicAdd(&wh[b], (uint32_t)fmaf(f, fmaf(f, 491.96f, 1419.57f), 2048.5f));
+  int b;
+  uint32_t add;
+  whist_entry(fmaf(fmaf(x, c2, nref), -(float)WHS, (float)WHOFF), b, add);
+  atomicAdd(&wh[b], add);
 }
 
 // ---------------------------------------------------------------------------
@@ -752,14 +762,10 @@ __device__ __noinline__ void whist_pass(Ctx<DT>& Xr, float nm, bool hmass) {
       for (int j = 0; j < EPV; ++j) {
         if (!(x[j] > -INFINITY)) continue;
         const float y = fmaf(fmaf(x[j], c2, nm), -(float)WHS, (float)WHOFF);
-        const float fy = floorf(y);
-        const int b = min(max((int)fy, 0), WBINS - 1);
-        uint32_t add = 1u;
-        if (hmass) {
-          const float f = (b == (int)fy) ? (1.f - (y - fy)) * (1.f / WHS) : 0.f;
-          add = (uint32_t)fmaf(f, fmaf(f, 491.96f, 1419.57f), 2048.5f);
-        }
-        atomicAdd(&wh[b], add);
+        int b;
+        uint32_t add;
+        whist_entry(y, b, add);
+        atomicAdd(&wh[b], hmass ? add : 1u);
       }
     }
     R.release(X);
