@@ -130,6 +130,69 @@ __device__ __forceinline__ uint32_t ge_mask(const uint4 r, uint32_t t2, float tf
   }
 }
 
+// Warp-cooperative append of the elements >= t of a staged chunk's hit
+// vectors.  hits (per lane): bit it marks vector (warp base + 32 it + lane)
+// as holding an element >= t or a NaN.  The warp's hit vectors are dealt out
+// one per lane, so the element tests and list writes run on all lanes at once
+// rather than on the few lanes that hold a hit, with one list reservation per
+// 32 hit vectors.  MASS: lm adds the appended elements' weights 2^(x c2 +
+// nref).  Called by all lanes; returns the largest key this lane appended.
+template <int DT, bool MASS>
+__device__ __forceinline__ uint32_t warp_append_hits(Ctx<DT>& X, const char* stage, int c,
+                                                     uint32_t hits, uint32_t t2, float tf,
+                                                     int& nf, float c2, float nref, float& lm) {
+  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE, VW = ElemT<DT>::VW;
+  const int lane = threadIdx.x & 31;
+  const int vbase = (threadIdx.x >> 5) * VW;
+  uint32_t bal[ITW];
+  int H = 0;
+#pragma unroll
+  for (int it = 0; it < ITW; ++it) {
+    bal[it] = __ballot_sync(0xffffffffu, (hits >> it) & 1u);
+    H += __popc(bal[it]);
+  }
+  uint32_t kmax = 0u;
+#pragma unroll 1
+  for (int k0 = 0; k0 < H; k0 += 32) {
+    // this lane's hit vector: the (k0 + lane)-th in (it, lane) order
+    int rem = k0 + lane, vi = -1;
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) {
+      const int pc = __popc(bal[it]);
+      if (rem >= 0 && rem < pc) vi = vbase + 32 * it + (int)__fns(bal[it], 0u, rem + 1);
+      rem -= pc;
+    }
+    uint32_t cm = 0u;
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (vi >= 0) {
+      r = load_vec(X, stage, c, vi);
+      cm = ge_mask<DT>(r, t2, tf, nf);
+    }
+    const int cnt = __popc(cm);
+    const int inc = warp_incl_scan(cnt);
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    int base = 0;
+    if (lane == 31 && tot) base = atomicAdd(&X.sh->n, tot);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int pos = base + inc - cnt;
+    const int id0 = c * CE + vi * EPV;
+    while (cm) {
+      const int j = __ffs(cm) - 1;
+      cm &= cm - 1u;
+      const uint32_t b = elem_bits_dyn<DT>(r, j);
+      const uint32_t k = bits_key<DT>(b);
+      kmax = max(kmax, k);
+      if (MASS) lm += fast_exp2(fmaf(bits_value<DT>(b), c2, nref));
+      if (pos < CAP) {
+        X.lk[pos] = k;
+        X.li[pos] = id0 + j;
+      }
+      ++pos;
+    }
+  }
+  return kmax;
+}
+
 // Bits of the elements >= tf; NaN or +inf raises nf.
 template <int DT>
 __device__ __forceinline__ uint32_t ge_bits(const uint4 r, float tf, int& nf) {

@@ -624,44 +624,8 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
       }
     }
     if (EMIT && __any_sync(0xffffffffu, hits != 0u) && X.sh->n <= CAP) {
-      // one list reservation per warp and chunk
       int dummy = 0;
-      uint32_t cms[ITW];
-      int cnt = 0;
-#pragma unroll
-      for (int it = 0; it < ITW; ++it) {
-        cms[it] = ((hits >> it) & 1u)
-                      ? ge_mask<DT>(load_vec(X, stage, c, v0 + 32 * it), t2, tf, dummy)
-                      : 0u;
-        cnt += __popc(cms[it]);
-      }
-      const int inc = warp_incl_scan(cnt);
-      const int tot = __shfl_sync(0xffffffffu, inc, 31);
-      int base = 0;
-      if (lane == 31 && tot) base = atomicAdd(&X.sh->n, tot);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      int pos = base + inc - cnt;
-#pragma unroll
-      for (int it = 0; it < ITW; ++it) {
-        uint32_t cm = cms[it];
-        if (!cm) continue;
-        const int vi = v0 + 32 * it;
-        const uint4 rv = load_vec(X, stage, c, vi);
-        const int id0 = c * CE + vi * EPV;
-        while (cm) {
-          const int j = __ffs(cm) - 1;
-          cm &= cm - 1u;
-          const uint32_t b = elem_bits_dyn<DT>(rv, j);
-          const uint32_t k = bits_key<DT>(b);
-          lkm = max(lkm, k);
-          lm += fast_exp2(fmaf(bits_value<DT>(b), c2, nref));
-          if (pos < CAP) {
-            X.lk[pos] = k;
-            X.li[pos] = id0 + j;
-          }
-          ++pos;
-        }
-      }
+      lkm = max(lkm, warp_append_hits<DT, true>(X, stage, c, hits, t2, tf, dummy, c2, nref, lm));
     }
     const float ws = warp_sum(cs);
     if (lane == 0) X.sh->cmass[c][warp] = ws;
