@@ -126,17 +126,7 @@ __device__ __noinline__ bool list_finish(Ctx<DT>& X, int n, int K, float p, uint
   }
   zero_outputs(X);
   __syncthreads();
-  bool ok;
-  if (n <= GSMALL) {
-    if (threadIdx.x < 32) {
-      ok = list_solve<32>(X, n, K, p, Pq, m_z, u, path);
-      if (threadIdx.x == 0) X.sh->bi[7] = ok ? 1 : 0;
-    }
-    __syncthreads();
-    ok = X.sh->bi[7] != 0;
-  } else {
-    ok = list_solve<NT>(X, n, K, p, Pq, m_z, u, path);
-  }
+  const bool ok = list_solve<NT>(X, n, K, p, Pq, m_z, u, path);
   __syncthreads();
   return ok;
 }
