@@ -652,7 +652,12 @@ __global__ void __launch_bounds__(NT, 2) smp_kernel(const __grid_constant__ KArg
   extern __shared__ unsigned char smem_raw[];
   char* base = reinterpret_cast<char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-  Ctx<DT> X;
+  // One context per warp in shared memory: every lane of a warp holds the
+  // same values, and functions that copy it into registers (LocalCtx) or read
+  // it in place then load from shared memory instead of the local-memory
+  // stack, which the L1 share left beside two CTAs' shared memory cannot hold.
+  __shared__ Ctx<DT> ctxw[NWARP];
+  Ctx<DT>& X = ctxw[threadIdx.x >> 5];
   X.a = &a;
   X.ring = base;
   X.lk = reinterpret_cast<uint32_t*>(base + SMEM_RING);

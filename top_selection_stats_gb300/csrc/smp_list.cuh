@@ -438,6 +438,16 @@ __device__ __noinline__ void list_range(Ctx<DT>& Xr, int n) {
   __syncthreads();
 }
 
+// Weight of a value relative to the row maximum.  Precise: the contract's
+// expf(fl32(x / T) - fl32(max / T)) (m_z = fl32(max / T)).  FAST: the base-2
+// hardware exponential of the row passes (nm = -max * log2(e) / T), so a band
+// list weighs its elements exactly as the pass that chose it.
+template <int DT, bool FAST>
+__device__ __forceinline__ float rel_weight(const Ctx<DT>& X, float x, float m_z, float nm) {
+  if (FAST) return fast_exp2(fmaf(x, X.c2, nm));
+  return expf(__fdiv_rn(x, X.temp) - m_z);
+}
+
 // Resolution of a kept set inside a list (targets already net of the part
 // of the row above the list).
 struct Res {
@@ -447,9 +457,135 @@ struct Res {
   int idP;  // S_p = S_k restricted to {key > vP} + {key == vP, id <= idP}
 };
 
+// ---------------------------------------------------------------------------
+// Selection on 16-bit keys by one count histogram.  A bf16 / fp16 value is
+// one of 2^16 keys, so when the
+// list's keys span fewer than NB16 values a histogram with one bin per key
+// gives the k-th key by suffix counts in one round, instead of radix rounds.
+// The tie quota by id comes from a gather of the boundary key's copies,
+// ranked by id when there are at most NT of them.
+// ---------------------------------------------------------------------------
+constexpr int NB16 = 4096;        // key bins
+constexpr int B16T = NB16 / NT;   // bins per thread (descending keys)
+constexpr int TG16 = 2048;        // ids gathered for a tie quota
+static_assert(CAP * 4 + NB16 * 4 + TG16 * 4 <= SMEM_RING, "16-bit selection scratch lives in the ring");
+
+template <int DT>
+__device__ __forceinline__ uint32_t* hist16(const Ctx<DT>& X) {
+  return reinterpret_cast<uint32_t*>(X.ring + CAP * 4);
+}
+template <int DT>
+__device__ __forceinline__ int* tie16(const Ctx<DT>& X) {
+  return reinterpret_cast<int*>(X.ring + CAP * 4 + NB16 * 4);
+}
+
+// Counts per key (bin key - kbase) of the list entries, of S_k members only
+// when sk is set.
+template <int DT>
+__device__ void hist16_build(Ctx<DT>& X, int n, uint32_t kbase, bool sk, uint32_t vK, int idK) {
+  uint32_t* hc = hist16(X);
+  __syncthreads();
+  for (int b = threadIdx.x; b < NB16; b += NT) hc[b] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t k = X.lk[i];
+    if (sk && !in_set(k, X.li[i], vK, idK)) continue;
+    atomicAdd(&hc[k - kbase], 1u);
+  }
+  __syncthreads();
+}
+
+// The j-th smallest id (j >= 1) among the entries with key v that are S_k
+// members; -2 when more than NT entries share the key (the caller then ranks
+// them by radix selection on ids).
+template <int DT>
+__device__ int nth_id16(Ctx<DT>& X, int n, uint32_t v, int j, uint32_t vK, int idK) {
+  int* g = tie16(X);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    X.sh->gn = 0;
+    X.sh->bi[3] = -1;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += NT) {
+    if (X.lk[i] != v) continue;
+    const int id = X.li[i];
+    if (!in_set(v, id, vK, idK)) continue;
+    const int slot = atomicAdd(&X.sh->gn, 1);
+    if (slot < TG16) g[slot] = id;
+  }
+  __syncthreads();
+  const int m = X.sh->gn;
+  if (m > NT) return -2;
+  if ((int)threadIdx.x < m) {
+    const int ida = g[threadIdx.x];
+    int r = 0;
+    for (int b = 0; b < m; ++b) r += (g[b] < ida) ? 1 : 0;  // ids are distinct
+    if (r == j - 1) X.sh->bi[3] = ida;
+  }
+  __syncthreads();
+  return X.sh->bi[3];
+}
+
+// k-th largest key: 1 = found (vK, idK), 0 = not found, -1 = the key range
+// does not fit the bins.
+template <int DT>
+__device__ __noinline__ int hsel_k16(Ctx<DT>& Xr, int n, int K, uint32_t& vK, int& idK) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const uint32_t kbase = X.sh->bu[4];
+  const uint32_t top = X.sh->bu[5] - kbase;
+  if (X.sh->bu[5] < kbase || top >= (uint32_t)NB16) return -1;
+  hist16_build(X, n, kbase, false, 0u, -1);
+  const uint32_t* hc = hist16(X);
+  const int t = threadIdx.x;
+  const int b0 = (int)top - t * B16T;  // this thread's bins b0, b0 - 1, ..., b0 - B16T + 1
+  uint32_t s = 0u;
+#pragma unroll 1
+  for (int e = 0; e < B16T; ++e) s += (b0 - e >= 0) ? hc[b0 - e] : 0u;
+  uint32_t tot;
+  uint32_t cum = bscan_excl<uint32_t>(s, X.sh->ru[0], tot);
+  if (t == 0) X.sh->bi[0] = -1;
+  __syncthreads();
+  if (cum < (uint32_t)K && cum + s >= (uint32_t)K) {
+#pragma unroll 1
+    for (int e = 0; e < B16T; ++e) {
+      const uint32_t c = (b0 - e >= 0) ? hc[b0 - e] : 0u;
+      if (c > 0u && cum + c >= (uint32_t)K) {
+        X.sh->bi[0] = b0 - e;
+        X.sh->bi[1] = (int)cum;
+        X.sh->bi[2] = (int)c;
+        break;
+      }
+      cum += c;
+    }
+  }
+  __syncthreads();
+  const int bK = X.sh->bi[0];
+  if (bK < 0) return 0;
+  const int above = X.sh->bi[1], atn = X.sh->bi[2];
+  vK = kbase + (uint32_t)bK;
+  idK = NOID;
+  const int keep = K - above;  // ties at vK kept, earliest ids first
+  if (keep < atn) {
+    idK = nth_id16(X, n, vK, keep, 0u, -1);
+    if (idK == -2) {
+      const SelOut ti = list_select<NT, DT, SEL_TIEID>(X, n, (uint64_t)keep, 0.f, 0u, NOID, vK);
+      if (!ti.ok) return 0;
+      idK = (int)(0xffffffu - ti.v);
+    }
+    if (idK < 0) return 0;
+  }
+  return 1;
+}
+
 // k-th largest key inside the list (K counted from the top of the list).
 template <int G, int DT>
 __device__ bool list_resolve_k(Ctx<DT>& X, int n, int K, uint32_t& vK, int& idK) {
+  if constexpr (DT != DT_F32 && G == NT) {
+    const int r = hsel_k16(X, n, K, vK, idK);
+    if (r >= 0) return r == 1;
+  }
   const SelOut s = list_select<G, DT, SEL_COUNT>(X, n, (uint64_t)K, 0.f, 0u, NOID, 0u);
   if (!s.ok) return false;
   vK = s.v;
@@ -461,16 +597,6 @@ __device__ bool list_resolve_k(Ctx<DT>& X, int n, int K, uint32_t& vK, int& idK)
     idK = (int)(0xffffffu - ti.v);
   }
   return true;
-}
-
-// Weight of a value relative to the row maximum.  Precise: the contract's
-// expf(fl32(x / T) - fl32(max / T)) (m_z = fl32(max / T)).  FAST: the base-2
-// hardware exponential of the row passes (nm = -max * log2(e) / T), so a band
-// list weighs its elements exactly as the pass that chose it.
-template <int DT, bool FAST>
-__device__ __forceinline__ float rel_weight(const Ctx<DT>& X, float x, float m_z, float nm) {
-  if (FAST) return fast_exp2(fmaf(x, X.c2, nm));
-  return expf(__fdiv_rn(x, X.temp) - m_z);
 }
 
 // Weights of the S_k members (others 0) into the list weight array.
