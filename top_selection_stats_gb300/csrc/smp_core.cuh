@@ -54,7 +54,9 @@ struct JobHdr {
   float nref, nm, c2;
   int above_n;
   uint32_t mxk;  // stream: largest key of the helpers' chunks
-  int nleg, nf, pad[3];
+  int nleg, nf;
+  float xa, xb;  // band: value thresholds of the bracket (above: x >= xa; band: xb <= x < xa)
+  int pad;
 };
 static_assert(sizeof(JobHdr) % 16 == 0, "job headers keep the board's arrays aligned");
 struct Board {

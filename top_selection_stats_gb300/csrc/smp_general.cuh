@@ -175,39 +175,88 @@ __device__ uint64_t cells_fixed_mass(Ctx<DT>& X) {
   }
   return bsum_q(s, X.sh->rq[1]);
 }
+// Smallest legal value x whose weight-histogram bin (relative to nref) is at
+// most bmax, or +inf: the bin is monotone in x, so a bisection over the
+// element type's order-preserving keys finds it.
+template <int DT>
+__device__ float first_value_in_bins(float c2, float nref, int bmax) {
+  uint32_t lo = ElemT<DT>::KLOW - 1u, hi = ElemT<DT>::KPINF;  // sentinels: lo fails, hi passes
+  while (hi - lo > 1u) {
+    const uint32_t mid = lo + ((hi - lo) >> 1);
+    if (wbin(key_value<DT>(mid), c2, nref) <= bmax) hi = mid;
+    else lo = mid;
+  }
+  return (hi == ElemT<DT>::KPINF) ? INFINITY : key_value<DT>(hi);
+}
+// Value thresholds of a bracket [b_lo, b_hi]: above it <=> x >= xa; inside
+// it <=> xb <= x < xa.
+template <int DT>
+__device__ void band_thresholds(float c2, float nref, int b_lo, int b_hi, float& xa, float& xb) {
+  xa = first_value_in_bins<DT>(c2, nref, b_lo - 1);
+  xb = first_value_in_bins<DT>(c2, nref, b_hi);
+}
+
 // Band classification of one staged chunk (the body of every band pass, the
 // same arithmetic whichever CTA runs the chunk): bracket elements go to this
 // CTA's list (sh->n), elements above the bracket get their kept-mask bits and
 // count (nk) and add their weights relative to the row maximum (nm) to the
-// returned per-thread mass.
+// returned per-thread mass.  The bracket is tested as two value thresholds
+// (packed compares), and the chunk's bracket elements are appended behind
+// one list reservation per warp.
 template <int DT>
-__device__ __forceinline__ float band_chunk(Ctx<DT>& X, const char* stage, int c, int b_lo,
-                                            int b_hi, float c2, float nref, float nm,
-                                            uint32_t* mrow, int& nk) {
+__device__ __forceinline__ float band_chunk(Ctx<DT>& X, const char* stage, int c, float xa,
+                                            float xb, float c2, float nm, uint32_t* mrow, int& nk) {
   constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
+  const uint32_t xa2 = pack_down<DT>(xa), xb2 = pack_down<DT>(xb);
+  int dummy = 0;
   float cs = 0.f;
-#pragma unroll 1
+  uint32_t cms[ITW];
+  uint32_t anyb = 0u;
+#pragma unroll
   for (int it = 0; it < ITW; ++it) {
     const int vi = warp_vec<DT>(it);
     const uint4 r = load_vec(X, stage, c, vi);
     const int id0 = c * CE + vi * EPV;
-    float x[EPV];
-    unpack<DT>(r, x);
-    uint32_t kb = 0u, cm = 0u;
+    const uint32_t kb = ge_mask<DT>(r, xa2, xa, dummy);
+    cms[it] = ge_mask<DT>(r, xb2, xb, dummy) & ~kb;
+    anyb |= cms[it];
+    if (__any_sync(0xffffffffu, kb != 0u)) {
+      float x[EPV];
+      unpack<DT>(r, x);
 #pragma unroll
-    for (int q = 0; q < EPV; ++q) {
-      if (!(x[q] > -INFINITY)) continue;
-      const int b = wbin(x[q], c2, nref);
-      if (b < b_lo) {
-        kb |= 1u << q;
-        cs += fast_exp2(fmaf(x[q], c2, nm));
-      } else if (b <= b_hi) {
-        cm |= 1u << q;
-      }
+      for (int q = 0; q < EPV; ++q)
+        if ((kb >> q) & 1u) cs += fast_exp2(fmaf(x[q], c2, nm));
     }
     nk += __popc(kb);
     put_mask_word<DT>(X, mrow, kb, id0);
-    if (__any_sync(0xffffffffu, cm != 0u)) list_append(X, r, id0, cm);
+  }
+  if (__any_sync(0xffffffffu, anyb != 0u)) {
+    int cnt = 0;
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) cnt += __popc(cms[it]);
+    const int inc = warp_incl_scan(cnt);
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    int base = 0;
+    if ((threadIdx.x & 31) == 31 && tot) base = atomicAdd(&X.sh->n, tot);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int pos = base + inc - cnt;
+#pragma unroll
+    for (int it = 0; it < ITW; ++it) {
+      uint32_t cm = cms[it];
+      if (!cm) continue;
+      const int vi = warp_vec<DT>(it);
+      const uint4 r = load_vec(X, stage, c, vi);
+      const int id0 = c * CE + vi * EPV;
+      while (cm) {
+        const int q = __ffs(cm) - 1;
+        cm &= cm - 1u;
+        if (pos < CAP) {
+          X.lk[pos] = bits_key<DT>(elem_bits_dyn<DT>(r, q));
+          X.li[pos] = id0 + q;
+        }
+        ++pos;
+      }
+    }
   }
   return cs;
 }
@@ -221,11 +270,13 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
   uint32_t* mrow = X.a->kept_mask ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
   if (threadIdx.x == 0) X.sh->n = 0;
   int nk = 0;
+  float xa, xb;
+  band_thresholds<DT>(X.c2, nref, b_lo, b_hi, xa, xb);
   ring_begin(X);
 #pragma unroll 1
   for (int c = 0; c < X.nch; ++c) {
     const char* stage = warp_wait(X, c);
-    const float ws = warp_sum(band_chunk<DT>(X, stage, c, b_lo, b_hi, X.c2, nref, nm, mrow, nk));
+    const float ws = warp_sum(band_chunk<DT>(X, stage, c, xa, xb, X.c2, nm, mrow, nk));
     if (lane == 0) X.sh->cmass[c][warp] = ws;
     warp_release(X, c);
   }
@@ -248,6 +299,7 @@ __device__ __noinline__ int band_owner_pass(Ctx<DT>& Xr, int j, int b_lo, int b_
   uint32_t* mrow = X.a->kept_mask ? X.a->kept_mask + (size_t)X.row * X.W : nullptr;
   if (threadIdx.x == 0) X.sh->n = 0;
   int nk = 0;
+  const float xa = X.a->board->hdr[j].xa, xb = X.a->board->hdr[j].xb;
   OwnerClaims<DT> oc;
   oc.start(X, &X.a->board->hdr[j], X.nch);
   ring_begin(X);  // chunks 0 and 1 are the owner's
@@ -255,7 +307,7 @@ __device__ __noinline__ int band_owner_pass(Ctx<DT>& Xr, int j, int b_lo, int b_
   for (int c = 0; c < X.nch; ++c) {
     if (c >= 2 && !oc.owns(X, c)) break;
     const char* stage = ring_wait(X, c);
-    const float ws = warp_sum(band_chunk<DT>(X, stage, c, b_lo, b_hi, X.c2, nref, nm, mrow, nk));
+    const float ws = warp_sum(band_chunk<DT>(X, stage, c, xa, xb, X.c2, nm, mrow, nk));
     if (lane == 0) X.sh->cmass[c][warp] = ws;
     __syncthreads();
     oc.decide(X, c + 2);
@@ -281,8 +333,8 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
   const KArgs& a = *X.a;
   Board* bd = a.board;
   volatile JobHdr* H = &bd->hdr[j];
-  const int row = H->row, b_lo = H->b_lo, b_hi = H->b_hi;
-  const float nref = H->nref, nm = H->nm, c2 = H->c2;
+  const int row = H->row;
+  const float nm = H->nm, c2 = H->c2, xa = H->xa, xb = H->xb;
   X.row = row;
   X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
   X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
@@ -293,7 +345,7 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
   if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
   const char* stage = ring_wait(X, c);
   int nk = 0;
-  const float ws = warp_sum(band_chunk<DT>(X, stage, c, b_lo, b_hi, c2, nref, nm, mrow, nk));
+  const float ws = warp_sum(band_chunk<DT>(X, stage, c, xa, xb, c2, nm, mrow, nk));
   if (lane == 0) bd->cmass[j][c * NWARP + warp] = ws;
   nk = __reduce_add_sync(0xffffffffu, nk);
   if (lane == 0 && nk) atomicAdd((int*)&H->above_n, nk);
@@ -693,7 +745,10 @@ __device__ __noinline__ int sample_tail(Ctx<DT>& Xr, double u, uint32_t vF, int 
   if (threadIdx.x == 0) X.sh->bi[6] = -1;
   __syncthreads();
   if (warp == ws) {
-    double base = 0.0;
+    // the cell's own scan runs in fp32 relative to the cell start (its error
+    // is a few fp32 ulps of the cell's mass; fp64 arithmetic is slow here)
+    const float Tf = (float)Tl;
+    float base = 0.f;
     int found = -1, lastk = -1;
 #pragma unroll 1
     for (int it = 0; it < ITW; ++it) {
@@ -701,7 +756,6 @@ __device__ __noinline__ int sample_tail(Ctx<DT>& Xr, double u, uint32_t vF, int 
       const uint4 r = load_vec(X, stage, cs, vi);
       const int id0 = cs * CE + vi * EPV;
       float w[EPV];
-      float vs = 0.f;
 #pragma unroll
       for (int j = 0; j < EPV; ++j) {
         const uint32_t b = elem_bits<DT>(r, j);
@@ -711,19 +765,19 @@ __device__ __noinline__ int sample_tail(Ctx<DT>& Xr, double u, uint32_t vF, int 
           w[j] = fast_exp2(fmaf(x, X.c2, nm));
           lastk = id0 + j;
         }
-        vs += w[j];
       }
-      const double vd = (double)vs;
-      const double inc = warp_incl_scan(vd);
-      const double pre = base + inc - vd;
-      if (found < 0 && vd > 0.0 && pre <= Tl && pre + vd > Tl) {
-        double cum = pre;
+      const float vs = tree_sum<EPV>(w);
+      const float inc = warp_incl_scan(vs);
+      const float pre = base + (inc - vs);
+      // the first vector in id order whose end passes T (the smallest id wins)
+      if (found < 0 && vs > 0.f && pre + vs > Tf) {
+        float cum = pre;
         int tok = -1, lastj = -1;
 #pragma unroll
         for (int j = 0; j < EPV; ++j) {
           if (w[j] > 0.f) lastj = id0 + j;
-          cum += (double)w[j];
-          if (tok < 0 && w[j] > 0.f && cum > Tl) tok = id0 + j;
+          cum += w[j];
+          if (tok < 0 && w[j] > 0.f && cum > Tf) tok = id0 + j;
         }
         found = tok >= 0 ? tok : lastj;
       }

@@ -244,7 +244,9 @@ __device__ __noinline__ int run_job(Ctx<DT>& X, int j, int b_lo, int b_hi, float
 // slot is free, else run by this CTA alone.  Returns the list length.
 template <int DT>
 __device__ int band_any(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm, BandOut& bo) {
-  const int j = publish_job(X, JOB_BAND, X.nch, b_lo, b_hi, nref, nm);
+  float xa, xb;
+  band_thresholds<DT>(X.c2, nref, b_lo, b_hi, xa, xb);
+  const int j = publish_job(X, JOB_BAND, X.nch, b_lo, b_hi, nref, nm, xa, xb);
   int ln;
   if (j >= 0) {
     ln = run_job(X, j, b_lo, b_hi, nref, nm, bo);

@@ -311,7 +311,7 @@ __device__ __forceinline__ int ends_back(unsigned long long e) {
 
 template <int DT>
 __device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, float nref,
-                           float nm) {
+                           float nm, float xa = INFINITY, float xb = INFINITY) {
   Board* bd = X.a->board;
   if (!bd) return -1;
   if (threadIdx.x == 0) {
@@ -335,6 +335,8 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, fl
     H->nref = nref;
     H->nm = nm;
     H->c2 = X.c2;
+    H->xa = xa;
+    H->xb = xb;
   }
   __threadfence();
   __syncthreads();
