@@ -340,9 +340,11 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
   X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
   X.c2 = c2;
   uint32_t* mrow = a.kept_mask ? a.kept_mask + (size_t)row * X.W : nullptr;
-  if (threadIdx.x == 0) X.sh->n = 0;
+  if (threadIdx.x == 0) {
+    issue_chunk(X, c, c % NSTAGE);  // (the previous task's last barrier freed the stage)
+    X.sh->n = 0;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
   const char* stage = ring_wait(X, c);
   int nk = 0;
   const float ws = warp_sum(band_chunk<DT>(X, stage, c, xa, xb, c2, nm, mrow, nk));

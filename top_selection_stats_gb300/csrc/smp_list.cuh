@@ -579,6 +579,89 @@ __device__ __noinline__ int hsel_k16(Ctx<DT>& Xr, int n, int K, uint32_t& vK, in
   return 1;
 }
 
+// Top-p boundary among the S_k members of a list weighed by the pass
+// exponential (as list_resolve_p): every copy of a key has the same weight, so
+// each bin's fixed-point mass is count * the key's weight (the same integer as
+// summing the copies).  1 = found, 0 = not found, -1 = the key range does not
+// fit the bins.
+template <int DT, bool FAST>
+__device__ __noinline__ int hsel_p16(Ctx<DT>& Xr, int n, uint64_t target, float p, float m_z,
+                                     float nm, Res& R, uint64_t& kept_mass, int* kept_n) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const uint32_t kbase = X.sh->bu[4];
+  const uint32_t top = X.sh->bu[5] - kbase;
+  if (X.sh->bu[5] < kbase || top >= (uint32_t)NB16) return -1;
+  hist16_build(X, n, kbase, true, R.vK, R.idK);
+  const uint32_t* hc = hist16(X);
+  const int t = threadIdx.x;
+  const int b0 = (int)top - t * B16T;  // this thread's bins b0, b0 - 1, ..., b0 - B16T + 1
+  uint64_t s = 0;
+#pragma unroll 1
+  for (int e = 0; e < B16T; ++e) {
+    const int b = b0 - e;
+    const uint32_t c = (b >= 0) ? hc[b] : 0u;
+    if (c) s += (uint64_t)c * to_fx(rel_weight<DT, FAST>(X, key_value<DT>(kbase + (uint32_t)b), m_z, nm));
+  }
+  uint64_t tot;
+  uint64_t cum = bscan_excl<uint64_t>(s, X.sh->rq[0], tot);
+  if (!target) {
+    target = (uint64_t)ceil((double)p * (double)tot);
+    if (target == 0) target = 1;
+  }
+  if (t == 0) X.sh->bi[0] = -1;
+  __syncthreads();
+  if (cum < target && cum + s >= target) {
+#pragma unroll 1
+    for (int e = 0; e < B16T; ++e) {
+      const int b = b0 - e;
+      const uint32_t c = (b >= 0) ? hc[b] : 0u;
+      if (!c) continue;
+      const uint64_t mb =
+          (uint64_t)c * to_fx(rel_weight<DT, FAST>(X, key_value<DT>(kbase + (uint32_t)b), m_z, nm));
+      if (mb > 0 && cum + mb >= target) {
+        X.sh->bi[0] = b;
+        X.sh->bq[0] = cum;
+        break;
+      }
+      cum += mb;
+    }
+  }
+  __syncthreads();
+  const int bP = X.sh->bi[0];
+  if (bP < 0) return 0;
+  const uint64_t above = X.sh->bq[0];
+  // S_k members strictly above the boundary key, and its copies
+  int an = 0;
+#pragma unroll 1
+  for (int e = 0; e < B16T; ++e) {
+    const int b = b0 - e;
+    if (b > bP) an += (int)hc[b];
+  }
+  an = bsum_i(an, X.sh->ri[0]);
+  const int at_n = (int)hc[bP];
+  R.vP = kbase + (uint32_t)bP;
+  const uint64_t qv = to_fx(rel_weight<DT, FAST>(X, key_value<DT>(R.vP), m_z, nm));
+  if (qv == 0) return 0;
+  const uint64_t need = target - above;  // > 0 by the selection
+  int j = (int)((need + qv - 1) / qv);
+  if (j > at_n) j = at_n;
+  R.idP = (R.vP == R.vK) ? R.idK : NOID;
+  if (j < at_n) {
+    int id = nth_id16(X, n, R.vP, j, R.vK, R.idK);
+    if (id == -2) {
+      const SelOut ti = list_select<NT, DT, SEL_TIEID>(X, n, (uint64_t)j, 0.f, R.vK, R.idK, R.vP);
+      if (!ti.ok) return 0;
+      id = (int)(0xffffffu - ti.v);
+    }
+    if (id < 0) return 0;
+    R.idP = id;
+  }
+  kept_mass = above + (uint64_t)j * qv;
+  if (kept_n) *kept_n = an + j;
+  return 1;
+}
+
 // k-th largest key inside the list (K counted from the top of the list).
 template <int G, int DT>
 __device__ bool list_resolve_k(Ctx<DT>& X, int n, int K, uint32_t& vK, int& idK) {
@@ -625,6 +708,11 @@ __device__ void list_weights(Ctx<DT>& X, int n, float m_z, float nm, uint32_t vK
 template <int G, int DT, bool FAST>
 __device__ bool list_resolve_p(Ctx<DT>& X, int n, uint64_t target, float p, float m_z, float nm,
                                Res& R, uint64_t& kept_mass, int* kept_n = nullptr) {
+  // band lists (weights by the pass exponential): one count histogram
+  if constexpr (DT != DT_F32 && G == NT && FAST) {
+    const int r = hsel_p16<DT, FAST>(X, n, target, p, m_z, nm, R, kept_mass, kept_n);
+    if (r >= 0) return r == 1;
+  }
   const SelOut s = list_select<G, DT, SEL_MASS>(X, n, target, target ? 0.f : p, R.vK, R.idK, 0u);
   if (!s.ok) return false;
   R.vP = s.v;

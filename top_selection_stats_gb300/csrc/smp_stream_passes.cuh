@@ -451,10 +451,12 @@ __device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
   X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
   X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
   X.c2 = c2;
+  // the chunk's copy first, the histogram clear while it is in flight (the
+  // previous task's last barrier freed the stage)
+  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
   uint32_t* wh = X.wh;
   for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
   __syncthreads();
-  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
   const char* stage = ring_wait(X, c);
   uint32_t amax = p_ninf<DT>();
   int nleg = 0;
