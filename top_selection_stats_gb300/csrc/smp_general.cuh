@@ -150,6 +150,89 @@ __device__ __noinline__ bool wh_bracket(Ctx<DT>& Xr, bool pmode, int K, double P
 }
 
 // ---------------------------------------------------------------------------
+// Bracket from a sampled weight histogram (one element in `scale`, excess-
+// weighted counts relative to the stream's reference).  The kept set is the
+// heaviest prefix reaching p of the row mass M, so its boundary bin b* is the
+// first whose lighter part L(b* + 1) (the mass of bins b* + 1 ... WBINS - 1)
+// is at most T1 = (1 - p) M.  L is estimated as scale times the sampled mass;
+// the bracket runs from the point estimate of b* outward over the bins where
+// that estimate is within a margin of T1 (four standard deviations of the
+// sampling error).  Returns false when the bracket would hold more than CAP
+// elements by the sample's count.  The exact band pass decides the result.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __noinline__ bool wh_bracket_sampled(Ctx<DT>& Xr, double T1, float scale, int& b_lo,
+                                                int& b_hi) {
+  LocalCtx<DT> lc_(Xr);
+  Ctx<DT>& X = lc_.v;
+  const uint32_t* wh = X.wh;
+  constexpr int BPT = WBINS / NT;
+  const int t = threadIdx.x;
+  // per bin: sampled mass (units of the reference weight) and sum of squares
+  // bound (mass times the bin's upper weight)
+  float v[BPT], q2[BPT];
+  float s = 0.f, s2 = 0.f;
+#pragma unroll
+  for (int q = 0; q < BPT; ++q) {
+    const int b = t * BPT + q;
+    const float lo_w = (b == WBINS - 1) ? 0.f : exp2f((float)(WHOFF - b - 1) * (1.f / WHS));
+    const float hi_w = exp2f((float)(WHOFF - b) * (1.f / WHS));
+    v[q] = (float)wh[b] * (1.f / 2048.f) * lo_w;
+    q2[q] = v[q] * hi_w;
+    s += v[q];
+    s2 += q2[q];
+  }
+  float tot, tot2;
+  float c = bscan_excl<float>(s, X.sh->rf[0], tot);
+  float c2 = bscan_excl<float>(s2, X.sh->rf[1], tot2);
+  if (t == 0) {
+    X.sh->bi[0] = WBINS;
+    X.sh->bi[1] = WBINS;
+    X.sh->bi[2] = -1;
+  }
+  __syncthreads();
+  const float T1f = (float)T1;
+  // L(b + 1) estimates and margins; the point estimate of b* and the
+  // lightest bin where L(b + 1) is surely below T1
+  float Lq[BPT], dq[BPT];
+#pragma unroll
+  for (int q = 0; q < BPT; ++q) {
+    const int b = t * BPT + q;
+    c += v[q];  // mass of bins 0 .. b
+    c2 += q2[q];
+    Lq[q] = scale * fmaxf(tot - c, 0.f);
+    dq[q] = 4.f * scale * sqrtf(fmaxf(tot2 - c2, 0.f)) + 1e-3f * T1f;
+    if (Lq[q] <= T1f) atomicMin(&X.sh->bi[0], b);
+    if (Lq[q] + dq[q] <= T1f) atomicMin(&X.sh->bi[1], b);
+  }
+  __syncthreads();
+  // the heaviest end: just below the last bin above the estimate where the
+  // boundary is surely not (heavier bins carry the sampled heads, whose
+  // sampling error says nothing about the bins near the boundary)
+  const int bhat = X.sh->bi[0];
+#pragma unroll
+  for (int q = 0; q < BPT; ++q) {
+    const int b = t * BPT + q;
+    if (b < bhat && Lq[q] - dq[q] > T1f) atomicMax(&X.sh->bi[2], b);
+  }
+  __syncthreads();
+  b_lo = X.sh->bi[2] + 1;
+  b_hi = min(X.sh->bi[1], WBINS - 1);
+  if (bhat >= WBINS || b_hi >= WBINS - 1 || b_hi < b_lo) {
+    __syncthreads();
+    return false;
+  }
+  int n = 0;
+#pragma unroll
+  for (int q = 0; q < BPT; ++q) {
+    const int b = t * BPT + q;
+    if (b >= b_lo && b <= b_hi) n += (int)(wh[b] >> 11) + 1;
+  }
+  n = bsum_i(n, X.sh->ri[1]);
+  return (float)n * scale <= (float)CAP;
+}
+
+// ---------------------------------------------------------------------------
 // Band-and-kept pass over a weight-histogram bracket [b_lo, b_hi]: legal
 // elements of bins inside go to the list; those of bins above (larger
 // weights) are kept: kept-mask bits, count, per-(chunk, warp) masses relative

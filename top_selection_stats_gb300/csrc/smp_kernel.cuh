@@ -491,6 +491,32 @@ __device__ __noinline__ bool row_list(Ctx<DT>& X, int K, float p, double u, floa
   return true;
 }
 
+// Band pass over a top-p bracket [b_lo, b_hi] (bins relative to nref), then
+// the exact boundary inside the band list; true when the row is finished.
+// Every kept-mask word is rewritten by the band pass, so a failed attempt
+// leaves nothing behind for the next one.
+template <int DT>
+__device__ __noinline__ bool band_try_p(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm,
+                                        uint64_t Pq, float m, double u) {
+  BandOut bo;
+  const int ln = band_any(X, b_lo, b_hi, nref, nm, bo);
+  if (X.sh->timeout) return false;
+  const int nb = min(max(ln, 0), CAP);
+  list_range(X, nb);
+  if (ln >= 0 && ln <= CAP && Pq > bo.above_q) {
+    list_weights<NT, DT, true>(X, nb, 0.f, nm, 0u, -1);
+    Res R;
+    R.vK = 0u;
+    R.idK = -1;
+    uint64_t km;
+    if (list_resolve_p<NT, DT, true>(X, nb, Pq - bo.above_q, 1.f, 0.f, nm, R, km)) {
+      finish_band(X, nb, bo, R.vP, R.idP, m, u, PATH_FULL);
+      return true;
+    }
+  }
+  return false;
+}
+
 template <int DT>
 __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, float vest) {
   // list target: the top-k set plus margin, or (no top-k boundary expected)
@@ -528,32 +554,17 @@ __device__ __noinline__ void row_general(Ctx<DT>& X, int K, float p, double u, f
   //    the bracket it gives
   int b_lo, b_hi;
   if (!needK && p < 1.f) {
-    // bins relative to the stream's reference when it built the histogram,
-    // else a histogram pass relative to the maximum
-    const float nref = E.hist ? -E.ref * X.c2 : nm;
-    bool br;
-    if (E.hist) {
-      br = wh_bracket(X, true, 0, (double)p * E.z, (m - E.ref) * X.c2, b_lo, b_hi);
-    } else {
-      whist_pass(X, nm, true);
-      br = wh_bracket(X, true, 0, (double)p * zq / 1099511627776.0, 0.f, b_lo, b_hi);
-    }
-    if (br) {
-      BandOut bo;
-      const int ln = band_any(X, b_lo, b_hi, nref, nm, bo);
+    const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));
+    // the stream's sampled histogram first (bins relative to its reference),
+    // then a full histogram pass relative to the maximum
+    if (E.hist && wh_bracket_sampled(X, (1.0 - (double)p) * E.z, (float)ElemT<DT>::EPV, b_lo, b_hi)) {
+      if (band_try_p(X, b_lo, b_hi, -E.ref * X.c2, nm, Pq, m, u)) return;
       if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
-      const int nb = min(max(ln, 0), CAP);
-      list_range(X, nb);
-      const uint64_t Pq = max((uint64_t)1, (uint64_t)ceil((double)p * zq));
-      if (ln >= 0 && ln <= CAP && Pq > bo.above_q) {
-        list_weights<NT, DT, true>(X, nb, 0.f, nm, 0u, -1);
-        Res R;
-        R.vK = 0u;
-        R.idK = -1;
-        uint64_t km;
-        if (list_resolve_p<NT, DT, true>(X, nb, Pq - bo.above_q, 1.f, 0.f, nm, R, km))
-          return finish_band(X, nb, bo, R.vP, R.idP, m, u, PATH_FULL);
-      }
+    }
+    whist_pass(X, nm, true);
+    if (wh_bracket(X, true, 0, (double)p * zq / 1099511627776.0, 0.f, b_lo, b_hi)) {
+      if (band_try_p(X, b_lo, b_hi, nm, nm, Pq, m, u)) return;
+      if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
     }
   } else if (needK) {
     whist_pass(X, nm, false);

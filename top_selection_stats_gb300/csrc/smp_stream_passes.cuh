@@ -261,7 +261,7 @@ struct ExpOut {
   int ovf;     // list overflow (EMIT)
   double lmass;  // mass of the list's elements (EMIT, relative to ref)
   uint32_t tkey, lkmax;  // the list threshold's key and the largest key listed (EMIT)
-  int hist;              // the weight histogram (relative to ref) was built
+  int hist;              // a weight histogram (relative to ref) of one element in EPV was built
 };
 
 // Sum of the EPV weights of a vector: a tree (short dependency chains).
@@ -405,8 +405,9 @@ __device__ bool wait_job(Ctx<DT>& X, int j, int n) {
 }
 
 // Mass (returned: this thread's float sum), legal count, packed maximum and
-// weight-histogram entries of one staged chunk: the body of a shared mass
-// stream, the same arithmetic whichever CTA runs the chunk.
+// sampled weight-histogram entries (one element per vector) of one staged
+// chunk: the body of a shared mass stream, the same arithmetic whichever CTA
+// runs the chunk.
 template <int DT>
 __device__ __forceinline__ float mass_hist_chunk(const Ctx<DT>& X, const char* stage, int c,
                                                  float c2, float nref, uint32_t* wh,
@@ -424,11 +425,13 @@ __device__ __forceinline__ float mass_hist_chunk(const Ctx<DT>& X, const char* s
     for (int q = 0; q < EPV; ++q) w[q] = fast_exp2(fmaf(x[q], c2, nref));  // -inf -> 0
     cs += tree_sum<EPV>(w);
 #pragma unroll
-    for (int q = 0; q < EPV; ++q) {
-      if (!(x[q] > -INFINITY)) continue;
-      ++nleg;
-      whist_add(wh, x[q], c2, nref);
-    }
+    for (int q = 0; q < EPV; ++q) nleg += (x[q] > -INFINITY) ? 1 : 0;
+    // the sampled element of this vector (as in the owner's stream)
+    const int qs = (v0 + 32 * it) & (EPV - 1);
+    float xs = x[0];
+#pragma unroll
+    for (int q = 1; q < EPV; ++q) xs = (qs == q) ? x[q] : xs;
+    if (xs > -INFINITY) whist_add(wh, xs, c2, nref);
   }
   return cs;
 }
@@ -547,11 +550,15 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
           m0 = bsum_f(m0, X.sh->rf[2]);
           hist = m0 < p_hist * z0;
           if (hist) {
+            // a sampled weight histogram: element (vector index mod EPV) of
+            // every vector, one in EPV of the row; no list (it could not hold
+            // the kept set).  The rest of the stream goes on the job board:
+            // this CTA streams from the front, helpers take chunks from the
+            // back (this loop ends after chunk 0).
             for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
             __syncthreads();
-            // such a row is slow to stream (every element is histogrammed):
-            // it goes on the job board, this CTA streams from the front and
-            // helpers take chunks from the back (this loop ends after chunk 0)
+            t2 = p_pinf<DT>();
+            tf = INFINITY;
             if (X.nch > 2) {
               js = publish_job(X, JOB_STREAM, X.nch, 0, 0, nref, 0.f);
               if (js >= 0) X.nch = 1;
@@ -575,11 +582,12 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
       for (int j = 0; j < EPV; ++j) w[j] = fast_exp2(fmaf(x[j], c2, nref));  // -inf -> 0
       cs += tree_sum<EPV>(w);
       if (EMIT && hist) {
+        // the sampled element of this vector (index v0 + 32 it + lane)
+        const int q = (v0 + 32 * it) & (EPV - 1);
+        float xs = x[0];
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) {
-          if (!(x[j] > -INFINITY)) continue;
-          whist_add(wh, x[j], c2, nref);
-        }
+        for (int j = 1; j < EPV; ++j) xs = (q == j) ? x[j] : xs;
+        if (xs > -INFINITY) whist_add(wh, xs, c2, nref);
       }
     }
     // legal count and kept-mask words: every slot legal unless the chunk
@@ -699,6 +707,7 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
   o.tkey = bits_key<DT>((DT == DT_F32) ? t2 : (t2 & 0xffffu));
   o.lkmax = EMIT ? bmax_u(lkm, X.sh->ru[0]) : 0u;
   o.hist = hist ? 1 : 0;
+  if (hist) o.ovf = 1;  // no list was kept
   return o;
 }
 
