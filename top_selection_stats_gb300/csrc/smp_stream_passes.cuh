@@ -352,23 +352,23 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, fl
 template <int DT>
 struct OwnerClaims {
   JobHdr* H;
-  unsigned long long pend;
   int live, first;
   __device__ __forceinline__ void start(Ctx<DT>& X, JobHdr* h, int nch) {
     H = h;
     live = 1;
     first = nch;
-    if (threadIdx.x == 0) pend = atomicAdd(&H->ends, 1ull << 32);
   }
+  // The claim of chunk d is taken when the owner is ready to stage it (after
+  // chunk d - 2), not earlier, so that helpers arriving meanwhile take it.
   __device__ __forceinline__ void decide(Ctx<DT>& X, int d) {
     if (threadIdx.x != 0) return;
     int own = 0;
     if (live) {
-      const int f = ends_front(pend);
-      if (f < ends_back(pend)) {
+      const unsigned long long old = atomicAdd(&H->ends, 1ull << 32);
+      const int f = ends_front(old);
+      if (f < ends_back(old)) {
         own = 1;
         issue_chunk(X, d, d % NSTAGE);
-        pend = atomicAdd(&H->ends, 1ull << 32);
       } else {
         live = 0;
         first = f;
