@@ -77,11 +77,13 @@ __device__ __forceinline__ int cell_of(int id) {
   constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE, VW = ElemT<DT>::VW;
   return (id / CE) * NWARP + ((id % CE) / EPV) / VW;
 }
-// Fixed-point kept masses of list entries, per cell (in the ring scratch).
+// Fixed-point kept masses of list entries, per cell (in the ring scratch),
+// and two 32-bit partial counters per cell after them.
 template <int DT>
 __device__ __forceinline__ uint64_t* cell_extra(const Ctx<DT>& X) {
   return list_scratch(X) + 1024;
 }
+static_assert(CAP * 4 + (2048 + MAXCH * NWARP) * 8 <= SMEM_RING, "cell masses live in the ring");
 
 // ---------------------------------------------------------------------------
 // Bracket from the weight histogram.  Bins (descending weight) 0..WBINS-1.

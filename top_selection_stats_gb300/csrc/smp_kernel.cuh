@@ -163,8 +163,16 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
   const float* wq = list_w(X);
   const uint32_t* lk = X.lk;
   const int* li = X.li;
+  // per-cell fixed-point masses of the kept band entries, summed as two
+  // 21-bit pieces in 32-bit counters (no carries, no returned values: every
+  // weight is at most 1, so a piece is below 2^21 and a cell's sum below 2^32)
+  uint32_t* p0 = reinterpret_cast<uint32_t*>(list_scratch(X) + 2048);
+  uint32_t* p1 = p0 + MAXCH * NWARP;
   __syncthreads();
-  for (int f = threadIdx.x; f < X.nch * NWARP; f += NT) extra[f] = 0;
+  for (int f = threadIdx.x; f < X.nch * NWARP; f += NT) {
+    p0[f] = 0u;
+    p1[f] = 0u;
+  }
   __syncthreads();
   int nk = 0;
   for (int i = threadIdx.x; i < n; i += NT) {
@@ -172,8 +180,14 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
     if (!in_set(lk[i], id, vF, idF)) continue;
     ++nk;
     if (a.kept_mask) atomicOr(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
-    smem_add_u64(&extra[cell_of<DT>(id)], to_fx(wq[i]));
+    const uint64_t q = to_fx(wq[i]);
+    const int f = cell_of<DT>(id);
+    atomicAdd(&p0[f], (uint32_t)(q & 0x1fffffull));
+    atomicAdd(&p1[f], (uint32_t)(q >> 21));
   }
+  __syncthreads();
+  for (int f = threadIdx.x; f < X.nch * NWARP; f += NT)
+    extra[f] = (uint64_t)p0[f] + ((uint64_t)p1[f] << 21);
   nk = bsum_i(nk, X.sh->ri[1]) + bo.above_n;
   double mtot = 0.0;
   int tok = -1;
