@@ -372,7 +372,7 @@ __device__ __noinline__ BandOut band_kept_pass(Ctx<DT>& Xr, int b_lo, int b_hi, 
 }
 
 // The owner's side of a band job (slot j): the band pass over the chunks this
-// CTA claims from the front (two-stage ring, one block barrier per chunk).
+// CTA claims from the front (one block barrier per chunk).
 // Returns the first helper chunk; the list (sh->n entries), the cells and
 // above_n cover the owner's chunks.
 template <int DT>
@@ -387,15 +387,22 @@ __device__ __noinline__ int band_owner_pass(Ctx<DT>& Xr, int j, int b_lo, int b_
   const float xa = X.a->board->hdr[j].xa, xb = X.a->board->hdr[j].xb;
   OwnerClaims<DT> oc;
   oc.start(X, &X.a->board->hdr[j], X.nch);
-  ring_begin(X);  // chunks 0 and 1 are the owner's
+  // chunk 0 is the owner's; each further chunk is claimed only when the owner
+  // is done with the previous one, so helpers (by then usually plentiful)
+  // take most of the pass
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) X.sh->done[s] = 0;
+    issue_chunk(X, 0, 0);
+  }
+  __syncthreads();
 #pragma unroll 1
   for (int c = 0; c < X.nch; ++c) {
-    if (c >= 2 && !oc.owns(X, c)) break;
+    if (c >= 1 && !oc.owns(X, c)) break;
     const char* stage = ring_wait(X, c);
     const float ws = warp_sum(band_chunk<DT>(X, stage, c, xa, xb, X.c2, nm, mrow, nk));
     if (lane == 0) X.sh->cmass[c][warp] = ws;
     __syncthreads();
-    oc.decide(X, c + 2);
+    oc.decide(X, c + 1);
   }
   if (threadIdx.x == 0) X.sh->bi[1] = oc.first;
   above_n = bsum_i(nk, X.sh->ri[0]);

@@ -299,7 +299,8 @@ __device__ __forceinline__ void whist_add(uint32_t* wh, float x, float c2, float
 
 // ---------------------------------------------------------------------------
 // Job board primitives.  publish_job writes a job's header for this CTA's row
-// (fenced before the ready flag; the owner keeps chunks 0 and 1) and returns
+// (fenced before the ready flag; the owner keeps chunk 0, and chunk 1 of a
+// stream job) and returns
 // its slot, or -1 without a board or a free slot.  OwnerClaims walks the
 // owner's claims from the front, one chunk ahead of the ring.  wait_job
 // waits, bounded, until n helper tasks of job j are done.
@@ -326,7 +327,9 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, fl
     for (int b = threadIdx.x; b < WBINS; b += NT) bd->wh[j][b] = 0u;
   if (threadIdx.x == 0) {
     JobHdr* H = &bd->hdr[j];
-    H->ends = (2ull << 32) | (unsigned long long)((uint32_t)nch + ENDS_OFF);
+    // the owner holds chunk 0 of a band job and chunks 0 and 1 of a stream
+    // job (its ring already has them)
+    H->ends = ((kind == JOB_BAND ? 1ull : 2ull) << 32) | (unsigned long long)((uint32_t)nch + ENDS_OFF);
     H->row = X.row;
     H->kind = kind;
     H->nch = nch;
