@@ -454,6 +454,15 @@ __device__ __forceinline__ uint64_t to_fx(float w) {
   if (ex > 63 - 24) return ~0ull;                  // beyond 2^64 (never a weight)
   return ex >= 0 ? (m << ex) : (ex > -24 ? (m >> -ex) : 0ull);
 }
+// floor(w * 2^s) for 0 <= w with a result below 2^63, by integer operations.
+__device__ __forceinline__ uint64_t fx_scaled(float w, int s) {
+  const uint32_t b = __float_as_uint(w);
+  if ((b >> 31) || (b >> 23) == 0u) return 0ull;
+  const int ex = (int)(b >> 23) - 150 + s;  // weight of the significand's unit bit
+  const uint64_t m = (uint64_t)((b & 0x7fffffu) | 0x800000u);
+  if (ex > 39) return ~0ull >> 1;
+  return ex >= 0 ? (m << ex) : (ex > -24 ? (m >> -ex) : 0ull);
+}
 // floor(max(y, -1)) as an int for y < 2^22 by one round-down add of 1.5 *
 // 2^23 (no float -> int conversion, which runs at an eighth of the ALU rate);
 // y >= 2^22 (or +inf) gives at least 2^22, NaN gives -1, so callers that clamp

@@ -790,26 +790,42 @@ __device__ __noinline__ int sample_tail(Ctx<DT>& Xr, double u, uint32_t vF, int 
     __syncwarp();
     const int per = (nf + 31) / 32;
     const int f0 = lane * per, f1 = min(nf, f0 + per);
-    double s = 0.0;
+    // cell masses as fixed-point integers in units of 2^-sc, the scale taken
+    // from the largest cell so that the total of all cells stays below 2^61:
+    // exact sums and compares, and no fp64 arithmetic (slow on this GPU)
+    float mx = 0.f;
     for (int f = f0; f < f1; ++f) {
-      double v = (double)X.sh->cmass[f / NWARP][f % NWARP];
-      if (extra) v += (double)extra[f] * (1.0 / 1099511627776.0);
-      s += v;
+      float v = X.sh->cmass[f / NWARP][f % NWARP];
+      if (extra) v += __ull2float_rz(extra[f] >> 20) * (1.f / 1048576.f);
+      mx = fmaxf(mx, v);
     }
-    const double inc = warp_incl_scan(s);
-    const double tot = __shfl_sync(0xffffffffu, inc, 31);
-    const double T = u * tot;
-    double cum = inc - s;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // every cell < 2^(ex + 1); at most 2^11 cells
+    const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+    const int sc = max(0, min(61 - 11 - (ex + 1), 100));
+    auto cell_fx = [&](int f) -> uint64_t {
+      uint64_t v = fx_scaled(X.sh->cmass[f / NWARP][f % NWARP], sc);
+      if (extra) v += (sc >= FX) ? (extra[f] << (sc - FX)) : (extra[f] >> (FX - sc));
+      return v;
+    };
+    uint64_t s = 0;
+    for (int f = f0; f < f1; ++f) s += cell_fx(f);
+    const uint64_t inc = warp_incl_scan(s);
+    const uint64_t tot = __shfl_sync(0xffffffffu, inc, 31);
+    // T = u * tot with u = k * 2^-24
+    const uint64_t k24 = (uint64_t)(u * 16777216.0);
+    const uint64_t T = __umul64hi(tot, k24 << 40);
+    uint64_t cum = inc - s;
     int hit = -1, last = -1;
-    double before = 0.0;
+    uint64_t before = 0;
     for (int f = f0; f < f1; ++f) {
-      double v = (double)X.sh->cmass[f / NWARP][f % NWARP];
-      if (extra) v += (double)extra[f] * (1.0 / 1099511627776.0);
-      if (hit < 0 && v > 0.0 && cum <= T && cum + v > T) {
+      const uint64_t v = cell_fx(f);
+      if (hit < 0 && v > 0 && cum <= T && cum + v > T) {
         hit = f;
         before = cum;
       }
-      if (v > 0.0) last = f;
+      if (v > 0) last = f;
       cum += v;
     }
     // the first cell in order holding T; if rounding leaves none, the last
@@ -820,13 +836,13 @@ __device__ __noinline__ int sample_tail(Ctx<DT>& Xr, double u, uint32_t vF, int 
       const int src = __ffs(bal) - 1;
       if (lane == src) {
         X.sh->bi[5] = hit;
-        X.sh->bd[0] = T - before;
+        X.sh->bd[0] = ldexp((double)(T - before), -sc);
       }
     } else if (lane == 0) {
       X.sh->bi[5] = lst;
       X.sh->bd[0] = 1e300;  // past the end: take the last kept element
     }
-    if (lane == 0) X.sh->bd[1] = tot;
+    if (lane == 0) X.sh->bd[1] = ldexp((double)tot, -sc);
   }
   __syncthreads();
   mtot = X.sh->bd[1];
