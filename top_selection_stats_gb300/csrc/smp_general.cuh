@@ -244,6 +244,7 @@ __device__ __noinline__ bool wh_bracket_sampled(Ctx<DT>& Xr, double T1, float sc
 struct BandOut {
   int above_n;
   uint64_t above_q;  // fixed-point mass above the bracket (from the per-cell sums)
+  float xa, xb;      // the bracket's value thresholds (band: xb <= x < xa)
 };
 
 // Fixed-point mass of the per-(chunk, warp) cells in sh->cmass: each chunk's

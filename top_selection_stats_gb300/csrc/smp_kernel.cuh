@@ -269,6 +269,8 @@ __device__ int band_any(Ctx<DT>& X, int b_lo, int b_hi, float nref, float nm, Ba
     ln = X.sh->n;
   }
   if (ln >= 0) bo.above_q = cells_fixed_mass(X);
+  bo.xa = xa;
+  bo.xb = xb;
   return ln;
 }
 
@@ -516,7 +518,16 @@ __device__ __noinline__ bool band_try_p(Ctx<DT>& X, int b_lo, int b_hi, float nr
   const int ln = band_any(X, b_lo, b_hi, nref, nm, bo);
   if (X.sh->timeout) return false;
   const int nb = min(max(ln, 0), CAP);
-  list_range(X, nb);
+  // the band's key range is the thresholds' (every entry has xb <= x < xa)
+  if (threadIdx.x == 0) {
+    const uint32_t k_lo = bits_key<DT>(DT == DT_F32 ? pack_down<DT>(bo.xb) : (pack_down<DT>(bo.xb) & 0xffffu));
+    const uint32_t k_hi = (bo.xa < INFINITY)
+        ? bits_key<DT>(DT == DT_F32 ? pack_down<DT>(bo.xa) : (pack_down<DT>(bo.xa) & 0xffffu)) - 1u
+        : ElemT<DT>::KPINF - 1u;
+    X.sh->bu[4] = k_lo;
+    X.sh->bu[5] = max(k_hi, k_lo);
+  }
+  __syncthreads();
   if (ln >= 0 && ln <= CAP && Pq > bo.above_q) {
     list_weights<NT, DT, true>(X, nb, 0.f, nm, 0u, -1);
     Res R;

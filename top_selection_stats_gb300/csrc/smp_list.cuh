@@ -519,9 +519,17 @@ __device__ int nth_id16(Ctx<DT>& X, int n, uint32_t v, int j, uint32_t vK, int i
   if (m > NT) return -2;
   if ((int)threadIdx.x < m) {
     const int ida = g[threadIdx.x];
-    int r = 0;
-    for (int b = 0; b < m; ++b) r += (g[b] < ida) ? 1 : 0;  // ids are distinct
-    if (r == j - 1) X.sh->bi[3] = ida;
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // ids are distinct
+    int b = 0;
+#pragma unroll 2
+    for (; b + 4 <= m; b += 4) {
+      r0 += (g[b] < ida) ? 1 : 0;
+      r1 += (g[b + 1] < ida) ? 1 : 0;
+      r2 += (g[b + 2] < ida) ? 1 : 0;
+      r3 += (g[b + 3] < ida) ? 1 : 0;
+    }
+    for (; b < m; ++b) r0 += (g[b] < ida) ? 1 : 0;
+    if (r0 + r1 + r2 + r3 == j - 1) X.sh->bi[3] = ida;
   }
   __syncthreads();
   return X.sh->bi[3];
