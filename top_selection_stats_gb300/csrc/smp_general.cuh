@@ -853,54 +853,56 @@ __device__ __noinline__ int sample_tail(Ctx<DT>& Xr, double u, uint32_t vF, int 
   const double Tl = X.sh->bd[0];
   if (threadIdx.x == 0) issue_chunk(X, cs, cs % NSTAGE);
   const char* stage = ring_wait(X, cs);
-  if (threadIdx.x == 0) X.sh->bi[6] = -1;
-  __syncthreads();
-  if (warp == ws) {
-    // the cell's own scan runs in fp32 relative to the cell start (its error
-    // is a few fp32 ulps of the cell's mass; fp64 arithmetic is slow here)
-    const float Tf = (float)Tl;
-    float base = 0.f;
-    int found = -1, lastk = -1;
-#pragma unroll 1
-    for (int it = 0; it < ITW; ++it) {
-      const int vi = warp_vec<DT>(it);
-      const uint4 r = load_vec(X, stage, cs, vi);
-      const int id0 = cs * CE + vi * EPV;
-      float w[EPV];
+  // the cell's scan, one vector per thread (its VW vectors are consecutive
+  // in id order), in fp32 relative to the cell start (its error is a few fp32
+  // ulps of the cell's mass; fp64 arithmetic is slow here)
+  constexpr int VW = ElemT<DT>::VW;
+  const float Tf = (float)Tl;
+  const int t = threadIdx.x;
+  float w[EPV];
+  int id0 = 0, lastk = -1;
 #pragma unroll
-      for (int j = 0; j < EPV; ++j) {
-        const uint32_t b = elem_bits<DT>(r, j);
-        const float x = bits_value<DT>(b);
-        w[j] = 0.f;
-        if (x > -INFINITY && in_set(bits_key<DT>(b), id0 + j, vF, idF)) {
-          w[j] = fast_exp2(fmaf(x, X.c2, nm));
-          lastk = id0 + j;
-        }
-      }
-      const float vs = tree_sum<EPV>(w);
-      const float inc = warp_incl_scan(vs);
-      const float pre = base + (inc - vs);
-      // the first vector in id order whose end passes T (the smallest id wins)
-      if (found < 0 && vs > 0.f && pre + vs > Tf) {
-        float cum = pre;
-        int tok = -1, lastj = -1;
+  for (int j = 0; j < EPV; ++j) w[j] = 0.f;
+  if (t < VW) {
+    const int vi = ws * VW + t;
+    const uint4 r = load_vec(X, stage, cs, vi);
+    id0 = cs * CE + vi * EPV;
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) {
-          if (w[j] > 0.f) lastj = id0 + j;
-          cum += w[j];
-          if (tok < 0 && w[j] > 0.f && cum > Tf) tok = id0 + j;
-        }
-        found = tok >= 0 ? tok : lastj;
+    for (int j = 0; j < EPV; ++j) {
+      const uint32_t b = elem_bits<DT>(r, j);
+      const float x = bits_value<DT>(b);
+      if (x > -INFINITY && in_set(bits_key<DT>(b), id0 + j, vF, idF)) {
+        w[j] = fast_exp2(fmaf(x, X.c2, nm));
+        lastk = id0 + j;
       }
-      const int fw = (int)__reduce_min_sync(0xffffffffu, (uint32_t)(found < 0 ? NOID : found));
-      found = (fw == NOID) ? -1 : fw;
-      base += __shfl_sync(0xffffffffu, inc, 31);
     }
-    const int lk = (int)__reduce_max_sync(0xffffffffu, (uint32_t)(lastk + 1)) - 1;
-    if (lane == 0) X.sh->bi[6] = (found >= 0) ? found : lk;
+  }
+  const float vs = tree_sum<EPV>(w);
+  float tot;
+  const float pre = bscan_excl<float>(vs, X.sh->rf[0], tot);
+  if (t == 0) {
+    X.sh->bi[6] = NOID;
+    X.sh->bi[2] = -1;
   }
   __syncthreads();
-  return X.sh->bi[6];
+  // the first vector in id order whose end passes T (the smallest id wins)
+  if (vs > 0.f && pre + vs > Tf) {
+    float cum = pre;
+    int tok = -1, lastj = -1;
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) {
+      if (w[j] > 0.f) lastj = id0 + j;
+      cum += w[j];
+      if (tok < 0 && w[j] > 0.f && cum > Tf) tok = id0 + j;
+    }
+    atomicMin(&X.sh->bi[6], tok >= 0 ? tok : lastj);
+  }
+  if (lastk >= 0) atomicMax(&X.sh->bi[2], lastk);
+  __syncthreads();
+  const int found = X.sh->bi[6];
+  const int res = (found != NOID) ? found : X.sh->bi[2];
+  __syncthreads();
+  return res;
 }
 
 // Probabilities of a boundary-decided kept set: the contract's weight
