@@ -105,6 +105,12 @@ __device__ __forceinline__ void smem_add_u64(uint64_t* p, uint64_t v) {
   if (up) atomicAdd(q + 1, up);
 }
 
+// Fire-and-forget OR into global memory (a reduction: the issuing thread does
+// not wait for the old value).
+__device__ __forceinline__ void red_or_global(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.or.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // --------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): round function and key
 // schedule from the paper.  key = (lo32 seed, hi32 seed), counter = (lo32

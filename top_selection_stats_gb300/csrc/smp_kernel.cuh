@@ -105,7 +105,7 @@ __device__ bool list_solve(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float
   for (int i = gtid<G>(); i < n; i += G) {
     const int id = li[i];
     if (!in_set(lk[i], id, R.vP, R.idP)) continue;
-    if (a.kept_mask) atomicOr(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
+    if (a.kept_mask) red_or_global(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
     if (a.probs && a.mode == MODE_MASK)
       a.probs[(size_t)X.row * X.V + id] = (float)((double)wq[i] * inv);
   }
@@ -179,7 +179,7 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
     const int id = li[i];
     if (!in_set(lk[i], id, vF, idF)) continue;
     ++nk;
-    if (a.kept_mask) atomicOr(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
+    if (a.kept_mask) red_or_global(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
     const uint64_t q = to_fx(wq[i]);
     const int f = cell_of<DT>(id);
     atomicAdd(&p0[f], (uint32_t)(q & 0x1fffffull));
