@@ -247,18 +247,13 @@ struct BandOut {
   float xa, xb;      // the bracket's value thresholds (band: xb <= x < xa)
 };
 
-// Fixed-point mass of the per-(chunk, warp) cells in sh->cmass: each chunk's
-// cells summed in warp order and converted on its own, so the total does not
-// depend on which CTA computed which chunk.
+// Fixed-point mass of the per-(chunk, warp) cells in sh->cmass: every cell
+// converted on its own (integer operations) and the integers summed, so the
+// total does not depend on which CTA computed which chunk or on the order.
 template <int DT>
 __device__ uint64_t cells_fixed_mass(Ctx<DT>& X) {
   uint64_t s = 0;
-  for (int c = threadIdx.x; c < X.nch; c += NT) {
-    double m = 0.0;
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) m += (double)X.sh->cmass[c][w];
-    s += (uint64_t)(m * 1099511627776.0);
-  }
+  for (int f = threadIdx.x; f < X.nch * NWARP; f += NT) s += to_fx(X.sh->cmass[f / NWARP][f % NWARP]);
   return bsum_q(s, X.sh->rq[1]);
 }
 // Smallest legal value x whose weight-histogram bin (relative to nref) is at
