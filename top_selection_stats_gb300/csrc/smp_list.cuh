@@ -756,7 +756,8 @@ __device__ int list_draw(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, d
   int sshift = 8;
   while (((X.V - 1) >> sshift) + 1 > SEG_MAX) ++sshift;
   const int nseg = ((X.V - 1) >> sshift) + 1;
-  const double T = u * (double)Mp;
+  // T = floor(u * Mp) exactly (u = k * 2^-24): integer compares below
+  const uint64_t T = __umul64hi(Mp, ((uint64_t)(u * 16777216.0)) << 40);
   gsync<G>();
   for (int s = t; s < nseg; s += G) seg[s] = 0;
   gsync<G>();
@@ -781,7 +782,7 @@ __device__ int list_draw(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, d
   uint64_t before = 0;
   for (int s = s0; s < s1; ++s) {
     const uint64_t v = seg[s];
-    if (hit < 0 && v > 0 && (double)cum <= T && (double)(cum + v) > T) {
+    if (hit < 0 && v > 0 && cum <= T && cum + v > T) {
       hit = s;
       before = cum;
     }
@@ -833,7 +834,7 @@ __device__ int list_draw(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, d
     uint64_t pre = bf;
     for (int r = 0; r < gn; ++r)
       if (gid[r] < my) pre += gq[r];
-    if (gq[q] > 0 && (double)pre <= T && (double)(pre + gq[q]) > T) tok = my;
+    if (gq[q] > 0 && pre <= T && pre + gq[q] > T) tok = my;
   }
   tok = (int)gmax_u<G>((uint32_t)(tok + 1), sh->ru[1]) - 1;
   return tok >= 0 ? tok : last;
@@ -852,7 +853,8 @@ __device__ int list_draw_small(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t
   int* gid = reinterpret_cast<int*>(sq + NT);  // compacted ids  [NT]
   int* sid = gid + NT;                         // id-ordered ids [NT]
   const int t = threadIdx.x;
-  const double T = u * (double)Mp;
+  // T = floor(u * Mp) exactly (u = k * 2^-24): integer compares below
+  const uint64_t T = __umul64hi(Mp, ((uint64_t)(u * 16777216.0)) << 40);
   __syncthreads();
   if (t == 0) {
     sh->gn = 0;
@@ -882,7 +884,7 @@ __device__ int list_draw_small(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t
   const uint64_t v = (t < m) ? sq[t] : 0;
   uint64_t tot;
   const uint64_t ex = bscan_excl<uint64_t>(v, sh->rq[0], tot);
-  if (t < m && v > 0 && (double)ex <= T && (double)(ex + v) > T) sh->bi[6] = sid[t];
+  if (t < m && v > 0 && ex <= T && ex + v > T) sh->bi[6] = sid[t];
   __syncthreads();
   const int tok = sh->bi[6];
   return tok >= 0 ? tok : ((m > 0) ? sid[m - 1] : -1);
