@@ -174,16 +174,36 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
     p1[f] = 0u;
   }
   __syncthreads();
+  // each thread takes a contiguous run of entries (list order follows the
+  // row's chunks, so a run mostly stays in one cell) and adds a cell's sum
+  // when the run leaves it: few shared atomics, and no lanes of a warp
+  // queueing on one address
   int nk = 0;
-  for (int i = threadIdx.x; i < n; i += NT) {
+  const int per = (n + NT - 1) / NT;
+  const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+  int fc = -1;
+  uint32_t a0 = 0u, a1 = 0u;
+  for (int i = i0; i < i1; ++i) {
     const int id = li[i];
     if (!in_set(lk[i], id, vF, idF)) continue;
     ++nk;
     if (a.kept_mask) red_or_global(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
     const uint64_t q = to_fx(wq[i]);
     const int f = cell_of<DT>(id);
-    atomicAdd(&p0[f], (uint32_t)(q & 0x1fffffull));
-    atomicAdd(&p1[f], (uint32_t)(q >> 21));
+    if (f != fc) {
+      if (fc >= 0) {
+        atomicAdd(&p0[fc], a0);
+        atomicAdd(&p1[fc], a1);
+      }
+      fc = f;
+      a0 = a1 = 0u;
+    }
+    a0 += (uint32_t)(q & 0x1fffffull);
+    a1 += (uint32_t)(q >> 21);
+  }
+  if (fc >= 0) {
+    atomicAdd(&p0[fc], a0);
+    atomicAdd(&p1[fc], a1);
   }
   __syncthreads();
   for (int f = threadIdx.x; f < X.nch * NWARP; f += NT)

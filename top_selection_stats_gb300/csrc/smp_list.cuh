@@ -761,14 +761,29 @@ __device__ int list_draw(Ctx<DT>& X, int n, uint32_t vP, int idP, uint64_t Mp, d
   gsync<G>();
   for (int s = t; s < nseg; s += G) seg[s] = 0;
   gsync<G>();
+  // contiguous runs of entries per thread (list order follows the row, so a
+  // run mostly stays in one segment): a segment's sum is added when the run
+  // leaves it, instead of one contended 64-bit add per entry
   int lastk = -1;
+  {
+    const int per = (n + G - 1) / G;
+    const int i0 = t * per, i1 = min(n, i0 + per);
+    int sc = -1;
+    uint64_t acc = 0;
 #pragma unroll 1
-  for (int i = t; i < n; i += G) {
-    const int id = li[i];
-    if (in_set(lk[i], id, vP, idP)) {
-      smem_add_u64(&seg[id >> sshift], to_fx(wq[i]));
+    for (int i = i0; i < i1; ++i) {
+      const int id = li[i];
+      if (!in_set(lk[i], id, vP, idP)) continue;
+      const int sg = id >> sshift;
+      if (sg != sc) {
+        if (sc >= 0) smem_add_u64(&seg[sc], acc);
+        sc = sg;
+        acc = 0;
+      }
+      acc += to_fx(wq[i]);
       lastk = max(lastk, id);
     }
+    if (sc >= 0) smem_add_u64(&seg[sc], acc);
   }
   const int last = (int)gmax_u<G>((uint32_t)(lastk + 1), sh->ru[0]) - 1;
   gsync<G>();
