@@ -466,7 +466,6 @@ struct Res {
 // ranked by id when there are at most NT of them.
 // ---------------------------------------------------------------------------
 constexpr int NB16 = 4096;        // key bins
-constexpr int B16T = NB16 / NT;   // bins per thread (descending keys)
 constexpr int TG16 = 2048;        // ids gathered for a tie quota
 static_assert(CAP * 4 + NB16 * 4 + TG16 * 4 <= SMEM_RING, "16-bit selection scratch lives in the ring");
 
@@ -547,17 +546,20 @@ __device__ __noinline__ int hsel_k16(Ctx<DT>& Xr, int n, int K, uint32_t& vK, in
   hist16_build(X, n, kbase, false, 0u, -1);
   const uint32_t* hc = hist16(X);
   const int t = threadIdx.x;
-  const int b0 = (int)top - t * B16T;  // this thread's bins b0, b0 - 1, ..., b0 - B16T + 1
+  // this thread's bins b0, b0 - 1, ..., b0 - bpt + 1 (as few per thread as
+  // the key range allows, so a narrow range spreads over many threads)
+  const int bpt = ((int)top + NT) / NT;
+  const int b0 = (int)top - t * bpt;
   uint32_t s = 0u;
 #pragma unroll 1
-  for (int e = 0; e < B16T; ++e) s += (b0 - e >= 0) ? hc[b0 - e] : 0u;
+  for (int e = 0; e < bpt; ++e) s += (b0 - e >= 0) ? hc[b0 - e] : 0u;
   uint32_t tot;
   uint32_t cum = bscan_excl<uint32_t>(s, X.sh->ru[0], tot);
   if (t == 0) X.sh->bi[0] = -1;
   __syncthreads();
   if (cum < (uint32_t)K && cum + s >= (uint32_t)K) {
 #pragma unroll 1
-    for (int e = 0; e < B16T; ++e) {
+    for (int e = 0; e < bpt; ++e) {
       const uint32_t c = (b0 - e >= 0) ? hc[b0 - e] : 0u;
       if (c > 0u && cum + c >= (uint32_t)K) {
         X.sh->bi[0] = b0 - e;
@@ -603,10 +605,13 @@ __device__ __noinline__ int hsel_p16(Ctx<DT>& Xr, int n, uint64_t target, float 
   hist16_build(X, n, kbase, true, R.vK, R.idK);
   const uint32_t* hc = hist16(X);
   const int t = threadIdx.x;
-  const int b0 = (int)top - t * B16T;  // this thread's bins b0, b0 - 1, ..., b0 - B16T + 1
+  // this thread's bins b0, b0 - 1, ..., b0 - bpt + 1 (as few per thread as
+  // the key range allows, so a narrow range spreads over many threads)
+  const int bpt = ((int)top + NT) / NT;
+  const int b0 = (int)top - t * bpt;
   uint64_t s = 0;
 #pragma unroll 1
-  for (int e = 0; e < B16T; ++e) {
+  for (int e = 0; e < bpt; ++e) {
     const int b = b0 - e;
     const uint32_t c = (b >= 0) ? hc[b] : 0u;
     if (c) s += (uint64_t)c * to_fx(rel_weight<DT, FAST>(X, key_value<DT>(kbase + (uint32_t)b), m_z, nm));
@@ -621,7 +626,7 @@ __device__ __noinline__ int hsel_p16(Ctx<DT>& Xr, int n, uint64_t target, float 
   __syncthreads();
   if (cum < target && cum + s >= target) {
 #pragma unroll 1
-    for (int e = 0; e < B16T; ++e) {
+    for (int e = 0; e < bpt; ++e) {
       const int b = b0 - e;
       const uint32_t c = (b >= 0) ? hc[b] : 0u;
       if (!c) continue;
@@ -642,7 +647,7 @@ __device__ __noinline__ int hsel_p16(Ctx<DT>& Xr, int n, uint64_t target, float 
   // S_k members strictly above the boundary key, and its copies
   int an = 0;
 #pragma unroll 1
-  for (int e = 0; e < B16T; ++e) {
+  for (int e = 0; e < bpt; ++e) {
     const int b = b0 - e;
     if (b > bP) an += (int)hc[b];
   }
