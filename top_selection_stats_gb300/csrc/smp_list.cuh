@@ -589,11 +589,10 @@ __device__ __noinline__ int hsel_k16(Ctx<DT>& Xr, int n, int K, uint32_t& vK, in
   return 1;
 }
 
-// Top-p boundary among the S_k members of a list weighed by the pass
-// exponential (as list_resolve_p): every copy of a key has the same weight, so
-// each bin's fixed-point mass is count * the key's weight (the same integer as
-// summing the copies).  1 = found, 0 = not found, -1 = the key range does not
-// fit the bins.
+// Top-p boundary among the S_k members of a list (as list_resolve_p): every
+// copy of a key has the same weight, so each bin's fixed-point mass is count *
+// the key's weight (the same integer as summing the copies).  1 = found, 0 =
+// not found, -1 = the key range does not fit the bins.
 template <int DT, bool FAST>
 __device__ __noinline__ int hsel_p16(Ctx<DT>& Xr, int n, uint64_t target, float p, float m_z,
                                      float nm, Res& R, uint64_t& kept_mass, int* kept_n) {
@@ -721,8 +720,8 @@ __device__ void list_weights(Ctx<DT>& X, int n, float m_z, float nm, uint32_t vK
 template <int G, int DT, bool FAST>
 __device__ bool list_resolve_p(Ctx<DT>& X, int n, uint64_t target, float p, float m_z, float nm,
                                Res& R, uint64_t& kept_mass, int* kept_n = nullptr) {
-  // band lists (weights by the pass exponential): one count histogram
-  if constexpr (DT != DT_F32 && G == NT && FAST) {
+  // bf16 / fp16 lists: one count histogram
+  if constexpr (DT != DT_F32 && G == NT) {
     const int r = hsel_p16<DT, FAST>(X, n, target, p, m_z, nm, R, kept_mass, kept_n);
     if (r >= 0) return r == 1;
   }
