@@ -15,6 +15,11 @@ Parity status of each function (what pins it is listed in the tests):
   * orc_philox4x32_10 -- pinned against cuRAND's host Philox4x32-10 generator
                         where libcurand is present, and by uniformity tests.
   * orc_row_stats    -- pinned against numpy on the same inputs.
+  * orc_spec_verify_u / orc_spec_verify -- pinned by the exact output
+                        distribution (it equals the target's, the identity of
+                        the lecture notes' section 5.2), the acceptance rate
+                        sum(min(p, q)), special cases (p == q, disjoint
+                        supports) and Philox frequencies.
 """
 import ctypes
 import os
@@ -48,6 +53,12 @@ def load(path):
     L.orc_batch.restype = ctypes.c_int
     L.orc_batch.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, P,
                             P, P, P, P, P, ctypes.c_int, P, P, P, P, P, P, P, ctypes.c_int]
+    L.orc_spec_verify_u.restype = ctypes.c_int
+    L.orc_spec_verify_u.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int64, P, P, P,
+                                    P, P, P]
+    L.orc_spec_verify.restype = ctypes.c_int
+    L.orc_spec_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                                  ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_int]
     L.orc_row_stats.restype = ctypes.c_int
     L.orc_row_stats.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
     return L
@@ -151,6 +162,44 @@ def row_stats(logits_row_bits, dtype, V, temperature=1.0, mask_row=None):
     lib().orc_row_stats(_ptr(arr), _DT[dtype], V, _ptr(mr), float(temperature), _ptr(out))
     return dict(max=out[0], argmax=int(out[1]), n_legal=int(out[2]), mean=out[3], std=out[4],
                 logsumexp=out[5], nonfinite=bool(out[6]))
+
+
+def spec_verify_u(p, q, d, u_acc, u_res, L=None):
+    """One sequence with explicit uniforms.  p: float32 [G+1, V], q: float32
+    [G, V], d: int [G], u_acc: [G], u_res: [G+1].  Returns a dict."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    G1, V = p.shape
+    G = G1 - 1
+    q = np.ascontiguousarray(q if G else np.zeros((1, V)), dtype=np.float32)
+    d = np.ascontiguousarray(d if G else [0], dtype=np.int32)
+    ua = np.ascontiguousarray(u_acc if G else [0.0], dtype=np.float64)
+    ur = np.ascontiguousarray(u_res, dtype=np.float64)
+    out = np.zeros(G + 1, dtype=np.int32)
+    n = np.zeros(1, dtype=np.int32)
+    mg = np.zeros(1, dtype=np.float64)
+    st = (L or lib()).orc_spec_verify_u(G, V, _ptr(p), _ptr(q), V, _ptr(d), _ptr(ua), _ptr(ur),
+                                        _ptr(out), _ptr(n), _ptr(mg))
+    return dict(status=st, tokens=out, n_accepted=int(n[0]), margin=float(mg[0]))
+
+
+def spec_verify(p, q, d, seed, offset, n_threads=1, L=None):
+    """Batch with Philox uniforms.  p: float32 [B, G+1, ld], q: float32
+    [B, G, ld], d: int32 [B, G]; seed, offset: uint64 [B]."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    B, G1, ld = p.shape
+    G = G1 - 1
+    V = ld
+    q = np.ascontiguousarray(q if G else np.zeros((B, 1, ld)), dtype=np.float32)
+    d = np.ascontiguousarray(d if G else np.zeros((B, 1)), dtype=np.int32)
+    s = np.ascontiguousarray(seed, dtype=np.uint64)
+    o = np.ascontiguousarray(offset, dtype=np.uint64)
+    out = np.zeros((B, G + 1), dtype=np.int32)
+    n = np.zeros(B, dtype=np.int32)
+    st = np.zeros(B, dtype=np.int32)
+    mg = np.zeros(B, dtype=np.float64)
+    (L or lib()).orc_spec_verify(B, G, V, _ptr(p), _ptr(q), ld, _ptr(d), _ptr(s), _ptr(o),
+                                 _ptr(out), _ptr(n), _ptr(st), _ptr(mg), int(n_threads))
+    return dict(status=st, tokens=out, n_accepted=n, margin=mg)
 
 
 def bf16_to_f32(bits):

@@ -387,3 +387,112 @@ int orc_row_stats(const void* row, int dtype, int V, const uint32_t* mask_row,
   out[7] = 0.0;
   return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Speculative-decoding verification, exact rule (lecture notes "Decoding: */
+/* Sampling, Beam Search and Speculative Decoding", section 5.2, after     */
+/* Leviathan et al. 2023 and Chen et al. 2023): accept the draft token x   */
+/* with probability min(1, p(x)/q(x)); at the first rejection draw from    */
+/* norm(max(0, p - q)) and stop; after G acceptances draw a bonus token    */
+/* from the target's distribution at position G.                           */
+/* ---------------------------------------------------------------------- */
+
+static int prob_ok(float v) { return !isnan(v) && v >= 0.0f && v <= 1.0f; }
+
+int orc_spec_verify_u(int G, int V, const float* p, const float* q, int64_t ld,
+                      const int32_t* d, const double* u_acc, const double* u_res,
+                      int32_t* out_tokens, int32_t* n_acc, double* margin) {
+  for (int i = 0; i <= G; ++i) out_tokens[i] = -1;
+  *n_acc = 0;
+  *margin = INFINITY;
+  /* every draft token and the two probabilities the test reads at it */
+  for (int i = 0; i < G; ++i) {
+    if (d[i] < 0 || d[i] >= V) return ORC_INVALID;
+    if (!prob_ok(p[(size_t)i * ld + d[i]]) || !prob_ok(q[(size_t)i * ld + d[i]]))
+      return ORC_INVALID;
+  }
+  /* acceptance tests in order; u * q < p is exact in double (24 x 24 bits) */
+  int j = G;
+  for (int i = 0; i < G; ++i) {
+    double a = (double)p[(size_t)i * ld + d[i]];
+    double b = (double)q[(size_t)i * ld + d[i]];
+    if (u_acc[i] * b < a) continue;
+    j = i;
+    break;
+  }
+  /* the drawn position: residual max(0, p_j - q_j) after a rejection, the
+     target row p_G after G acceptances */
+  const float* pr = p + (size_t)j * ld;
+  const float* qr = (j < G) ? q + (size_t)j * ld : NULL;
+  double* w = (double*)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+  if (!w) return ORC_INVALID;
+  double S = 0.0;
+  for (int x = 0; x < V; ++x) {
+    if (!prob_ok(pr[x]) || (qr && !prob_ok(qr[x]))) {
+      free(w);
+      return ORC_INVALID;
+    }
+    double r = (double)pr[x] - (qr ? (double)qr[x] : 0.0);
+    w[x] = r > 0.0 ? r : 0.0;
+    S += w[x];
+  }
+  if (!(S > 0.0)) {
+    free(w);
+    return ORC_EMPTY;
+  }
+  /* inverse CDF in id order: the first id whose cumulative weight exceeds
+     u * S; the last id of positive weight if rounding leaves none */
+  const double T = u_res[j] * S;
+  int tok = -1, last = -1;
+  double cum = 0.0, best = INFINITY;
+  for (int x = 0; x < V; ++x) {
+    if (w[x] <= 0.0) continue;
+    cum += w[x];
+    last = x;
+    if (tok < 0 && cum > T) tok = x;
+    if (cum < S) {  /* a switch point between two candidates */
+      double dist = fabs(cum - T) / S;
+      if (dist < best) best = dist;
+    }
+  }
+  if (tok < 0) tok = last;
+  free(w);
+  for (int i = 0; i < j; ++i) out_tokens[i] = d[i];
+  out_tokens[j] = tok;
+  *n_acc = j;
+  *margin = best;
+  return ORC_OK;
+}
+
+int orc_spec_verify(int B, int G, int V, const float* p, const float* q, int64_t ld,
+                    const int32_t* d, const uint64_t* seed, const uint64_t* offset,
+                    int32_t* out_tokens, int32_t* n_acc, int32_t* status, double* margin,
+                    int n_threads) {
+  if (n_threads < 1) n_threads = 1;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+#endif
+  for (int s = 0; s < B; ++s) {
+    double ua[64], ur[65];
+    for (int i = 0; i <= G; ++i) {
+      uint64_t c = offset[s] + (uint64_t)i;
+      uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
+      uint32_t key[2] = {(uint32_t)seed[s], (uint32_t)(seed[s] >> 32)};
+      uint32_t out[4];
+      orc_philox4x32_10(ctr, key, out);
+      if (i < G) ua[i] = (double)(out[0] >> 8) * (1.0 / 16777216.0);
+      ur[i] = (double)(out[1] >> 8) * (1.0 / 16777216.0);
+    }
+    int32_t* ot = out_tokens + (size_t)s * (size_t)(G + 1);
+    status[s] = orc_spec_verify_u(G, V, p + (size_t)s * (size_t)(G + 1) * (size_t)ld,
+                                  G ? q + (size_t)s * (size_t)G * (size_t)ld : NULL, ld,
+                                  d + (size_t)s * (size_t)G, ua, ur, ot, &n_acc[s],
+                                  &margin[s]);
+    if (status[s] != ORC_OK) {
+      for (int i = 0; i <= G; ++i) ot[i] = -1;
+      n_acc[s] = 0;
+      margin[s] = INFINITY;
+    }
+  }
+  return 0;
+}

@@ -84,6 +84,44 @@ int orc_batch(const void* logits, int dtype, int B, int V, int64_t ld,
 int orc_row_stats(const void* logits_row, int dtype, int V, const uint32_t* mask_row,
                   float temperature, double out[8]);
 
+/*
+ * Speculative-decoding verification with the exact accept / reject rule
+ * (lecture notes "Decoding: Sampling, Beam Search and Speculative Decoding",
+ * section 5.2, after Leviathan et al. 2023 and Chen et al. 2023).  One
+ * sequence with G draft tokens d[0..G-1]; q_i is the draft distribution at
+ * draft position i, p_i the target distribution at position i (i = 0..G).
+ * For i = 0, 1, ...: accept d_i iff u_acc[i] * q_i(d_i) < p_i(d_i) (that is,
+ * with probability min(1, p/q)); at the first rejection draw the token from
+ * norm(max(0, p_i - q_i)) with u_res[i] and stop; if all G are accepted,
+ * draw one more token from p_G with u_res[G].  A draw is the inverse CDF in
+ * token-id order: the first id whose cumulative weight exceeds u * S.
+ *   p       : [G+1] rows of V floats, row stride ld
+ *   q       : [G] rows of V floats, row stride ld (NULL when G == 0)
+ *   u_acc   : [G] uniforms in [0,1); u_res: [G+1] uniforms in [0,1)
+ * Outputs: out_tokens[G+1] (accepted drafts, then the drawn token, then -1),
+ * n_acc, and margin = distance of u_res to the nearest switch point of the
+ * draw, in units of u (infinity when the draw has a single candidate).
+ * Status: ORC_INVALID when a draft token is outside [0, V) or a probability
+ * the rule reads (p_i(d_i), q_i(d_i) for every i < G; the whole drawn row or
+ * rows) is NaN or outside [0, 1]; ORC_EMPTY when the drawn weights sum to 0.
+ * Every output of a sequence with a status other than ORC_OK is -1 / 0.
+ */
+int orc_spec_verify_u(int G, int V, const float* p, const float* q, int64_t ld,
+                      const int32_t* d, const double* u_acc, const double* u_res,
+                      int32_t* out_tokens, int32_t* n_acc, double* margin);
+
+/*
+ * Batch of B sequences with Philox4x32-10 uniforms: for draft position i
+ * (i = 0..G) the block at key (lo32 seed[s], hi32 seed[s]) and counter
+ * offset[s] + i gives u_acc[i] = (word0 >> 8) * 2^-24 and
+ * u_res[i] = (word1 >> 8) * 2^-24.  p: [B][G+1][ld], q: [B][G][ld],
+ * d: [B][G], out_tokens: [B][G+1].
+ */
+int orc_spec_verify(int B, int G, int V, const float* p, const float* q, int64_t ld,
+                    const int32_t* d, const uint64_t* seed, const uint64_t* offset,
+                    int32_t* out_tokens, int32_t* n_acc, int32_t* status, double* margin,
+                    int n_threads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 import pins
+import pins_spec
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
 
@@ -41,6 +42,27 @@ MUTATIONS = [
      "legal[i] = (unsigned char)(mask_allows(mask_row, i));"),
     ("K clamped to top_k - 1", "int K = top_k < nl ? top_k : nl;",
      "int K = top_k < nl ? (top_k > 1 ? top_k - 1 : 1) : nl;"),
+    # speculative verification (lecture notes, section 5.2)
+    ("verify: accept when u*q > p", "if (u_acc[i] * b < a) continue;",
+     "if (u_acc[i] * b > a) continue;"),
+    ("verify: accept when u*q <= p", "if (u_acc[i] * b < a) continue;",
+     "if (u_acc[i] * b <= a) continue;"),
+    ("verify: residual without max(0, .)", "w[x] = r > 0.0 ? r : 0.0;", "w[x] = fabs(r);"),
+    ("verify: residual q - p", "double r = (double)pr[x] - (qr ? (double)qr[x] : 0.0);",
+     "double r = (qr ? (double)qr[x] - (double)pr[x] : (double)pr[x]);"),
+    ("verify: no stop at the first rejection", "    j = i;\n    break;", "    j = i;"),
+    ("verify: bonus drawn from position 0", "const float* pr = p + (size_t)j * ld;",
+     "const float* pr = p + (size_t)(j < G ? j : 0) * ld;"),
+    ("verify: draw uses position 0's uniform", "const double T = u_res[j] * S;",
+     "const double T = u_res[0] * S;"),
+    ("verify: draw takes cum >= u*S", "if (tok < 0 && cum > T) tok = x;",
+     "if (tok < 0 && cum >= T) tok = x;"),
+    ("verify: residual draw reuses word 0", "ur[i] = (double)(out[1] >> 8) * (1.0 / 16777216.0);",
+     "ur[i] = (double)(out[0] >> 8) * (1.0 / 16777216.0);"),
+    ("verify: token range check off by one", "if (d[i] < 0 || d[i] >= V) return ORC_INVALID;",
+     "if (d[i] < 0 || d[i] > V) return ORC_INVALID;"),
+    ("verify: drawn row not checked", "if (!prob_ok(pr[x]) || (qr && !prob_ok(qr[x]))) {",
+     "if (0) {"),
 ]
 
 
@@ -68,7 +90,10 @@ def test_pins_catch_mutation(workdir, name, old, new):
     assert res.returncode == 0, res.stderr
     L = oracle.load(so)
     caught = []
-    for chk in pins.ALL_CHECKS:
+    checks = pins.ALL_CHECKS + pins_spec.SPEC_CHECKS
+    if name.startswith("verify"):
+        checks = pins_spec.SPEC_CHECKS + pins.ALL_CHECKS
+    for chk in checks:
         try:
             out = chk(L=L)
         except AssertionError:
