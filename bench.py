@@ -224,6 +224,184 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+VERIFY_METRIC = ("sequences/sec and achieved HBM GB/s (fraction of roofline), speculative "
+                 "verification, B=256 G=4 V=128256 f32")
+
+
+def verify_bytes(B, G, V, n_acc):
+    """Algorithmic bytes of one verification launch given its outcomes: per
+    sequence the drawn row (p_j and q_j after a rejection, p_G after G
+    acceptances) once, plus draft token, p and q at it per draft position,
+    seed, offset and the outputs."""
+    rows = np.where(np.asarray(n_acc) < G, 2, 1)
+    per = rows * V * 4 + G * 12 + 16 + 4 * (G + 1) + 8
+    return int(per.sum())
+
+
+def verify_oracle_rate(c, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.spec_verify(c["p"][:rows].numpy(), c["q"][:rows].numpy(), c["d"][:rows].numpy(),
+                       c["seed"][:rows].numpy().view(np.uint64),
+                       c["offset"][:rows].numpy().view(np.uint64), n_threads=oracle.host_cores())
+    return time.perf_counter() - t0, oracle.host_cores()
+
+
+def run_verify_reference(args, rank, world):
+    if rank != 0:
+        return
+    from top_selection_stats_gb300 import workloads
+    c = workloads.make_verify(args.workload)
+    rows = c["B"]
+    for _ in range(args.warmup):
+        verify_oracle_rate(c, rows)
+    total, cores = 0.0, 1
+    for _ in range(args.steps):
+        dt, cores = verify_oracle_rate(c, rows)
+        total += dt
+    value = rows * args.steps / total
+    line = {
+        "impl": "reference", "metric": VERIFY_METRIC, "value": value, "unit": "sequences/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": c["B"], "G": c["G"], "V": c["V"]},
+        "cpu_baseline": {"value": value, "unit": "sequences/s", "cores": cores, "kind": "oracle",
+                         "sample": f"all {rows} sequences of {args.workload} per step"},
+        "e2e": {"value": value, "unit": "sequences/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_verify(args, rank, world, local):
+    """Speculative-decoding verification (smp_spec_verify) on a named
+    workload: one step = one call over B sequences of G draft tokens."""
+    from top_selection_stats_gb300 import Sampler, workloads
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    c = workloads.make_verify(args.workload)
+    B, G, V = c["B"], c["G"], c["V"]
+    stream = torch.cuda.current_stream(dev)
+    nbuf = 2  # each step draws up to 2 rows of 0.5 MB per sequence: > L2 between reuses
+    ps = [c["p"].to(dev) for _ in range(nbuf)]
+    qs = [c["q"].to(dev) for _ in range(nbuf)]
+    d = c["d"].to(dev)
+    seed = c["seed"].to(dev)
+    total = args.warmup + args.steps
+    offsets = [(c["offset"] + s * B * (G + 1)).to(dev) for s in range(total)]
+    smp = Sampler(local, max_batch=max(B, 64), max_vocab=max(V, 1024))
+    out_t = torch.empty((B, G + 1), dtype=torch.int32, device=dev)
+    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    st = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def step(s):
+        smp.spec_verify(ps[s % nbuf], qs[s % nbuf], d, seed, offsets[s], out_tokens=out_t,
+                        n_accepted=n_acc, status=st)
+
+    # algorithmic bytes: the drawn rows depend on the outcomes of each step
+    bytes_per = []
+    for s in range(total):
+        step(s)
+        bytes_per.append(verify_bytes(B, G, V, n_acc.cpu().numpy()))
+    torch.cuda.synchronize(dev)
+    alg_bytes = float(np.mean(bytes_per[args.warmup:]))
+    clk = ClockSampler(local) if rank == 0 else None
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                step(args.warmup + i)
+    stream.wait_stream(cap)
+    torch.cuda.synchronize(dev)
+    if clk:
+        clk.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = clk.stop() if clk else None
+    elapsed_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = B * world / (ms_per_step / 1000.0)
+
+    # end to end: probabilities, drafts and offsets from pinned host memory,
+    # outputs read back, every step
+    hp, hq, hd = (x.pin_memory() for x in (c["p"], c["q"], c["d"]))
+    hseed = c["seed"].pin_memory()
+    hoff = [o.pin_memory() for o in (c["offset"] + s * B * (G + 1) for s in range(4))]
+    ho = [torch.empty(x.shape, dtype=torch.int32).pin_memory() for x in (out_t, n_acc, st)]
+    dp, dq = torch.empty_like(ps[0]), torch.empty_like(qs[0])
+    dd, dseed = torch.empty_like(d), torch.empty_like(seed)
+    doff = torch.empty_like(offsets[0])
+
+    def e2e_step(s):
+        dp.copy_(hp, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        dd.copy_(hd, non_blocking=True)
+        dseed.copy_(hseed, non_blocking=True)
+        doff.copy_(hoff[s % 4], non_blocking=True)
+        smp.spec_verify(dp, dq, dd, dseed, doff, out_tokens=out_t, n_accepted=n_acc, status=st)
+        for h, x in zip(ho, (out_t, n_acc, st)):
+            h.copy_(x, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    e2e_steps = 5
+    for s in range(2):
+        e2e_step(s)
+    barrier(world)
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        e2e_step(s)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    h2d = sum(x.numel() * x.element_size() for x in (hp, hq, hd, hseed)) + B * 8
+    d2h = sum(x.numel() * 4 for x in ho)
+    e2e = {"value": B * world * e2e_steps / e2e_s, "unit": "sequences/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (ms_per_step / 1000.0) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+            "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg_bytes,
+            "kernel_ms": ms_per_step}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        secs, passes, cores = 0.0, 0, 1
+        while passes == 0 or (secs < 5.0 and passes < 1000):
+            dt, cores = verify_oracle_rate(c, B)
+            secs += dt
+            passes += 1
+        cpu = {"value": B * passes / secs, "unit": "sequences/s", "cores": cores,
+               "kind": "oracle", "sample": f"all {B} sequences of {args.workload}, {passes} "
+                                           f"passes ({secs:.1f} s)"}
+    if rank == 0:
+        n = n_acc.cpu().numpy()
+        line = {
+            "metric": VERIFY_METRIC, "value": value, "unit": "sequences/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "G": G, "V": V,
+                       "l2": f"inputs rotated over {nbuf} copies of "
+                             f"{(c['p'].numel() + c['q'].numel()) * 4 / 1e6:.0f} MB",
+                       "rejected_sequences_last_step": int((n < G).sum()),
+                       "timing": "cuda graph of the K launches"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    smp.close()
+
+
 def run_ours(args, rank, world, local):
     from top_selection_stats_gb300 import Sampler, workloads
     dev = torch.device("cuda", local)
@@ -401,12 +579,13 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_setup(args.gpus)
+    verify = args.workload.startswith("verify")
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        (run_verify_reference if verify else run_reference)(args, rank, world)
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py --impl ours needs a CUDA GPU")
-        run_ours(args, rank, world, local)
+        (run_verify if verify else run_ours)(args, rank, world, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

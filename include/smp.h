@@ -152,6 +152,51 @@ int smp_sample_noalloc(const void* logits, smp_dtype dtype, int B, int V, int64_
                        int32_t* row_status, uint32_t* kept_mask, int32_t* kept_count,
                        smp_stream stream);
 
+/* Speculative-decoding verification with the exact accept / reject rule
+ * (lecture notes "Decoding: Sampling, Beam Search and Speculative Decoding",
+ * section 5.2, after Leviathan et al. 2023 and Chen et al. 2023), for B
+ * sequences that each carry G draft tokens.  The output tokens are then
+ * distributed exactly as the target's distributions, whatever the draft.
+ * Per sequence s, for i = 0, 1, ...: with d = draft_tokens[s][i], accept d
+ * iff u_acc(i) * q_i(d) < p_i(d) (probability min(1, p/q)); at the first
+ * rejection draw one token from norm(max(0, p_i - q_i)) and stop; if all G
+ * drafts are accepted, draw one more token from p_G.  A draw is the inverse
+ * CDF in token-id order: the first id whose cumulative weight exceeds u
+ * times the total, with weights held as exact integers floor(w * 2^42) so
+ * that the result does not depend on summation order.
+ *   target_probs: fp32 [B][G+1][ld]: p_i, the target's probabilities at
+ *                 draft positions 0..G-1 and at the bonus position G (for
+ *                 example probs_out of smp_topk_topp_mask on the target's
+ *                 logits).  Base address 16-byte aligned.
+ *   draft_probs : fp32 [B][G][ld]: q_i, the distributions the drafts were
+ *                 drawn from; 16-byte aligned; NULL allowed when G == 0.
+ *   draft_tokens: int32 [B][G]; NULL allowed when G == 0.
+ *   B >= 0; 0 <= G <= 31; 1 <= V <= 1,048,576; ld >= V, a multiple of 4.
+ *   seed, offset: uint64 [B].  Position i (0..G) uses the Philox4x32-10
+ *                 block at counter offset[s] + i (key as for smp_sample):
+ *                 u_acc(i) = (word0 >> 8) * 2^-24, and the draw at position
+ *                 i uses u_res(i) = (word1 >> 8) * 2^-24.  A call consumes
+ *                 G + 1 blocks per sequence: advance offsets by G + 1.
+ * Outputs (DEVICE, caller-owned): out_tokens int32 [B][G+1] (the accepted
+ * drafts, then the drawn token, then -1), n_accepted int32 [B] (0..G),
+ * row_status int32 [B]:
+ *   SMP_ERR_INVALID_PARAM -- a draft token outside [0, V), or a probability
+ *     the rule reads (p_i(d_i) and q_i(d_i) for every i < G, and every entry
+ *     of the drawn row or rows) that is NaN or outside [0, 1];
+ *   SMP_ERR_EMPTY -- the drawn weights sum to zero (for example p_i <= q_i
+ *     everywhere after a rejection).
+ * Such a sequence gets out_tokens all -1 and n_accepted 0.
+ * Call status: SMP_ERR_INVALID_PARAM for NULL required pointers, unaligned
+ * probabilities, ld not a multiple of 4 or ld < V; SMP_ERR_CAPACITY for G >
+ * 31, V beyond 1,048,576 or B / V beyond the handle's limits; SMP_ERR_CUDA
+ * when the launch fails.  Work: one launch, a cluster of up to 8 CTAs per
+ * sequence; it reads two probabilities per draft token and the one drawn row
+ * (p_j and q_j after a rejection) once.  No workspace is used. */
+int smp_spec_verify(smp_handle h, const float* target_probs, const float* draft_probs,
+                    const int32_t* draft_tokens, int B, int G, int V, int64_t ld,
+                    const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
+                    int32_t* n_accepted, int32_t* row_status, smp_stream stream);
+
 /* Optional per-row diagnostics for subsequent calls on this handle: when
  * row_info is not NULL, each call writes int32 [B][4] to it (DEVICE memory
  * owned by the caller, at least max_batch*4 entries): {path, band size,

@@ -182,13 +182,14 @@ def spec_verify_u(p, q, d, u_acc, u_res, L=None):
     return dict(status=st, tokens=out, n_accepted=int(n[0]), margin=float(mg[0]))
 
 
-def spec_verify(p, q, d, seed, offset, n_threads=1, L=None):
+def spec_verify(p, q, d, seed, offset, V=None, n_threads=1, L=None):
     """Batch with Philox uniforms.  p: float32 [B, G+1, ld], q: float32
-    [B, G, ld], d: int32 [B, G]; seed, offset: uint64 [B]."""
+    [B, G, ld], d: int32 [B, G]; seed, offset: uint64 [B]; V <= ld (default
+    ld)."""
     p = np.ascontiguousarray(p, dtype=np.float32)
     B, G1, ld = p.shape
     G = G1 - 1
-    V = ld
+    V = ld if V is None else V
     q = np.ascontiguousarray(q if G else np.zeros((B, 1, ld)), dtype=np.float32)
     d = np.ascontiguousarray(d if G else np.zeros((B, 1)), dtype=np.int32)
     s = np.ascontiguousarray(seed, dtype=np.uint64)

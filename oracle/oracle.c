@@ -421,41 +421,48 @@ int orc_spec_verify_u(int G, int V, const float* p, const float* q, int64_t ld,
     break;
   }
   /* the drawn position: residual max(0, p_j - q_j) after a rejection, the
-     target row p_G after G acceptances */
+     target row p_G after G acceptances.  The draw is an integer decision
+     taken from floating-point weights, so it is taken in the library's
+     stated precision: the residual is the binary32 difference, and each
+     weight is held as the integer floor(w * 2^42); sums and prefixes of
+     these are exact. */
   const float* pr = p + (size_t)j * ld;
   const float* qr = (j < G) ? q + (size_t)j * ld : NULL;
-  double* w = (double*)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+  uint64_t* w = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(V > 0 ? V : 1));
   if (!w) return ORC_INVALID;
-  double S = 0.0;
+  uint64_t S = 0;
   for (int x = 0; x < V; ++x) {
     if (!prob_ok(pr[x]) || (qr && !prob_ok(qr[x]))) {
       free(w);
       return ORC_INVALID;
     }
-    double r = (double)pr[x] - (qr ? (double)qr[x] : 0.0);
-    w[x] = r > 0.0 ? r : 0.0;
+    float r = qr ? pr[x] - qr[x] : pr[x];
+    if (!(r > 0.0f)) r = 0.0f;
+    w[x] = (uint64_t)floor(ldexp((double)r, 42));
     S += w[x];
   }
-  if (!(S > 0.0)) {
+  if (S == 0) {
     free(w);
     return ORC_EMPTY;
   }
   /* inverse CDF in id order: the first id whose cumulative weight exceeds
-     u * S; the last id of positive weight if rounding leaves none */
-  const double T = u_res[j] * S;
-  int tok = -1, last = -1;
-  double cum = 0.0, best = INFINITY;
+     u * S, u = k * 2^-24; with integer prefixes P, P > u * S iff
+     P > floor(k * S / 2^24) */
+  const uint64_t k = (uint64_t)ldexp(u_res[j], 24);
+  const uint64_t T = (uint64_t)(((unsigned __int128)S * k) >> 24);
+  const double Tr = u_res[j] * (double)S;
+  int tok = -1;
+  uint64_t cum = 0;
+  double best = INFINITY;
   for (int x = 0; x < V; ++x) {
-    if (w[x] <= 0.0) continue;
+    if (w[x] == 0) continue;
     cum += w[x];
-    last = x;
     if (tok < 0 && cum > T) tok = x;
     if (cum < S) {  /* a switch point between two candidates */
-      double dist = fabs(cum - T) / S;
+      double dist = fabs((double)cum - Tr) / (double)S;
       if (dist < best) best = dist;
     }
   }
-  if (tok < 0) tok = last;
   free(w);
   for (int i = 0; i < j; ++i) out_tokens[i] = d[i];
   out_tokens[j] = tok;

@@ -94,7 +94,10 @@ int orc_row_stats(const void* logits_row, int dtype, int V, const uint32_t* mask
  * with probability min(1, p/q)); at the first rejection draw the token from
  * norm(max(0, p_i - q_i)) with u_res[i] and stop; if all G are accepted,
  * draw one more token from p_G with u_res[G].  A draw is the inverse CDF in
- * token-id order: the first id whose cumulative weight exceeds u * S.
+ * token-id order: the first id whose cumulative weight exceeds u * S.  As
+ * this integer decision is taken from floating-point weights, it is taken in
+ * the precision the library states: the residual is the binary32 difference
+ * p - q, each weight is the integer floor(w * 2^42), and u = k * 2^-24.
  *   p       : [G+1] rows of V floats, row stride ld
  *   q       : [G] rows of V floats, row stride ld (NULL when G == 0)
  *   u_acc   : [G] uniforms in [0,1); u_res: [G+1] uniforms in [0,1)

@@ -47,6 +47,8 @@ def test_null_handle_is_rejected_without_device_work(lib):
     assert lib.smp_set_row_info(None, None) == 3
     assert lib.smp_destroy(None) == 0
     assert lib.smp_create(None, 0, 1, 1) == 3
+    assert lib.smp_spec_verify(None, None, None, None, 1, 1, 8, 8, None, None, None, None, None,
+                               None) == 3
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -47,14 +47,15 @@ MUTATIONS = [
      "if (u_acc[i] * b > a) continue;"),
     ("verify: accept when u*q <= p", "if (u_acc[i] * b < a) continue;",
      "if (u_acc[i] * b <= a) continue;"),
-    ("verify: residual without max(0, .)", "w[x] = r > 0.0 ? r : 0.0;", "w[x] = fabs(r);"),
-    ("verify: residual q - p", "double r = (double)pr[x] - (qr ? (double)qr[x] : 0.0);",
-     "double r = (qr ? (double)qr[x] - (double)pr[x] : (double)pr[x]);"),
+    ("verify: residual without max(0, .)", "if (!(r > 0.0f)) r = 0.0f;", "r = fabsf(r);"),
+    ("verify: residual q - p", "float r = qr ? pr[x] - qr[x] : pr[x];",
+     "float r = qr ? qr[x] - pr[x] : pr[x];"),
     ("verify: no stop at the first rejection", "    j = i;\n    break;", "    j = i;"),
     ("verify: bonus drawn from position 0", "const float* pr = p + (size_t)j * ld;",
      "const float* pr = p + (size_t)(j < G ? j : 0) * ld;"),
-    ("verify: draw uses position 0's uniform", "const double T = u_res[j] * S;",
-     "const double T = u_res[0] * S;"),
+    ("verify: draw uses position 0's uniform",
+     "const uint64_t k = (uint64_t)ldexp(u_res[j], 24);",
+     "const uint64_t k = (uint64_t)ldexp(u_res[0], 24);"),
     ("verify: draw takes cum >= u*S", "if (tok < 0 && cum > T) tok = x;",
      "if (tok < 0 && cum >= T) tok = x;"),
     ("verify: residual draw reuses word 0", "ur[i] = (double)(out[1] >> 8) * (1.0 / 16777216.0);",

@@ -15,7 +15,8 @@ PATH_NAMES = {0: "error", 1: "greedy", 2: "all", 3: "sigma", 4: "full"}
 _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_F16}
 
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
-           "smp_sample_noalloc", "smp_set_row_info", "smp_plan", "smp_status_string")
+           "smp_sample_noalloc", "smp_spec_verify", "smp_set_row_info", "smp_plan",
+           "smp_status_string")
 
 
 class SmpError(RuntimeError):
@@ -53,6 +54,7 @@ def load_library(path=None):
     L.smp_argmax.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P]
     L.smp_sample_noalloc.argtypes = [P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams), P,
                                      P, P, P, P]
+    L.smp_spec_verify.argtypes = [P, P, P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P]
     L.smp_set_row_info.argtypes = [P, P]
     L.smp_plan.argtypes = [P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
@@ -196,6 +198,45 @@ class Sampler:
                                  _ptr(bitmask), _ptr(tokens), _ptr(status), self._stream())
         _check(rc, "smp_argmax")
         return dict(tokens=tokens, status=status)
+
+    def spec_verify(self, target_probs, draft_probs, draft_tokens, seed, offset, V=None,
+                    out_tokens=None, n_accepted=None, status=None):
+        """Speculative-decoding verification (exact accept / reject rule).
+
+        target_probs: float32 [B, G+1, ld]; draft_probs: float32 [B, G, ld]
+        (None when G == 0); draft_tokens: int32 [B, G] (None when G == 0);
+        seed, offset: int64 [B] holding uint64 bit patterns.  Returns
+        out_tokens int32 [B, G+1], n_accepted int32 [B], status int32 [B].
+        """
+        self._check_tensor(target_probs, "target_probs", torch.float32)
+        B, G1, ld = target_probs.shape
+        G = G1 - 1
+        V = ld if V is None else V
+        if G > 0:
+            self._check_tensor(draft_probs, "draft_probs", torch.float32)
+            self._check_tensor(draft_tokens, "draft_tokens", torch.int32)
+            if tuple(draft_probs.shape) != (B, G, ld) or tuple(draft_tokens.shape) != (B, G):
+                raise ValueError("draft_probs must be [B, G, ld] and draft_tokens [B, G]")
+        for name, t in (("seed", seed), ("offset", offset)):
+            self._check_tensor(t, name, torch.int64)
+            if t.numel() != B:
+                raise ValueError(f"{name} must have B={B} entries")
+        dev = self.device
+        if out_tokens is None:
+            out_tokens = torch.empty((B, G + 1), dtype=torch.int32, device=dev)
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev) if n_accepted is None \
+            else n_accepted
+        status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+        for name, t in (("out_tokens", out_tokens), ("n_accepted", n_accepted),
+                        ("status", status)):
+            self._check_tensor(t, name, torch.int32)
+        rc = self.lib.smp_spec_verify(self.h, _ptr(target_probs),
+                                      _ptr(draft_probs) if G > 0 else None,
+                                      _ptr(draft_tokens) if G > 0 else None, B, G, V, ld,
+                                      _ptr(seed), _ptr(offset), _ptr(out_tokens),
+                                      _ptr(n_accepted), _ptr(status), self._stream())
+        _check(rc, "smp_spec_verify")
+        return dict(tokens=out_tokens, n_accepted=n_accepted, status=status)
 
 
 def sample_noalloc(logits, temperature, top_k, top_p, seed, offset, tokens, status,

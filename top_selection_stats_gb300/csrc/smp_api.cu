@@ -21,6 +21,9 @@ const void* kernel_f16();
 cudaError_t launch_f32(const KArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_bf16(const KArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_f16(const KArgs& a, int grid, cudaStream_t st);
+int verify_enqueue(const float* p, const float* q, const int32_t* d, int B, int G, int V,
+                   int64_t ld, const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
+                   int32_t* n_acc, int32_t* status, cudaStream_t st);
 }  // namespace smp
 
 using namespace smp;
@@ -242,6 +245,24 @@ int smp_plan(smp_handle h, smp_dtype dtype, int V, int* cluster, int* slice, int
   if (smem_bytes) *smem_bytes = SMEM_TOTAL;
   if (capacity) *capacity = CAP;
   return ((long long)V > (long long)MAXCH * ce) ? SMP_ERR_CAPACITY : SMP_OK;
+}
+
+int smp_spec_verify(smp_handle h, const float* target_probs, const float* draft_probs,
+                    const int32_t* draft_tokens, int B, int G, int V, int64_t ld,
+                    const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
+                    int32_t* n_accepted, int32_t* row_status, smp_stream stream) {
+  if (!h || B < 0 || G < 0 || V < 1 || ld < V || (ld & 3)) return SMP_ERR_INVALID_PARAM;
+  if (B == 0) return SMP_OK;
+  if (!target_probs || !seed || !offset || !out_tokens || !n_accepted || !row_status)
+    return SMP_ERR_INVALID_PARAM;
+  if (G > 0 && (!draft_probs || !draft_tokens)) return SMP_ERR_INVALID_PARAM;
+  if ((reinterpret_cast<uintptr_t>(target_probs) & 15) ||
+      (G > 0 && (reinterpret_cast<uintptr_t>(draft_probs) & 15)))
+    return SMP_ERR_INVALID_PARAM;
+  if (B > h->max_batch || V > h->max_vocab) return SMP_ERR_CAPACITY;
+  DeviceGuard guard(h->device);
+  return verify_enqueue(target_probs, draft_probs, draft_tokens, B, G, V, ld, seed, offset,
+                        out_tokens, n_accepted, row_status, (cudaStream_t)stream);
 }
 
 const char* smp_status_string(int code) {

@@ -16,6 +16,8 @@ Named workloads:
   mixed256x128256_bf16 B=256 V=128256 bf16 -- mixed per-row parameters
   ties512x151936_bf16 B=512  V=151936 bf16 -- quantised head (ties) + grammar masks
   decode1024x256000_f16 B=1024 V=256000 fp16 -- repeated decode, drawn on the device
+  verify256x4x128256_f32 B=256 sequences, G=4 draft tokens, V=128256 -- inputs of
+                      speculative-decoding verification (see verify_case)
 """
 import numpy as np
 import torch
@@ -26,6 +28,10 @@ WORKLOADS = {
     "mixed256x128256_bf16": dict(B=256, V=128256, dtype="bf16", seed=2),
     "ties512x151936_bf16": dict(B=512, V=151936, dtype="bf16", seed=3),
     "decode1024x256000_f16": dict(B=1024, V=256000, dtype="f16", seed=4),
+}
+
+VERIFY_WORKLOADS = {
+    "verify256x4x128256_f32": dict(B=256, G=4, V=128256, seed=5),
 }
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
@@ -199,3 +205,62 @@ def random_case(seed, B, V, dtype="f32", sigma=2.0, n_head=(0, 64), head=(2.0, 1
     par = _params(B, t, k, p, int(rng.integers(0, 2**31)))
     return dict(name=f"random{seed}", B=B, V=V, dtype=dtype, logits=to_dtype(x, dtype),
                 bitmask=bitmask, **par)
+
+
+def verify_case(seed, B, G, V, ld=None, support=(50, 500), wide_frac=0.1, wide=(20000, 50000),
+                overlap=0.7, noise=0.5):
+    """Inputs of speculative-decoding verification: per sequence, G draft
+    positions with a draft distribution q_i and a draft token drawn from it,
+    and G+1 target distributions p_i (the last one for the bonus token).
+
+    Each p_i is a normalised distribution on a random support (UniformInt
+    ``support`` ids, or ``wide`` ids for a ``wide_frac`` share of positions),
+    the shape of the kept sets that top-k / top-p leave.  q_i shares
+    ``overlap`` of p_i's support with weights perturbed by a log-normal factor
+    (sigma ``noise``) and puts the rest of its mass on ids of its own.  Values
+    are normalised in float64 and stored as float32; draft tokens are drawn
+    from the stored q_i with numpy.  Rows are padded with zeros to ``ld``.
+    Returns torch CPU tensors p [B, G+1, ld], q [B, G, ld], d int32 [B, G],
+    seed / offset int64 [B] (offsets G+1 apart), and B, G, V, ld.
+    """
+    ld = V if ld is None else ld
+    rng = np.random.Generator(np.random.PCG64(seed))
+    p = np.zeros((B, G + 1, ld), dtype=np.float32)
+    q = np.zeros((B, max(G, 1), ld), dtype=np.float32)
+    d = np.zeros((B, max(G, 1)), dtype=np.int32)
+
+    def support_size():
+        lo, hi = wide if rng.random() < wide_frac else support
+        return int(min(V, rng.integers(lo, hi + 1)))
+
+    for s in range(B):
+        for i in range(G + 1):
+            n = support_size()
+            ids = rng.choice(V, size=n, replace=False)
+            w = rng.gamma(0.6, size=n) + 1e-4
+            p[s, i, ids] = (w / w.sum()).astype(np.float32)
+            if i == G:
+                continue
+            n_sh = int(round(overlap * n))
+            wq = np.zeros(V)
+            wq[ids[:n_sh]] = w[:n_sh] * np.exp(noise * rng.standard_normal(n_sh))
+            n_own = max(1, n - n_sh)
+            own = rng.choice(V, size=n_own, replace=False)
+            wq[own] += rng.gamma(0.6, size=n_own) + 1e-4
+            qi = (wq / wq.sum()).astype(np.float32)
+            q[s, i, :V] = qi
+            c = np.cumsum(qi.astype(np.float64))
+            d[s, i] = min(int(np.searchsorted(c, rng.random() * c[-1], side="right")), V - 1)
+            while qi[d[s, i]] == 0.0:  # land on a support id
+                d[s, i] -= 1
+    return dict(B=B, G=G, V=V, ld=ld, p=torch.from_numpy(p),
+                q=torch.from_numpy(q[:, :G]), d=torch.from_numpy(d[:, :G]),
+                seed=torch.full((B,), int(seed) * 7919 + 1, dtype=torch.int64),
+                offset=torch.arange(B, dtype=torch.int64) * (G + 1))
+
+
+def make_verify(name):
+    cfg = VERIFY_WORKLOADS[name]
+    out = verify_case(cfg["seed"], cfg["B"], cfg["G"], cfg["V"])
+    out["name"] = name
+    return out
