@@ -10,9 +10,11 @@
 // drawn row (two rows, p_j and q_j, after a rejection), streamed once from HBM.
 //
 // Layout on GB300: a thread-block cluster of NC CTAs per sequence splits the
-// drawn row into NC segments of whole 1024-element blocks, each CTA's eight
+// drawn row into NC segments of whole 512-element blocks, each CTA's four
 // warps into contiguous slabs walked in 128-element steps (one float4 per
-// lane).  Weights are fixed-point integers, floor(w * 2^42), so the row sum
+// lane).  Small CTAs, eight per SM, keep the per-CTA latencies (acceptance
+// tests, cluster barriers, the final re-read) overlapped with other CTAs'
+// streaming; each lane keeps four steps of loads in flight.  Weights are fixed-point integers, floor(w * 2^42), so the row sum
 // and every prefix are exact and independent of the order of summation.  Each
 // warp keeps its per-step sums in shared memory; after one cluster barrier
 // every CTA reads the NC segment sums through distributed shared memory, and
@@ -30,11 +32,11 @@ namespace cg = cooperative_groups;
 
 namespace smp {
 
-constexpr int VT = 256;             // threads per CTA
+constexpr int VT = 128;             // threads per CTA
 constexpr int VWARPS = VT / 32;
 constexpr int VSTEP = 128;          // elements per warp step (32 lanes x float4)
-constexpr int VBLOCK = VSTEP * VWARPS;  // segment granule: 1024 elements
-constexpr int VMAXSTEPS = 128;      // steps per warp slab: segments of <= 131072
+constexpr int VBLOCK = VSTEP * VWARPS;  // segment granule: 512 elements
+constexpr int VMAXSTEPS = 256;      // steps per warp slab: segments of <= 131072
 constexpr int VMAXC = 8;            // CTAs per cluster (portable size)
 constexpr int VMAXG = 31;           // draft tokens per sequence (lanes 0..G of a warp)
 
@@ -118,7 +120,7 @@ __device__ __forceinline__ void step_weights(float4 pv, float4 qv, bool residual
   }
 }
 
-__global__ void __launch_bounds__(VT, 4) spec_verify_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(VT, 8) spec_verify_kernel(const VerifyArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int s = blockIdx.x / a.nc;
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(VT, 4) spec_verify_kernel(const VerifyArgs a) 
   const int nsteps = slab1 > slab0 ? (slab1 - slab0 + VSTEP - 1) / VSTEP : 0;
   bool bad = false;
   uint64_t wtot = 0;
-  constexpr int UNR = 2;
+  constexpr int UNR = 4;
   for (int st = 0; st < nsteps; st += UNR) {
     float4 pv[UNR], qv[UNR];
 #pragma unroll
@@ -299,8 +301,8 @@ __global__ void __launch_bounds__(VT, 4) spec_verify_kernel(const VerifyArgs a) 
 
 const void* verify_kernel_ptr() { return reinterpret_cast<const void*>(spec_verify_kernel); }
 
-// Cluster size and segment length for V: whole 1024-element blocks per CTA,
-// about 16 K elements each, at most VMAXC CTAs and VMAXSTEPS steps per warp.
+// Cluster size and segment length for V: whole 512-element blocks per CTA, at
+// least 8 K elements each, at most VMAXC CTAs and VMAXSTEPS steps per warp.
 void verify_plan(int V, int& nc, int& seg) {
   const int blocks = (V + VBLOCK - 1) / VBLOCK;
   nc = (blocks + 15) / 16;

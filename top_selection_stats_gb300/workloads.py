@@ -18,6 +18,7 @@ Named workloads:
   decode1024x256000_f16 B=1024 V=256000 fp16 -- repeated decode, drawn on the device
   verify256x4x128256_f32 B=256 sequences, G=4 draft tokens, V=128256 -- inputs of
                       speculative-decoding verification (see verify_case)
+  verify64x4x128256_f32  the same with B=64 (small case for profiling)
 """
 import numpy as np
 import torch
@@ -32,6 +33,7 @@ WORKLOADS = {
 
 VERIFY_WORKLOADS = {
     "verify256x4x128256_f32": dict(B=256, G=4, V=128256, seed=5),
+    "verify64x4x128256_f32": dict(B=64, G=4, V=128256, seed=6),
 }
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
