@@ -432,10 +432,12 @@ def run_ours(args, rank, world, local):
     kmask = torch.empty((B, W), dtype=torch.int32, device=dev)
     kcount = torch.empty(B, dtype=torch.int32, device=dev)
 
+    logprobs = torch.empty(B, dtype=torch.float32, device=dev) if args.logprob else None
+
     def step(s, lg=None):
         smp.sample(logits[s % nbuf] if lg is None else lg, t, k, p, seed, offsets[s],
                    bitmask=bitmask, kept_mask=kmask, kept_count=kcount, tokens=tokens,
-                   status=status)
+                   status=status, logprobs=logprobs)
 
     # path statistics (untimed)
     smp.set_row_info(True, max_batch=B)
@@ -539,7 +541,7 @@ def run_ours(args, rank, world, local):
            "d2h_bytes_per_step": d2h}
 
     peak, peak_kind = measured_peaks()
-    alg_bytes = B * row_bytes(V, bitmask is not None, True, esize)
+    alg_bytes = B * (row_bytes(V, bitmask is not None, True, esize) + (4 if args.logprob else 0))
     achieved = alg_bytes / (kern_ms / 1000.0) / 1e9
     traffic = profiled_traffic(args.workload)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -564,7 +566,8 @@ def run_ours(args, rank, world, local):
                        "kept_mask": True,
                        "l2": f"inputs rotated over {nbuf} copies ({nbuf * bytes_logits / 1e6:.0f} MB > L2)",
                        "cluster": plan["cluster"], "slice": plan["slice"],
-                       "smem_per_cta": plan["smem"], "paths": paths, "timing": timing},
+                       "smem_per_cta": plan["smem"], "paths": paths, "timing": timing,
+                       "logprob": bool(args.logprob)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps,
         }
@@ -582,6 +585,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=256)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--logprob", action="store_true",
+                    help="also return each drawn token's log-probability (smp_sample_logprob)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_setup(args.gpus)

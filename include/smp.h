@@ -117,6 +117,21 @@ int smp_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, 
                int32_t* row_status, uint32_t* kept_mask, int32_t* kept_count,
                smp_stream stream);
 
+/* smp_sample plus the log-probability of each drawn token ("Sampling system
+ * design" post, section on logprobs: a sampler that returns logprobs returns
+ * the selected token's log-probability and states the distribution it is
+ * taken under).  The distribution here is the PROCESSED one the token was
+ * drawn from: after temperature, mask, top-k and top-p, renormalised over
+ * the kept set -- the final probability smp_topk_topp_mask writes to
+ * probs_out for that token.  logprobs: DEVICE float [B], required.
+ * Greedy rows (kept set {argmax}) get 0; rows whose status is not SMP_OK
+ * get NaN.  Other arguments, outputs and statuses are those of smp_sample;
+ * the tokens drawn are the same as smp_sample's for the same inputs. */
+int smp_sample_logprob(smp_handle h, const void* logits, smp_dtype dtype, int B, int V,
+                       int64_t ld, const uint32_t* bitmask, const smp_row_params* params,
+                       int32_t* tokens, float* logprobs, int32_t* row_status,
+                       uint32_t* kept_mask, int32_t* kept_count, smp_stream stream);
+
 /* Greedy path alone (KB note section 02; lecture 9 answer 1): the legal
  * finite token with the largest logit, the smallest id on ties.  Rows with
  * no legal finite logit get SMP_ERR_EMPTY, rows with NaN / +inf in a legal

@@ -211,3 +211,52 @@ def test_few_legal_tokens_take_the_whole_legal_set():
                 top_p=torch.tensor([0.95, 1.0, 0.5, 0.9] * 3, dtype=torch.float32),
                 seed=torch.full((12,), 9, dtype=torch.int64), offset=torch.arange(12))
     run_and_compare(case)
+
+
+def check_logprobs(case):
+    """smp_sample_logprob: the same tokens as smp_sample, and the log of each
+    drawn token's final probability within the probabilities' tolerance
+    (|d log r| = |dr| / r <= 1e-5); greedy rows 0, error rows NaN."""
+    r = H.oracle_run(case, want_probs=True)
+    s = H.sampler()
+    d = H.to_dev(case)
+    args = (d["logits"], d["temperature"], d["top_k"], d["top_p"], d["seed"], d["offset"])
+    g = s.sample(*args, bitmask=d["bitmask"], want_logprob=True)
+    plain = s.sample(*args, bitmask=d["bitmask"])
+    torch.cuda.synchronize()
+    tok, st, lp = (g[k].cpu().numpy() for k in ("tokens", "status", "logprobs"))
+    ptok, pst = plain["tokens"].cpu().numpy(), plain["status"].cpu().numpy()
+    bad = np.nonzero((tok != ptok) | (st != pst))[0]
+    assert bad.size == 0, (case["name"], bad[:8], tok[bad[:8]], ptok[bad[:8]], st[bad[:8]],
+                           pst[bad[:8]], r["token"][bad[:8]], r["flags"][bad[:8]])
+    assert np.array_equal(st, r["status"])
+    assert np.all(np.isnan(lp[st != 0]))
+    greedy = (st == 0) & (case["temperature"].cpu().numpy() == 0)
+    assert np.all(lp[greedy] == 0.0)
+    ok = (st == 0) & (tok == r["token"]) & ((r["flags"] & oracle.FLAG_TOPP_BOUNDARY) == 0)
+    rows = np.nonzero(ok)[0]
+    want = np.log(r["probs"][rows, tok[rows]])
+    err = np.abs(lp[rows].astype(np.float64) - want)
+    assert err.max(initial=0.0) <= H.PROB_RTOL, (case["name"], rows[err.argmax()], err.max())
+    return len(rows)
+
+
+@pytest.mark.parametrize("name", ["tiny4x1024_f32", "topk64x32000_f32"])
+def test_logprobs_named(name):
+    assert check_logprobs(workloads.make(name)) > 0
+
+
+def test_logprobs_bench_workload():
+    # every row class of the bench workload: greedy, keep-all, lists, flat top-p
+    assert check_logprobs(workloads.make("mixed256x128256_bf16")) > 200
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_logprobs_random(dtype):
+    case = workloads.random_case(4242 + len(dtype), 48, 20000, dtype=dtype, mask_frac=0.3,
+                                 neg_inf_frac=0.01)
+    assert check_logprobs(case) > 0
+
+
+def test_logprobs_ties_and_masks():
+    assert check_logprobs(workloads.make("ties512x151936_bf16", rows=96)) > 0

@@ -15,7 +15,8 @@ PATH_NAMES = {0: "error", 1: "greedy", 2: "all", 3: "sigma", 4: "full"}
 _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_F16}
 
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
-           "smp_sample_noalloc", "smp_spec_verify", "smp_set_row_info", "smp_plan",
+           "smp_sample_noalloc", "smp_sample_logprob", "smp_spec_verify", "smp_set_row_info",
+           "smp_plan",
            "smp_status_string")
 
 
@@ -52,6 +53,8 @@ def load_library(path=None):
     L.smp_sample.argtypes = [P, P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams), P, P,
                              P, P, P]
     L.smp_argmax.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P]
+    L.smp_sample_logprob.argtypes = [P, P, I, I, I, ctypes.c_int64, P,
+                                     ctypes.POINTER(RowParams), P, P, P, P, P, P]
     L.smp_sample_noalloc.argtypes = [P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams), P,
                                      P, P, P, P]
     L.smp_spec_verify.argtypes = [P, P, P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P]
@@ -160,7 +163,10 @@ class Sampler:
 
     # -- entry points -------------------------------------------------------------
     def sample(self, logits, temperature, top_k, top_p, seed, offset, bitmask=None, V=None,
-               kept_mask=None, kept_count=None, want_mask=False, tokens=None, status=None):
+               kept_mask=None, kept_count=None, want_mask=False, tokens=None, status=None,
+               want_logprob=False, logprobs=None):
+        """smp_sample, or smp_sample_logprob when want_logprob or logprobs (float32
+        [B]) is given: the log of each drawn token's final probability."""
         B, V, ld, params = self._prep(logits, V, bitmask, temperature, top_k, top_p, seed, offset)
         dev = self.device
         tokens = torch.empty(B, dtype=torch.int32, device=dev) if tokens is None else tokens
@@ -168,11 +174,25 @@ class Sampler:
         if want_mask and kept_mask is None:
             kept_mask = torch.empty((B, (V + 31) // 32), dtype=torch.int32, device=dev)
             kept_count = torch.empty(B, dtype=torch.int32, device=dev)
-        rc = self.lib.smp_sample(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V, ld,
-                                 _ptr(bitmask), ctypes.byref(params), _ptr(tokens), _ptr(status),
-                                 _ptr(kept_mask), _ptr(kept_count), self._stream())
-        _check(rc, "smp_sample")
-        return dict(tokens=tokens, status=status, kept_mask=kept_mask, kept_count=kept_count)
+        if want_logprob and logprobs is None:
+            logprobs = torch.empty(B, dtype=torch.float32, device=dev)
+        if logprobs is not None:
+            self._check_tensor(logprobs, "logprobs", torch.float32)
+            rc = self.lib.smp_sample_logprob(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V,
+                                             ld, _ptr(bitmask), ctypes.byref(params),
+                                             _ptr(tokens), _ptr(logprobs), _ptr(status),
+                                             _ptr(kept_mask), _ptr(kept_count), self._stream())
+            _check(rc, "smp_sample_logprob")
+        else:
+            rc = self.lib.smp_sample(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V, ld,
+                                     _ptr(bitmask), ctypes.byref(params), _ptr(tokens),
+                                     _ptr(status), _ptr(kept_mask), _ptr(kept_count),
+                                     self._stream())
+            _check(rc, "smp_sample")
+        out = dict(tokens=tokens, status=status, kept_mask=kept_mask, kept_count=kept_count)
+        if logprobs is not None:
+            out["logprobs"] = logprobs
+        return out
 
     def topk_topp_mask(self, logits, temperature, top_k, top_p, bitmask=None, V=None,
                        want_probs=False):

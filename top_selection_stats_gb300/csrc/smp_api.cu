@@ -82,7 +82,7 @@ struct DeviceGuard {
 int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64_t ld,
            const uint32_t* bitmask, const smp_row_params* params, int32_t* tokens,
            int32_t* status, uint32_t* kept_mask, int32_t* kept_count, float* probs,
-           smp_stream stream) {
+           smp_stream stream, float* logprob = nullptr) {
   if (!h || !logits || !status) return SMP_ERR_INVALID_PARAM;
   if (dt != DT_F32 && dt != DT_BF16 && dt != DT_F16) return SMP_ERR_INVALID_PARAM;
   if (B < 0 || V < 1 || ld < V) return SMP_ERR_INVALID_PARAM;
@@ -118,6 +118,7 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   a.kept_mask = kept_mask;
   a.kept_count = kept_count;
   a.probs = probs;
+  a.logprob = logprob;
   a.row_info = h->row_info;
   a.board = h->board;
   a.mode = mode;
@@ -220,6 +221,15 @@ int smp_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, 
                smp_stream stream) {
   return launch(h, MODE_SAMPLE, logits, (int)dtype, B, V, ld, bitmask, params, tokens,
                 row_status, kept_mask, kept_count, nullptr, stream);
+}
+
+int smp_sample_logprob(smp_handle h, const void* logits, smp_dtype dtype, int B, int V,
+                       int64_t ld, const uint32_t* bitmask, const smp_row_params* params,
+                       int32_t* tokens, float* logprobs, int32_t* row_status,
+                       uint32_t* kept_mask, int32_t* kept_count, smp_stream stream) {
+  if (!logprobs) return SMP_ERR_INVALID_PARAM;
+  return launch(h, MODE_SAMPLE, logits, (int)dtype, B, V, ld, bitmask, params, tokens,
+                row_status, kept_mask, kept_count, nullptr, stream, logprobs);
 }
 
 int smp_argmax(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,

@@ -83,6 +83,7 @@ struct KArgs {
   uint32_t* kept_mask;
   int* kept_count;
   float* probs;
+  float* logprob;  // natural log of the drawn token's final probability, or null
   int* row_info;
   int mode;
   int use_tma;  // rows are 16-byte aligned: stage them with bulk copies

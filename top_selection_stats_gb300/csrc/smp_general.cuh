@@ -399,6 +399,7 @@ __device__ __noinline__ int band_owner_pass(Ctx<DT>& Xr, int j, int b_lo, int b_
     if (lane == 0) X.sh->cmass[c][warp] = ws;
     __syncthreads();
     oc.decide(X, c + 1);
+    __syncthreads();  // every thread reads the claim of chunk c + 1 after thread 0 made it
   }
   if (threadIdx.x == 0) X.sh->bi[1] = oc.first;
   above_n = bsum_i(nk, X.sh->ri[0]);

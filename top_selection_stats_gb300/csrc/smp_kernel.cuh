@@ -41,6 +41,7 @@ __device__ void put_row(Ctx<DT>& X, int status, int token, int count, int path, 
   const KArgs& a = *X.a;
   a.status[X.row] = status;
   if (a.tokens) a.tokens[X.row] = (status == ST_OK) ? token : -1;
+  if (a.logprob && status != ST_OK) a.logprob[X.row] = __int_as_float(0x7fffffff);
   if (a.kept_count) a.kept_count[X.row] = (status == ST_OK) ? count : 0;
   if (a.row_info) {
     int* ri = a.row_info + (size_t)X.row * 4;
@@ -108,6 +109,7 @@ __device__ bool list_solve(Ctx<DT>& X, int n, int K, float p, uint64_t Pq, float
     if (a.kept_mask) red_or_global(a.kept_mask + (size_t)X.row * X.W + (id >> 5), 1u << (id & 31));
     if (a.probs && a.mode == MODE_MASK)
       a.probs[(size_t)X.row * X.V + id] = (float)((double)wq[i] * inv);
+    if (a.logprob && id == tok) a.logprob[X.row] = (float)fmin(log((double)wq[i] * inv), 0.0);
   }
   if (gtid<G>() == 0) put_row(X, ST_OK, tok, nk, path, n);
   return true;
@@ -131,6 +133,20 @@ __device__ __noinline__ bool list_finish(Ctx<DT>& X, int n, int K, float p, uint
   return ok;
 }
 
+// Log of the drawn token's final probability for a kept set decided over the
+// whole row: the contract's weight expf(fl32(x / T) - zr) over the kept mass
+// mtot relative to the same reference, as probs_pass writes probabilities.
+template <int DT>
+__device__ void put_logprob(Ctx<DT>& X, int tok, float zr, double mtot) {
+  if (threadIdx.x != 0 || !X.a->logprob || tok < 0) return;
+  uint32_t b;
+  if constexpr (DT == DT_F32) b = reinterpret_cast<const uint32_t*>(X.src)[tok];
+  else b = reinterpret_cast<const uint16_t*>(X.src)[tok];
+  const float x = bits_value<DT>(b);
+  // (a probability a rounding above 1 is taken as 1)
+  X.a->logprob[X.row] = (float)fmin(log((double)expf(__fdiv_rn(x, X.temp) - zr) / mtot), 0.0);
+}
+
 // ---------------------------------------------------------------------------
 // Kept set decided by a boundary over the whole row: kept pass (mask, count,
 // masses), draw and probabilities.
@@ -147,6 +163,7 @@ __device__ __noinline__ void finish_by_pass(Ctx<DT>& X, uint32_t vF, int idF, fl
     tok = sample_tail(X, u, vF, idF, nm, nullptr, mtot);
   if (a.probs && a.mode == MODE_MASK) probs_pass(X, vF, idF, __fdiv_rn(ref, X.temp), mtot);
   if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  put_logprob(X, tok, __fdiv_rn(ref, X.temp), mtot);
   write_row(X, ST_OK, tok, nk, path);
   __syncthreads();
 }
@@ -215,6 +232,7 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
     tok = sample_tail(X, u, vF, idF, nm, extra, mtot);
   if (a.probs && a.mode == MODE_MASK) probs_pass(X, vF, idF, __fdiv_rn(m, X.temp), mtot);
   if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  put_logprob(X, tok, __fdiv_rn(m, X.temp), mtot);
   write_row(X, ST_OK, tok, nk, path);
   __syncthreads();
 }
@@ -458,6 +476,7 @@ __device__ __noinline__ void row_argmax(Ctx<DT>& X) {
   if (threadIdx.x == 0) {
     if (a.kept_mask) a.kept_mask[(size_t)X.row * X.W + (bid >> 5)] = 1u << (bid & 31);
     if (a.probs && a.mode == MODE_MASK) a.probs[(size_t)X.row * X.V + bid] = 1.f;
+    if (a.logprob) a.logprob[X.row] = 0.f;  // the kept set is {argmax}
     put_row(X, ST_OK, bid, 1, PATH_GREEDY, 0);
   }
   __syncthreads();
@@ -492,6 +511,7 @@ __device__ __noinline__ void row_keepall(Ctx<DT>& X, double u, float vest) {
     tok = sample_tail(X, u, 0u, -1, nm, nullptr, mtot);
   if (a.probs && a.mode == MODE_MASK) probs_pass(X, 0u, -1, __fdiv_rn(E.ref, X.temp), mtot);
   if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
+  put_logprob(X, tok, __fdiv_rn(E.ref, X.temp), mtot);
   write_row(X, ST_OK, tok, E.nleg, PATH_ALL);
   __syncthreads();
 }

@@ -347,11 +347,11 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, fl
   return j;
 }
 
-// The owner's claims (thread 0 holds the pending one).  decide(d) resolves
-// the claim of chunk d, issues d into stage d % NSTAGE when it is the
-// owner's, claims d + 1, and leaves the answer in sh->bi[6 + d % 2] for the
-// other threads (read after the next block barrier).  After the first failed
-// claim, `first` is the first helper chunk.
+// The owner's claims, made by thread 0.  decide(d) claims chunk d, issues it
+// into stage d % NSTAGE when the claim succeeds and leaves the answer in
+// sh->bi[6 + d % 2]; the other threads may read it (owns) only after a block
+// barrier that follows the call.  After the first failed claim, `first` is
+// the first helper chunk.
 template <int DT>
 struct OwnerClaims {
   JobHdr* H;
