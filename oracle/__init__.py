@@ -15,6 +15,10 @@ Parity status of each function (what pins it is listed in the tests):
   * orc_philox4x32_10 -- pinned against cuRAND's host Philox4x32-10 generator
                         where libcurand is present, and by uniformity tests.
   * orc_row_stats    -- pinned against numpy on the same inputs.
+  * orc_repetition_penalty, orc_f32_to_bf16, orc_f32_to_f16 -- pinned by
+                        worked values of the CTRL rule, duplicates and padding
+                        in the history, and the encoders against numpy / torch
+                        round-to-nearest-even casts over many values.
   * orc_spec_verify_u / orc_spec_verify -- pinned by the exact output
                         distribution (it equals the target's, the identity of
                         the lecture notes' section 5.2), the acceptance rate
@@ -59,6 +63,13 @@ def load(path):
     L.orc_spec_verify.restype = ctypes.c_int
     L.orc_spec_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                   ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_int]
+    L.orc_f32_to_bf16.restype = ctypes.c_uint16
+    L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.orc_f32_to_f16.restype = ctypes.c_uint16
+    L.orc_f32_to_f16.argtypes = [ctypes.c_float]
+    L.orc_repetition_penalty.restype = ctypes.c_int
+    L.orc_repetition_penalty.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int64, P, ctypes.c_int, ctypes.c_int64, P, P]
     L.orc_row_stats.restype = ctypes.c_int
     L.orc_row_stats.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
     return L
@@ -201,6 +212,29 @@ def spec_verify(p, q, d, seed, offset, V=None, n_threads=1, L=None):
     (L or lib()).orc_spec_verify(B, G, V, _ptr(p), _ptr(q), ld, _ptr(d), _ptr(s), _ptr(o),
                                  _ptr(out), _ptr(n), _ptr(st), _ptr(mg), int(n_threads))
     return dict(status=st, tokens=out, n_accepted=n, margin=mg)
+
+
+def repetition_penalty(logits_bits, dtype, V, history, penalty, L=None):
+    """Returns a penalised copy of logits_bits (float32 values or uint16
+    bit patterns, [B, ld]) and the per-row statuses.  history: int32 [B, H]
+    (entries outside [0, V) are padding); penalty: float32 [B]."""
+    out = np.array(logits_bits, copy=True, order="C")
+    B, ld = out.shape
+    h = np.ascontiguousarray(history, dtype=np.int32)
+    H = h.shape[1] if h.ndim == 2 else 0
+    pen = np.ascontiguousarray(penalty, dtype=np.float32)
+    st = np.zeros(B, dtype=np.int32)
+    (L or lib()).orc_repetition_penalty(_ptr(out), _DT[dtype], B, V, ld, _ptr(h), H, H,
+                                        _ptr(pen), _ptr(st))
+    return out, st
+
+
+def f32_to_bf16(x, L=None):
+    return (L or lib()).orc_f32_to_bf16(float(x))
+
+
+def f32_to_f16(x, L=None):
+    return (L or lib()).orc_f32_to_f16(float(x))
 
 
 def bf16_to_f32(bits):

@@ -503,3 +503,75 @@ int orc_spec_verify(int B, int G, int V, const float* p, const float* q, int64_t
   }
   return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Repetition penalty ("Sampling system design" post, section on the      */
+/* repetition penalty: a logits processor that reads the sequence's       */
+/* history and lowers the logits of tokens already seen).  The pages leave */
+/* the formula open; this build takes the CTRL rule (Keskar et al. 2019):  */
+/* x / theta for a positive logit, x * theta otherwise, once per distinct  */
+/* token of the history, in binary32, stored back in the logits' format   */
+/* with round-to-nearest-even.                                             */
+/* ---------------------------------------------------------------------- */
+
+uint16_t orc_f32_to_bf16(float f) {
+  uint32_t b;
+  memcpy(&b, &f, sizeof b);
+  if (isnan(f)) return (uint16_t)(((b >> 16) & 0x8000u) | 0x7fc0u);
+  /* round to nearest, ties to even, on the 16 bits kept */
+  uint32_t r = b + 0x7fffu + ((b >> 16) & 1u);
+  return (uint16_t)(r >> 16);
+}
+
+uint16_t orc_f32_to_f16(float f) {
+  uint16_t sign = signbit(f) ? 0x8000u : 0u;
+  double a = fabs((double)f);
+  if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u); /* rounds past 65504 */
+  if (a < ldexp(1.0, -14)) {
+    /* subnormal (or zero): units of 2^-24, ties to even; 1024 units is the
+       smallest normal, which the same code word encodes */
+    double q = rint(ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)q);
+  }
+  int e;
+  frexp(a, &e); /* a = m * 2^e, m in [0.5, 1): the leading bit weighs 2^(e-1) */
+  e -= 1;
+  double q = rint(ldexp(a, 10 - e)); /* significand with 10 fraction bits */
+  if (q >= 2048.0) {
+    q = 1024.0;
+    e += 1;
+  }
+  if (e + 15 >= 31) return (uint16_t)(sign | 0x7c00u);
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0));
+}
+
+int orc_repetition_penalty(void* logits, int dtype, int B, int V, int64_t ld,
+                           const int32_t* history, int H, int64_t hld, const float* penalty,
+                           int32_t* status) {
+  size_t es = (dtype == ORC_F32) ? 4 : 2;
+  unsigned char* seen = (unsigned char*)malloc((size_t)(V > 0 ? V : 1));
+  if (!seen) return -1;
+  for (int r = 0; r < B; ++r) {
+    float th = penalty[r];
+    if (!(th > 0.0f) || isinf(th)) {
+      status[r] = ORC_INVALID;
+      continue;
+    }
+    status[r] = ORC_OK;
+    memset(seen, 0, (size_t)V);
+    char* row = (char*)logits + (size_t)r * (size_t)ld * es;
+    for (int i = 0; i < H; ++i) {
+      int t = history[(size_t)r * (size_t)hld + i];
+      if (t < 0 || t >= V || seen[t]) continue; /* padding, or already penalised */
+      seen[t] = 1;
+      float x = load_logit(row, dtype, t);
+      float y = (x > 0.0f) ? x / th : x * th;
+      if (dtype == ORC_F32) ((float*)row)[t] = y;
+      else if (dtype == ORC_BF16) ((uint16_t*)row)[t] = orc_f32_to_bf16(y);
+      else ((uint16_t*)row)[t] = orc_f32_to_f16(y);
+    }
+  }
+  free(seen);
+  return 0;
+}

@@ -125,6 +125,24 @@ int orc_spec_verify(int B, int G, int V, const float* p, const float* q, int64_t
                     int32_t* out_tokens, int32_t* n_acc, int32_t* status, double* margin,
                     int n_threads);
 
+/* float -> bfloat16 / binary16 with round-to-nearest-even (NaN stays NaN,
+ * overflow gives infinity). */
+uint16_t orc_f32_to_bf16(float f);
+uint16_t orc_f32_to_f16(float f);
+
+/*
+ * Repetition penalty, in place ("Sampling system design" post, section on the
+ * repetition penalty; the formula, which the post leaves open, is the CTRL
+ * rule of Keskar et al. 2019).  For row r and every DISTINCT token t of
+ * history[r][0..H-1] (row stride hld; entries outside [0, V) are padding):
+ * x = x / penalty[r] if x > 0, else x * penalty[r], in binary32, stored back
+ * in the logits' format with round-to-nearest-even.  A penalty that is not
+ * finite and > 0 leaves the row unchanged and sets status[r] = ORC_INVALID.
+ */
+int orc_repetition_penalty(void* logits, int dtype, int B, int V, int64_t ld,
+                           const int32_t* history, int H, int64_t hld, const float* penalty,
+                           int32_t* status);
+
 #ifdef __cplusplus
 }
 #endif

@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 import pins
+import pins_penalty
 import pins_spec
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
@@ -64,6 +65,18 @@ MUTATIONS = [
      "if (d[i] < 0 || d[i] > V) return ORC_INVALID;"),
     ("verify: drawn row not checked", "if (!prob_ok(pr[x]) || (qr && !prob_ok(qr[x]))) {",
      "if (0) {"),
+    # repetition penalty (CTRL rule) and the float encoders
+    ("penalty: every logit divided", "float y = (x > 0.0f) ? x / th : x * th;",
+     "float y = x / th;"),
+    ("penalty: signs swapped", "float y = (x > 0.0f) ? x / th : x * th;",
+     "float y = (x > 0.0f) ? x * th : x / th;"),
+    ("penalty: once per occurrence", "if (t < 0 || t >= V || seen[t]) continue;",
+     "if (t < 0 || t >= V) continue;"),
+    ("penalty: invalid penalty accepted", "if (!(th > 0.0f) || isinf(th)) {", "if (isinf(th)) {"),
+    ("penalty: bf16 truncates", "uint32_t r = b + 0x7fffu + ((b >> 16) & 1u);",
+     "uint32_t r = b;"),
+    ("penalty: f16 ties away from zero", "double q = rint(ldexp(a, 10 - e));",
+     "double q = floor(ldexp(a, 10 - e) + 0.5);"),
 ]
 
 
@@ -94,6 +107,8 @@ def test_pins_catch_mutation(workdir, name, old, new):
     checks = pins.ALL_CHECKS + pins_spec.SPEC_CHECKS
     if name.startswith("verify"):
         checks = pins_spec.SPEC_CHECKS + pins.ALL_CHECKS
+    if name.startswith("penalty"):
+        checks = pins_penalty.PENALTY_CHECKS
     for chk in checks:
         try:
             out = chk(L=L)
