@@ -433,8 +433,33 @@ def run_ours(args, rank, world, local):
     kcount = torch.empty(B, dtype=torch.int32, device=dev)
 
     logprobs = torch.empty(B, dtype=torch.float32, device=dev) if args.logprob else None
+    pen_hist = pen_theta = pen_status = None
+    pen_bytes = 0
+    if args.repetition_penalty:
+        # a history of H token ids per row (repeats included) and a per-row penalty
+        rng = np.random.Generator(np.random.PCG64(11))
+        Hn = args.repetition_penalty
+        hist = rng.integers(0, V, size=(B, Hn)).astype(np.int32)
+        hist[:, Hn // 2:] = hist[:, :Hn - Hn // 2][:, :Hn // 2]
+        pen_hist = torch.as_tensor(hist).to(dev)
+        pen_theta = torch.as_tensor(rng.choice(np.array([1.1, 1.2, 1.3], np.float32),
+                                               size=B)).to(dev)
+        pen_status = torch.empty(B, dtype=torch.int32, device=dev)
+        distinct = sum(len(np.unique(hist[r])) for r in range(B))
+        pen_bytes = B * (Hn * 4 + 4 + 4) + distinct * 2 * esize
+        # every rotated buffer is penalised once, as a decode step's fresh
+        # logits would be; the timed launches then run the same kernel with
+        # theta = 1 (the same loads, arithmetic and stores) so that repeated
+        # steps on a buffer do not compound the penalty
+        for buf in logits:
+            smp.repetition_penalty(buf, pen_hist, pen_theta, status=pen_status)
+        pen_theta = torch.ones(B, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize(dev)
 
     def step(s, lg=None):
+        if pen_hist is not None:
+            smp.repetition_penalty(logits[s % nbuf] if lg is None else lg, pen_hist, pen_theta,
+                                   status=pen_status)
         smp.sample(logits[s % nbuf] if lg is None else lg, t, k, p, seed, offsets[s],
                    bitmask=bitmask, kept_mask=kmask, kept_count=kcount, tokens=tokens,
                    status=status, logprobs=logprobs)
@@ -542,6 +567,32 @@ def run_ours(args, rank, world, local):
 
     peak, peak_kind = measured_peaks()
     alg_bytes = B * (row_bytes(V, bitmask is not None, True, esize) + (4 if args.logprob else 0))
+    alg_bytes += pen_bytes
+    pen_info = None
+    if pen_hist is not None:
+        # the penalty kernel alone, same rotation, timed the same way
+        pg = torch.cuda.CUDAGraph()
+        cap2 = torch.cuda.Stream(dev)
+        cap2.wait_stream(stream)
+        with torch.cuda.stream(cap2):
+            with torch.cuda.graph(pg, stream=cap2):
+                for i in range(args.steps):
+                    smp.repetition_penalty(logits[i % nbuf], pen_hist, pen_theta,
+                                           status=pen_status)
+        stream.wait_stream(cap2)
+        pg.replay()
+        torch.cuda.synchronize(dev)
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        pg.replay()
+        q1.record(stream)
+        torch.cuda.synchronize(dev)
+        pen_ms = q0.elapsed_time(q1) / args.steps
+        pen_info = {"history_per_row": args.repetition_penalty, "kernel_us": 1000 * pen_ms,
+                    "timed_theta": "1 (buffers penalised once with 1.1-1.3 before timing)",
+                    "algorithmic_bytes": pen_bytes,
+                    "gbs": pen_bytes / (pen_ms / 1000.0) / 1e9}
     achieved = alg_bytes / (kern_ms / 1000.0) / 1e9
     traffic = profiled_traffic(args.workload)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -567,9 +618,9 @@ def run_ours(args, rank, world, local):
                        "l2": f"inputs rotated over {nbuf} copies ({nbuf * bytes_logits / 1e6:.0f} MB > L2)",
                        "cluster": plan["cluster"], "slice": plan["slice"],
                        "smem_per_cta": plan["smem"], "paths": paths, "timing": timing,
-                       "logprob": bool(args.logprob)},
+                       "logprob": bool(args.logprob), "repetition_penalty": pen_info},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if pen_hist is not None else 1),
         }
         print(json.dumps(line), flush=True)
     smp.close()
@@ -585,6 +636,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=256)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repetition-penalty", type=int, default=0, metavar="H",
+                    help="apply the repetition penalty (H history ids per row) before each "
+                         "sample call, in place on the step's logits")
     ap.add_argument("--logprob", action="store_true",
                     help="also return each drawn token's log-probability (smp_sample_logprob)")
     args = ap.parse_args()

@@ -212,6 +212,33 @@ int smp_spec_verify(smp_handle h, const float* target_probs, const float* draft_
                     const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
                     int32_t* n_accepted, int32_t* row_status, smp_stream stream);
 
+/* Repetition penalty, applied IN PLACE to the logits before sampling
+ * ("Sampling system design" post, section on the repetition penalty: a
+ * logits processor that reads each sequence's history tokens and lowers the
+ * logits of tokens already seen).  The post leaves the formula open; this is
+ * the CTRL rule (Keskar et al. 2019): for row r, theta = penalty[r], and
+ * every DISTINCT token t among history[r][0..H-1],
+ *     x_t <- x_t / theta  if x_t > 0,   x_t <- x_t * theta  otherwise,
+ * computed in binary32 with correct rounding and stored back in the logits'
+ * format with round-to-nearest-even (-inf stays -inf; theta = 1 changes
+ * nothing).  Tokens that appear several times are penalised once.
+ *   logits    : DEVICE [B][ld] of dtype, modified in place.
+ *   history   : DEVICE int32 [B][history_ld], H entries per row; entries
+ *               outside [0, V) are padding.  NULL allowed when H == 0.
+ *   penalty   : DEVICE float [B]; a value that is not finite and > 0 leaves
+ *               the row unchanged with row_status SMP_ERR_INVALID_PARAM.
+ *   row_status: DEVICE int32 [B], required (SMP_OK or the above).
+ * Call status: SMP_ERR_INVALID_PARAM for NULL required pointers, B < 0,
+ * V < 1, ld < V, H < 0, history_ld < H or an unknown dtype;
+ * SMP_ERR_CAPACITY for B or V beyond the handle's limits or V above
+ * 1,572,864; SMP_ERR_CUDA when the launch fails.  Work: one launch, one CTA
+ * per row; it reads the history and reads and writes only the logits of the
+ * history's tokens (never the whole row).  Issue it on the sampler's stream
+ * before smp_sample. */
+int smp_repetition_penalty(smp_handle h, void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                           const int32_t* history, int H, int64_t history_ld,
+                           const float* penalty, int32_t* row_status, smp_stream stream);
+
 /* Optional per-row diagnostics for subsequent calls on this handle: when
  * row_info is not NULL, each call writes int32 [B][4] to it (DEVICE memory
  * owned by the caller, at least max_batch*4 entries): {path, band size,

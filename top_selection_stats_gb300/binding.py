@@ -15,7 +15,8 @@ PATH_NAMES = {0: "error", 1: "greedy", 2: "all", 3: "sigma", 4: "full"}
 _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_F16}
 
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
-           "smp_sample_noalloc", "smp_sample_logprob", "smp_spec_verify", "smp_set_row_info",
+           "smp_sample_noalloc", "smp_sample_logprob", "smp_spec_verify",
+           "smp_repetition_penalty", "smp_set_row_info",
            "smp_plan",
            "smp_status_string")
 
@@ -58,6 +59,8 @@ def load_library(path=None):
     L.smp_sample_noalloc.argtypes = [P, I, I, I, ctypes.c_int64, P, ctypes.POINTER(RowParams), P,
                                      P, P, P, P]
     L.smp_spec_verify.argtypes = [P, P, P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P]
+    L.smp_repetition_penalty.argtypes = [P, P, I, I, I, ctypes.c_int64, P, I, ctypes.c_int64, P,
+                                         P, P]
     L.smp_set_row_info.argtypes = [P, P]
     L.smp_plan.argtypes = [P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
@@ -218,6 +221,29 @@ class Sampler:
                                  _ptr(bitmask), _ptr(tokens), _ptr(status), self._stream())
         _check(rc, "smp_argmax")
         return dict(tokens=tokens, status=status)
+
+    def repetition_penalty(self, logits, history, penalty, V=None, status=None):
+        """Repetition penalty in place on logits ([B, ld]): history int32 [B, H]
+        (entries outside [0, V) are padding), penalty float32 [B].  Returns the
+        per-row status tensor."""
+        if logits.dtype not in _DTYPES:
+            raise ValueError(f"unsupported logits dtype {logits.dtype}")
+        self._check_tensor(logits, "logits")
+        self._check_tensor(history, "history", torch.int32)
+        self._check_tensor(penalty, "penalty", torch.float32)
+        B, ld = logits.shape
+        V = ld if V is None else V
+        if history.dim() != 2 or history.shape[0] != B or penalty.numel() != B:
+            raise ValueError("history must be [B, H] and penalty [B]")
+        H = history.shape[1]
+        status = torch.empty(B, dtype=torch.int32, device=self.device) if status is None \
+            else status
+        self._check_tensor(status, "status", torch.int32)
+        rc = self.lib.smp_repetition_penalty(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V,
+                                             ld, _ptr(history) if H else None, H, H,
+                                             _ptr(penalty), _ptr(status), self._stream())
+        _check(rc, "smp_repetition_penalty")
+        return status
 
     def spec_verify(self, target_probs, draft_probs, draft_tokens, seed, offset, V=None,
                     out_tokens=None, n_accepted=None, status=None):

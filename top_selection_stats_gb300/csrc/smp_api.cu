@@ -24,6 +24,10 @@ cudaError_t launch_f16(const KArgs& a, int grid, cudaStream_t st);
 int verify_enqueue(const float* p, const float* q, const int32_t* d, int B, int G, int V,
                    int64_t ld, const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
                    int32_t* n_acc, int32_t* status, cudaStream_t st);
+cudaError_t penalty_setup();
+int penalty_enqueue(void* logits, int dtype, int B, int V, long long ld, const int32_t* history,
+                    int H, long long hld, const float* penalty, int32_t* status,
+                    cudaStream_t st);
 }  // namespace smp
 
 using namespace smp;
@@ -181,7 +185,8 @@ int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
     }
     per_sm = nb < per_sm ? nb : per_sm;
   }
-  if (per_sm < 1) {
+  if (per_sm < 1 || penalty_setup() != cudaSuccess) {
+    cudaGetLastError();
     delete h;
     return SMP_ERR_CUDA;
   }
@@ -273,6 +278,19 @@ int smp_spec_verify(smp_handle h, const float* target_probs, const float* draft_
   DeviceGuard guard(h->device);
   return verify_enqueue(target_probs, draft_probs, draft_tokens, B, G, V, ld, seed, offset,
                         out_tokens, n_accepted, row_status, (cudaStream_t)stream);
+}
+
+int smp_repetition_penalty(smp_handle h, void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                           const int32_t* history, int H, int64_t history_ld,
+                           const float* penalty, int32_t* row_status, smp_stream stream) {
+  if (!h || !logits || !penalty || !row_status) return SMP_ERR_INVALID_PARAM;
+  if ((int)dtype < 0 || (int)dtype > 2) return SMP_ERR_INVALID_PARAM;
+  if (B < 0 || V < 1 || ld < V || H < 0 || history_ld < H) return SMP_ERR_INVALID_PARAM;
+  if (H > 0 && !history) return SMP_ERR_INVALID_PARAM;
+  if (B > h->max_batch || V > h->max_vocab) return SMP_ERR_CAPACITY;
+  DeviceGuard guard(h->device);
+  return penalty_enqueue(logits, (int)dtype, B, V, ld, history, H, history_ld, penalty,
+                         row_status, (cudaStream_t)stream);
 }
 
 const char* smp_status_string(int code) {
