@@ -19,6 +19,9 @@ Parity status of each function (what pins it is listed in the tests):
                         worked values of the CTRL rule, duplicates and padding
                         in the history, and the encoders against numpy / torch
                         round-to-nearest-even casts over many values.
+  * orc_gumbel_sample -- pinned by its frequencies against the exact softmax
+                        of the kept set (the lecture's Gumbel-max identity),
+                        greedy at T = 0, statuses and the uniform's range.
   * orc_spec_verify_u / orc_spec_verify -- pinned by the exact output
                         distribution (it equals the target's, the identity of
                         the lecture notes' section 5.2), the acceptance rate
@@ -70,6 +73,11 @@ def load(path):
     L.orc_repetition_penalty.restype = ctypes.c_int
     L.orc_repetition_penalty.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int64, P, ctypes.c_int, ctypes.c_int64, P, P]
+    L.orc_gumbel_uniform.restype = ctypes.c_double
+    L.orc_gumbel_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int]
+    L.orc_gumbel_sample.restype = ctypes.c_int
+    L.orc_gumbel_sample.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                    P, P, P, P, P, P, P, ctypes.c_int]
     L.orc_row_stats.restype = ctypes.c_int
     L.orc_row_stats.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
     return L
@@ -235,6 +243,29 @@ def f32_to_bf16(x, L=None):
 
 def f32_to_f16(x, L=None):
     return (L or lib()).orc_f32_to_f16(float(x))
+
+
+def gumbel_uniform(seed, offset, i, L=None):
+    return (L or lib()).orc_gumbel_uniform(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                           int(i))
+
+
+def gumbel_sample(logits_bits, dtype, V, temperature, seed, offset, kept_mask=None, ld=None,
+                  n_threads=1, L=None):
+    """Gumbel-max draw per row; returns dict(token, status, margin)."""
+    arr = np.ascontiguousarray(logits_bits)
+    B = arr.shape[0]
+    ld = arr.shape[1] if ld is None else ld
+    km = None if kept_mask is None else np.ascontiguousarray(kept_mask, dtype=np.uint32)
+    t = np.ascontiguousarray(temperature, dtype=np.float32)
+    s = np.ascontiguousarray(seed, dtype=np.uint64)
+    o = np.ascontiguousarray(offset, dtype=np.uint64)
+    tok = np.zeros(B, dtype=np.int32)
+    st = np.zeros(B, dtype=np.int32)
+    mg = np.zeros(B, dtype=np.float64)
+    (L or lib()).orc_gumbel_sample(_ptr(arr), _DT[dtype], B, V, ld, _ptr(km), _ptr(t), _ptr(s),
+                                   _ptr(o), _ptr(tok), _ptr(st), _ptr(mg), int(n_threads))
+    return dict(token=tok, status=st, margin=mg)
 
 
 def bf16_to_f32(bits):

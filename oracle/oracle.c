@@ -575,3 +575,83 @@ int orc_repetition_penalty(void* logits, int dtype, int B, int V, int64_t ld,
   free(seen);
   return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Gumbel-max sampling over a kept set (lecture notes "Decoding: Sampling, */
+/* Beam Search and Speculative Decoding", section 3.2: argmax of the       */
+/* logits plus Gumbel noise is a draw from their softmax): a sort-free     */
+/* second sampler family, used for comparison with the inverse-CDF draw.   */
+/* ---------------------------------------------------------------------- */
+
+/* The uniform of element i of a row: word (i mod 4) of the Philox4x32-10
+   block at key (lo32 seed, hi32 seed), counter (lo32 offset, hi32 offset,
+   i / 4, 0x47554D42), mapped to the open interval (0, 1) as
+   ((w >> 8) + 1/2) * 2^-24. */
+double orc_gumbel_uniform(uint64_t seed, uint64_t offset, int i) {
+  uint32_t ctr[4] = {(uint32_t)offset, (uint32_t)(offset >> 32), (uint32_t)(i >> 2),
+                     0x47554D42u};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  return ((double)(out[i & 3] >> 8) + 0.5) * (1.0 / 16777216.0);
+}
+
+int orc_gumbel_sample(const void* logits, int dtype, int B, int V, int64_t ld,
+                      const uint32_t* kept_mask, const float* temperature,
+                      const uint64_t* seed, const uint64_t* offset, int32_t* token,
+                      int32_t* status, double* margin, int n_threads) {
+  int W = (V + 31) / 32;
+  size_t es = (dtype == ORC_F32) ? 4 : 2;
+  if (n_threads < 1) n_threads = 1;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+#endif
+  for (int r = 0; r < B; ++r) {
+    const char* row = (const char*)logits + (size_t)r * (size_t)ld * es;
+    const uint32_t* mrow = kept_mask ? kept_mask + (size_t)r * (size_t)W : NULL;
+    float t = temperature[r];
+    token[r] = -1;
+    margin[r] = INFINITY;
+    if (!(t >= 0.0f)) {
+      status[r] = ORC_INVALID;
+      continue;
+    }
+    int best = -1, nonfinite = 0;
+    double bv = -INFINITY, second = -INFINITY;
+    for (int i = 0; i < V; ++i) {
+      if (!mask_allows(mrow, i)) continue;
+      float x = load_logit(row, dtype, i);
+      if (isinf(x) && x < 0) continue;
+      if (isnan(x) || isinf(x)) {
+        nonfinite = 1;
+        break;
+      }
+      double v;
+      if (t == 0.0f) {
+        v = (double)x; /* greedy: no noise, the first maximum wins */
+      } else {
+        double u = orc_gumbel_uniform(seed[r], offset[r], i);
+        v = (double)(x / t) - log(-log(u));
+      }
+      if (v > bv) {
+        second = bv;
+        bv = v;
+        best = i;
+      } else if (v > second) {
+        second = v;
+      }
+    }
+    if (nonfinite) {
+      status[r] = ORC_NONFINITE;
+      continue;
+    }
+    if (best < 0) {
+      status[r] = ORC_EMPTY;
+      continue;
+    }
+    status[r] = ORC_OK;
+    token[r] = best;
+    margin[r] = bv - second;
+  }
+  return 0;
+}

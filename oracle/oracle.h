@@ -143,6 +143,23 @@ int orc_repetition_penalty(void* logits, int dtype, int B, int V, int64_t ld,
                            const int32_t* history, int H, int64_t hld, const float* penalty,
                            int32_t* status);
 
+/*
+ * Gumbel-max sampling (lecture notes, section 3.2: the argmax of
+ * z_i + g_i with g_i = -log(-log(u_i)) is a draw from softmax(z)), a
+ * sort-free second sampler for comparison.  Per row: candidates are the
+ * tokens whose kept_mask bit is set (kept_mask [B][ceil(V/32)], NULL = all)
+ * and whose logit is not -inf; z_i = fl32(x_i / T); u_i from
+ * orc_gumbel_uniform; T == 0 takes the argmax of x (first maximum).  The
+ * perturbed values are evaluated in double; margin[r] = best - second best.
+ * Status: ORC_INVALID (T NaN or < 0), ORC_NONFINITE (NaN / +inf among the
+ * candidates), ORC_EMPTY (no candidate); token -1 on those rows.
+ */
+double orc_gumbel_uniform(uint64_t seed, uint64_t offset, int i);
+int orc_gumbel_sample(const void* logits, int dtype, int B, int V, int64_t ld,
+                      const uint32_t* kept_mask, const float* temperature,
+                      const uint64_t* seed, const uint64_t* offset, int32_t* token,
+                      int32_t* status, double* margin, int n_threads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 import pins
+import pins_gumbel
 import pins_penalty
 import pins_spec
 
@@ -77,6 +78,15 @@ MUTATIONS = [
      "uint32_t r = b;"),
     ("penalty: f16 ties away from zero", "double q = rint(ldexp(a, 10 - e));",
      "double q = floor(ldexp(a, 10 - e) + 0.5);"),
+    # Gumbel-max sampler
+    ("gumbel: noise sign flipped", "v = (double)(x / t) - log(-log(u));",
+     "v = (double)(x / t) + log(-log(u));"),
+    ("gumbel: temperature ignored", "v = (double)(x / t) - log(-log(u));",
+     "v = (double)x - log(-log(u));"),
+    ("gumbel: kept mask ignored", "if (!mask_allows(mrow, i)) continue;", ";"),
+    ("gumbel: greedy keeps the last maximum", "if (v > bv) {", "if (v >= bv) {"),
+    ("gumbel: one word per block", "return ((double)(out[i & 3] >> 8) + 0.5) * (1.0 / 16777216.0);",
+     "return ((double)(out[0] >> 8) + 0.5) * (1.0 / 16777216.0);"),
 ]
 
 
@@ -109,6 +119,8 @@ def test_pins_catch_mutation(workdir, name, old, new):
         checks = pins_spec.SPEC_CHECKS + pins.ALL_CHECKS
     if name.startswith("penalty"):
         checks = pins_penalty.PENALTY_CHECKS
+    if name.startswith("gumbel"):
+        checks = pins_gumbel.GUMBEL_CHECKS
     for chk in checks:
         try:
             out = chk(L=L)
