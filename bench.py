@@ -18,6 +18,7 @@ Multi-GPU (torchrun): rows are independent, every rank runs its own batch,
 no collective on the data path (weak scaling).
 """
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -407,7 +408,7 @@ def run_verify(args, rank, world, local):
 
 
 def run_ours(args, rank, world, local):
-    from top_selection_stats_gb300 import Sampler, workloads
+    from top_selection_stats_gb300 import Sampler, binding, workloads
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     case = workloads.make(args.workload, device="cpu")
@@ -599,6 +600,54 @@ def run_ours(args, rank, world, local):
             "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
             "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kern_ms}
 
+    gumbel_info = None
+    if args.gumbel:
+        # the sort-free second sampler: the kept set from smp_topk_topp_mask,
+        # then a Gumbel-max draw over it (two launches per step), against the
+        # fused smp_sample timed above
+        mk = smp.topk_topp_mask(logits[0], t, k, p, bitmask=bitmask)["kept_mask"]
+        gtok = torch.empty(B, dtype=torch.int32, device=dev)
+        gst = torch.empty(B, dtype=torch.int32, device=dev)
+        gbuf = torch.empty((B, W), dtype=torch.int32, device=dev)
+        gcnt = torch.empty(B, dtype=torch.int32, device=dev)
+        gstat = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def gumbel_only(i):
+            smp.gumbel_sample(logits[i % nbuf], t, seed, offsets[i], kept_mask=mk, tokens=gtok,
+                              status=gst)
+
+        def mask_then_gumbel(i):
+            smp.lib.smp_topk_topp_mask(
+                smp.h, binding._ptr(logits[i % nbuf]), binding._DTYPES[logits[0].dtype], B, V, V,
+                binding._ptr(bitmask), ctypes.byref(binding.RowParams(
+                    t.data_ptr(), k.data_ptr(), p.data_ptr(), None, None)),
+                binding._ptr(gbuf), binding._ptr(gcnt), binding._ptr(gstat), None,
+                smp._stream())
+            smp.gumbel_sample(logits[i % nbuf], t, seed, offsets[i], kept_mask=gbuf, tokens=gtok,
+                              status=gst)
+
+        gumbel_info = {}
+        for name, fn in (("gumbel_kernel_us", gumbel_only), ("mask_plus_gumbel_us",
+                                                              mask_then_gumbel)):
+            gg = torch.cuda.CUDAGraph()
+            cap3 = torch.cuda.Stream(dev)
+            cap3.wait_stream(stream)
+            with torch.cuda.stream(cap3):
+                with torch.cuda.graph(gg, stream=cap3):
+                    for i in range(args.steps):
+                        fn(args.warmup + i)
+            stream.wait_stream(cap3)
+            gg.replay()
+            torch.cuda.synchronize(dev)
+            q0 = torch.cuda.Event(enable_timing=True)
+            q1 = torch.cuda.Event(enable_timing=True)
+            q0.record(stream)
+            gg.replay()
+            q1.record(stream)
+            torch.cuda.synchronize(dev)
+            gumbel_info[name] = 1000 * q0.elapsed_time(q1) / args.steps
+        gumbel_info["fused_smp_sample_us"] = 1000 * kern_ms
+
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
         rows = min(B, args.cpu_rows)
@@ -618,7 +667,8 @@ def run_ours(args, rank, world, local):
                        "l2": f"inputs rotated over {nbuf} copies ({nbuf * bytes_logits / 1e6:.0f} MB > L2)",
                        "cluster": plan["cluster"], "slice": plan["slice"],
                        "smem_per_cta": plan["smem"], "paths": paths, "timing": timing,
-                       "logprob": bool(args.logprob), "repetition_penalty": pen_info},
+                       "logprob": bool(args.logprob), "repetition_penalty": pen_info,
+                       "gumbel": gumbel_info},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * (2 if pen_hist is not None else 1),
         }
@@ -639,6 +689,8 @@ def main():
     ap.add_argument("--repetition-penalty", type=int, default=0, metavar="H",
                     help="apply the repetition penalty (H history ids per row) before each "
                          "sample call, in place on the step's logits")
+    ap.add_argument("--gumbel", action="store_true",
+                    help="also time the Gumbel-max sampler (kept mask + smp_gumbel_sample)")
     ap.add_argument("--logprob", action="store_true",
                     help="also return each drawn token's log-probability (smp_sample_logprob)")
     args = ap.parse_args()

@@ -239,6 +239,32 @@ int smp_repetition_penalty(smp_handle h, void* logits, smp_dtype dtype, int B, i
                            const int32_t* history, int H, int64_t history_ld,
                            const float* penalty, int32_t* row_status, smp_stream stream);
 
+/* Gumbel-max sampling over a kept set: a sort-free second sampler family
+ * for distribution and timing comparisons (lecture notes "Decoding:
+ * Sampling, Beam Search and Speculative Decoding", section 3.2: the argmax of
+ * z_i + g_i, with g_i = -log(-log(u_i)) independent Gumbel noise, is a draw
+ * from softmax(z)).  Per row: candidates are the tokens whose kept_mask bit
+ * is set (kept_mask NULL: every token) and whose logit is not -inf; z_i =
+ * fl32(x_i / T); u_i = ((w >> 8) + 1/2) * 2^-24 with w word (i mod 4) of the
+ * Philox4x32-10 block at key (lo32 seed[r], hi32 seed[r]) and counter
+ * (lo32 offset[r], hi32 offset[r], i / 4, 0x47554D42); the token is the
+ * argmax of z_i + g_i (fp32; smallest id on ties); T == 0 takes the argmax
+ * of x.  With the kept_mask that smp_topk_topp_mask writes, the draw follows
+ * the same top-k / top-p distribution as smp_sample's (different draws: it
+ * uses its own random numbers and no prefix sum).
+ *   kept_mask : DEVICE uint32 [B][ceil(V/32)], nullable (layout of bitmask).
+ *   temperature, seed, offset: DEVICE [B]; tokens, row_status: DEVICE [B].
+ * Row status: SMP_ERR_INVALID_PARAM (T NaN or < 0), SMP_ERR_NONFINITE (NaN
+ * or +inf among the candidates), SMP_ERR_EMPTY (no candidate); token -1.
+ * Call status: SMP_ERR_INVALID_PARAM for NULL required pointers, B < 0,
+ * V < 1, ld < V or an unknown dtype; SMP_ERR_CAPACITY beyond the handle's
+ * limits; SMP_ERR_CUDA when the launch fails.  Work: one pass over each row
+ * (a cluster of up to 8 CTAs per row); no workspace. */
+int smp_gumbel_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                      const uint32_t* kept_mask, const float* temperature, const uint64_t* seed,
+                      const uint64_t* offset, int32_t* tokens, int32_t* row_status,
+                      smp_stream stream);
+
 /* Optional per-row diagnostics for subsequent calls on this handle: when
  * row_info is not NULL, each call writes int32 [B][4] to it (DEVICE memory
  * owned by the caller, at least max_batch*4 entries): {path, band size,

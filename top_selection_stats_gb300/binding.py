@@ -16,7 +16,7 @@ _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_
 
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
            "smp_sample_noalloc", "smp_sample_logprob", "smp_spec_verify",
-           "smp_repetition_penalty", "smp_set_row_info",
+           "smp_repetition_penalty", "smp_gumbel_sample", "smp_set_row_info",
            "smp_plan",
            "smp_status_string")
 
@@ -61,6 +61,7 @@ def load_library(path=None):
     L.smp_spec_verify.argtypes = [P, P, P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P]
     L.smp_repetition_penalty.argtypes = [P, P, I, I, I, ctypes.c_int64, P, I, ctypes.c_int64, P,
                                          P, P]
+    L.smp_gumbel_sample.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P, P]
     L.smp_set_row_info.argtypes = [P, P]
     L.smp_plan.argtypes = [P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
@@ -244,6 +245,20 @@ class Sampler:
                                              _ptr(penalty), _ptr(status), self._stream())
         _check(rc, "smp_repetition_penalty")
         return status
+
+    def gumbel_sample(self, logits, temperature, seed, offset, kept_mask=None, V=None,
+                      tokens=None, status=None):
+        """Gumbel-max draw per row over the kept set (kept_mask int32 [B, W] as
+        written by topk_topp_mask, or None for every token)."""
+        B, V, ld, _ = self._prep(logits, V, kept_mask, temperature, None, None, seed, offset)
+        dev = self.device
+        tokens = torch.empty(B, dtype=torch.int32, device=dev) if tokens is None else tokens
+        status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+        rc = self.lib.smp_gumbel_sample(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V, ld,
+                                        _ptr(kept_mask), _ptr(temperature), _ptr(seed),
+                                        _ptr(offset), _ptr(tokens), _ptr(status), self._stream())
+        _check(rc, "smp_gumbel_sample")
+        return dict(tokens=tokens, status=status)
 
     def spec_verify(self, target_probs, draft_probs, draft_tokens, seed, offset, V=None,
                     out_tokens=None, n_accepted=None, status=None):

@@ -14,7 +14,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libsmp.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = [os.path.join(CSRC, f) for f in ("smp_api.cu", "smp_k_f32.cu", "smp_k_bf16.cu",
-                                           "smp_k_f16.cu", "smp_verify.cu", "smp_penalty.cu")]
+                                           "smp_k_f16.cu", "smp_verify.cu", "smp_penalty.cu",
+                                           "smp_gumbel.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("smp_device.cuh", "smp_core.cuh", "smp_list.cuh",
                                            "smp_stream_passes.cuh", "smp_general.cuh",
                                            "smp_kernel.cuh")]

@@ -25,6 +25,9 @@ int verify_enqueue(const float* p, const float* q, const int32_t* d, int B, int 
                    int64_t ld, const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
                    int32_t* n_acc, int32_t* status, cudaStream_t st);
 cudaError_t penalty_setup();
+int gumbel_enqueue(const void* logits, int dtype, int B, int V, long long ld,
+                   const uint32_t* kept, const float* temperature, const uint64_t* seed,
+                   const uint64_t* offset, int32_t* tokens, int32_t* status, cudaStream_t st);
 int penalty_enqueue(void* logits, int dtype, int B, int V, long long ld, const int32_t* history,
                     int H, long long hld, const float* penalty, int32_t* status,
                     cudaStream_t st);
@@ -291,6 +294,20 @@ int smp_repetition_penalty(smp_handle h, void* logits, smp_dtype dtype, int B, i
   DeviceGuard guard(h->device);
   return penalty_enqueue(logits, (int)dtype, B, V, ld, history, H, history_ld, penalty,
                          row_status, (cudaStream_t)stream);
+}
+
+int smp_gumbel_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                      const uint32_t* kept_mask, const float* temperature, const uint64_t* seed,
+                      const uint64_t* offset, int32_t* tokens, int32_t* row_status,
+                      smp_stream stream) {
+  if (!h || !logits || !temperature || !seed || !offset || !tokens || !row_status)
+    return SMP_ERR_INVALID_PARAM;
+  if ((int)dtype < 0 || (int)dtype > 2) return SMP_ERR_INVALID_PARAM;
+  if (B < 0 || V < 1 || ld < V) return SMP_ERR_INVALID_PARAM;
+  if (B > h->max_batch || V > h->max_vocab) return SMP_ERR_CAPACITY;
+  DeviceGuard guard(h->device);
+  return gumbel_enqueue(logits, (int)dtype, B, V, ld, kept_mask, temperature, seed, offset, tokens,
+                        row_status, (cudaStream_t)stream);
 }
 
 const char* smp_status_string(int code) {
