@@ -40,7 +40,8 @@ KERNEL_SOURCES = ["top_selection_stats_gb300/csrc/" + f for f in (
     "smp_general.cuh", "smp_kernel.cuh", "smp_api.cu")]
 
 
-VERIFY_SOURCES = ["top_selection_stats_gb300/csrc/" + f for f in ("smp_verify.cu", "smp_api.cu")]
+# the verification kernel, its launch plan and its enqueue all live in one file
+VERIFY_SOURCES = ["top_selection_stats_gb300/csrc/smp_verify.cu"]
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES):
