@@ -36,12 +36,13 @@ sys.path.insert(0, ROOT)
 METRIC = "rows/sec and achieved HBM GB/s (fraction of roofline), B=256 V=128256 bf16"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["top_selection_stats_gb300/csrc/" + f for f in (
-    "smp_device.cuh", "smp_core.cuh", "smp_list.cuh", "smp_stream_passes.cuh",
+    "smp_philox.cuh", "smp_device.cuh", "smp_core.cuh", "smp_list.cuh", "smp_stream_passes.cuh",
     "smp_general.cuh", "smp_kernel.cuh", "smp_api.cu")]
 
 
 # the verification kernel, its launch plan and its enqueue all live in one file
-VERIFY_SOURCES = ["top_selection_stats_gb300/csrc/smp_verify.cu"]
+VERIFY_SOURCES = ["top_selection_stats_gb300/csrc/" + f for f in ("smp_verify.cu",
+                                                                  "smp_philox.cuh")]
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES):

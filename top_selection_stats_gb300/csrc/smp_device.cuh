@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "smp_philox.cuh"
+
 namespace smp {
 namespace cg = cooperative_groups;
 
@@ -112,28 +114,14 @@ __device__ __forceinline__ void red_or_global(uint32_t* p, uint32_t v) {
 }
 
 // --------------------------------------------------------------------------
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): round function and key
-// schedule from the paper.  key = (lo32 seed, hi32 seed), counter = (lo32
-// offset, hi32 offset, 0, 0); u = (word0 >> 8) * 2^-24 in [0, 1).
+// The sampler's uniform: Philox4x32-10 (smp_philox.cuh) at key (lo32 seed,
+// hi32 seed), counter (lo32 offset, hi32 offset, 0, 0); u = (word0 >> 8) *
+// 2^-24 in [0, 1).
 // --------------------------------------------------------------------------
 __device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t offset) {
-  uint32_t c0 = (uint32_t)offset, c1 = (uint32_t)(offset >> 32), c2 = 0u, c3 = 0u;
-  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-    uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-    uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-    c0 = n0;
-    c1 = lo1;
-    c2 = n2;
-    c3 = lo0;
-  }
-  return (double)(c0 >> 8) * (1.0 / 16777216.0);
+  uint32_t w[4];
+  philox4x32_10(seed, (uint32_t)offset, (uint32_t)(offset >> 32), 0u, 0u, w);
+  return (double)(w[0] >> 8) * (1.0 / 16777216.0);
 }
 
 // --------------------------------------------------------------------------

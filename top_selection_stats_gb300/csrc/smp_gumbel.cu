@@ -26,6 +26,7 @@
 #include <cstdint>
 
 #include "../../include/smp.h"
+#include "smp_philox.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -56,29 +57,6 @@ struct Best {
 
 __device__ __forceinline__ bool better(float v, int id, float bv, int bid) {
   return v > bv || (v == bv && id < bid);
-}
-
-__device__ __forceinline__ void philox_block(uint64_t seed, uint32_t c0, uint32_t c1, uint32_t c2,
-                                             uint32_t c3, uint32_t (&o)[4]) {
-  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-    const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-    c0 = n0;
-    c1 = lo1;
-    c2 = n2;
-    c3 = lo0;
-  }
-  o[0] = c0;
-  o[1] = c1;
-  o[2] = c2;
-  o[3] = c3;
 }
 
 // -log(-log(u)) for u = (k + 1/2) * 2^-24, k = w >> 8 in [0, 2^24).
@@ -157,8 +135,8 @@ __global__ void __launch_bounds__(GT, 8) gumbel_kernel(const GumbelArgs a) {
       float x[4];
       load4<DT>(row, i, a.V, a.vec != 0, x);
       uint32_t w[4] = {0u, 0u, 0u, 0u};
-      if (!greedy) philox_block(seed, (uint32_t)off, (uint32_t)(off >> 32), (uint32_t)(i >> 2),
-                                0x47554D42u, w);
+      if (!greedy) philox4x32_10(seed, (uint32_t)off, (uint32_t)(off >> 32), (uint32_t)(i >> 2),
+                                 0x47554D42u, w);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (!((kw >> e) & 1u) || i + e >= i1) continue;

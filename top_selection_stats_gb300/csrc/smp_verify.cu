@@ -27,6 +27,7 @@
 #include <cstdint>
 
 #include "../../include/smp.h"
+#include "smp_philox.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -69,28 +70,14 @@ __device__ __forceinline__ uint64_t fx42(float w) {
 
 __device__ __forceinline__ bool prob_ok(float v) { return v >= 0.f && v <= 1.f; }
 
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): words 0 and 1 of the
-// block at key (lo32 seed, hi32 seed), counter (lo32 ctr, hi32 ctr, 0, 0).
+// Words 0 and 1 of the Philox4x32-10 block at key (lo32 seed, hi32 seed),
+// counter (lo32 ctr, hi32 ctr, 0, 0).
 __device__ __forceinline__ void philox_w01(uint64_t seed, uint64_t ctr, uint32_t& w0,
                                            uint32_t& w1) {
-  uint32_t c0 = (uint32_t)ctr, c1 = (uint32_t)(ctr >> 32), c2 = 0u, c3 = 0u;
-  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-    const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-    c0 = n0;
-    c1 = lo1;
-    c2 = n2;
-    c3 = lo0;
-  }
-  w0 = c0;
-  w1 = c1;
+  uint32_t w[4];
+  philox4x32_10(seed, (uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, w);
+  w0 = w[0];
+  w1 = w[1];
 }
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
