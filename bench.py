@@ -602,6 +602,40 @@ def run_ours(args, rank, world, local):
             "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
             "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kern_ms}
 
+    toplp_info = None
+    if args.top_logprobs:
+        # the n best kept tokens and their logprobs from the last step's outputs
+        tl_ids = torch.empty((B, args.top_logprobs), dtype=torch.int32, device=dev)
+        tl_lp = torch.empty((B, args.top_logprobs), dtype=torch.float32, device=dev)
+        last = args.warmup + args.steps - 1
+
+        def toplp(i):
+            smp.lib.smp_top_logprobs(smp.h, binding._ptr(logits[last % nbuf]),
+                                     binding._DTYPES[logits[0].dtype], B, V, V,
+                                     binding._ptr(kmask), binding._ptr(t), binding._ptr(tokens),
+                                     binding._ptr(logprobs), args.top_logprobs,
+                                     binding._ptr(tl_ids), binding._ptr(tl_lp), smp._stream())
+
+        tg = torch.cuda.CUDAGraph()
+        cap4 = torch.cuda.Stream(dev)
+        cap4.wait_stream(stream)
+        with torch.cuda.stream(cap4):
+            with torch.cuda.graph(tg, stream=cap4):
+                for i in range(args.steps):
+                    toplp(i)
+        stream.wait_stream(cap4)
+        tg.replay()
+        torch.cuda.synchronize(dev)
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        tg.replay()
+        q1.record(stream)
+        torch.cuda.synchronize(dev)
+        toplp_info = {"n": args.top_logprobs,
+                      "kernel_us": 1000 * q0.elapsed_time(q1) / args.steps,
+                      "note": "one buffer (its kept masks in L2 between launches)"}
+
     gumbel_info = None
     if args.gumbel:
         # the sort-free second sampler: the kept set from smp_topk_topp_mask,
@@ -670,7 +704,7 @@ def run_ours(args, rank, world, local):
                        "cluster": plan["cluster"], "slice": plan["slice"],
                        "smem_per_cta": plan["smem"], "paths": paths, "timing": timing,
                        "logprob": bool(args.logprob), "repetition_penalty": pen_info,
-                       "gumbel": gumbel_info},
+                       "gumbel": gumbel_info, "top_logprobs": toplp_info},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * (2 if pen_hist is not None else 1),
         }
@@ -691,12 +725,16 @@ def main():
     ap.add_argument("--repetition-penalty", type=int, default=0, metavar="H",
                     help="apply the repetition penalty (H history ids per row) before each "
                          "sample call, in place on the step's logits")
+    ap.add_argument("--top-logprobs", type=int, default=0, metavar="N",
+                    help="also time smp_top_logprobs (N best kept tokens; implies --logprob)")
     ap.add_argument("--gumbel", action="store_true",
                     help="also time the Gumbel-max sampler (kept mask + smp_gumbel_sample)")
     ap.add_argument("--logprob", action="store_true",
                     help="also return each drawn token's log-probability (smp_sample_logprob)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.top_logprobs:
+        args.logprob = True
     rank, world, local = dist_setup(args.gpus)
     verify = args.workload.startswith("verify")
     if args.impl == "reference":

@@ -132,6 +132,26 @@ int smp_sample_logprob(smp_handle h, const void* logits, smp_dtype dtype, int B,
                        int32_t* tokens, float* logprobs, int32_t* row_status,
                        uint32_t* kept_mask, int32_t* kept_count, smp_stream stream);
 
+/* Top logprobs: the n most likely tokens of each row's kept set with their
+ * log-probabilities ("Sampling system design" post, section on logprobs),
+ * under the same processed distribution as smp_sample_logprob.  Inputs are
+ * that call's outputs for the same logits and parameters: kept_mask
+ * [B][ceil(V/32)], tokens [B] and logprobs [B] (all DEVICE).  Per row the
+ * kept tokens are ranked by logit (descending, smallest id first among equal
+ * logits); top_ids [B][n] receives the first n ids, top_logprobs [B][n]
+ * their log-probabilities, computed as
+ *     logprobs[r] + (fl32(x_j / T) - fl32(x_tok / T))
+ * (two kept tokens' log-probabilities differ by their scaled logits' difference;
+ * greedy rows: 0 for the argmax).  Slots past the kept set's size get id -1
+ * and -inf; rows whose token is -1 (an error row) get -1 and NaN.
+ * 1 <= n <= 32 (larger n: SMP_ERR_CAPACITY).  Call status as for
+ * smp_gumbel_sample.  Work: one pass over each row's kept mask and its kept
+ * logits (a cluster of up to 8 CTAs per row). */
+int smp_top_logprobs(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                     const uint32_t* kept_mask, const float* temperature, const int32_t* tokens,
+                     const float* logprobs, int n, int32_t* top_ids, float* top_logprobs,
+                     smp_stream stream);
+
 /* Greedy path alone (KB note section 02; lecture 9 answer 1): the legal
  * finite token with the largest logit, the smallest id on ties.  Rows with
  * no legal finite logit get SMP_ERR_EMPTY, rows with NaN / +inf in a legal

@@ -19,6 +19,8 @@ Parity status of each function (what pins it is listed in the tests):
                         worked values of the CTRL rule, duplicates and padding
                         in the history, and the encoders against numpy / torch
                         round-to-nearest-even casts over many values.
+  * top_logprobs (numpy, on the oracle's outputs) -- pinned by a worked
+                        example and the normalisation of a whole kept set.
   * orc_gumbel_sample -- pinned by its frequencies against the exact softmax
                         of the kept set (the lecture's Gumbel-max identity),
                         greedy at T = 0, statuses and the uniform's range.
@@ -266,6 +268,27 @@ def gumbel_sample(logits_bits, dtype, V, temperature, seed, offset, kept_mask=No
     (L or lib()).orc_gumbel_sample(_ptr(arr), _DT[dtype], B, V, ld, _ptr(km), _ptr(t), _ptr(s),
                                    _ptr(o), _ptr(tok), _ptr(st), _ptr(mg), int(n_threads))
     return dict(token=tok, status=st, margin=mg)
+
+
+def top_logprobs(x, kept, probs, status, n):
+    """The n most likely tokens of each row's final kept set and their
+    log-probabilities, from the oracle's own outputs: x float [B, V] (the
+    logits as values), kept bool [B, V], probs [B, V] (final probabilities),
+    status [B].  Ranked by logit descending, smallest id first among equal
+    logits; slots past the kept set get id -1 and -inf, error rows -1 and
+    NaN."""
+    B, V = x.shape
+    ids = np.full((B, n), -1, dtype=np.int32)
+    lps = np.full((B, n), -np.inf)
+    for r in range(B):
+        if status[r] != ORC_OK:
+            lps[r] = np.nan
+            continue
+        cand = np.nonzero(kept[r])[0]
+        order = cand[np.lexsort((cand, -x[r, cand].astype(np.float64)))][:n]
+        ids[r, :len(order)] = order
+        lps[r, :len(order)] = np.log(probs[r, order])
+    return ids, lps
 
 
 def bf16_to_f32(bits):

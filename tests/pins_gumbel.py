@@ -66,3 +66,35 @@ def check_gumbel_uniforms(L=None, n=40000):
 
 
 GUMBEL_CHECKS = [check_gumbel_greedy_and_status, check_gumbel_uniforms, check_gumbel_frequencies]
+
+
+def check_top_logprobs(L=None):
+    """Top logprobs of a worked row: p = (0.5, 0.2, 0.2, 0.1) at logits ln p
+    (T = 1, top-k 3, top-p 1): the kept set is the first three, renormalised
+    to (5/9, 2/9, 2/9); ranked by logit with the smaller id first among the
+    tied pair; a fourth slot is empty.  Over a whole kept set the
+    probabilities sum to one."""
+    p = np.array([0.5, 0.2, 0.2, 0.1])
+    x = np.log(p).astype(np.float32)[None]
+    r = oracle.run_batch(x, "f32", 4, temperature=[1.0], top_k=[3], top_p=[1.0],
+                         want_probs=True, L=L)
+    kept = r["probs"] > 0
+    ids, lps = oracle.top_logprobs(x, kept, r["probs"], r["status"], 4)
+    assert list(ids[0]) == [0, 1, 2, -1], ids
+    want = np.log(np.array([5 / 9, 2 / 9, 2 / 9]))
+    assert np.allclose(lps[0, :3], want, rtol=0, atol=1e-6) and lps[0, 3] == -np.inf, lps
+    rng = np.random.Generator(np.random.PCG64(33))
+    xs = (rng.standard_normal((3, 50)) * 2).astype(np.float32)
+    r = oracle.run_batch(xs, "f32", 50, temperature=[0.7] * 3, top_k=[10, 50, 30],
+                         top_p=[0.9, 0.8, 1.0], want_probs=True, L=L)
+    kept = r["probs"] > 0
+    ids, lps = oracle.top_logprobs(xs, kept, r["probs"], r["status"], 32)
+    for b in range(3):
+        m = ids[b] >= 0
+        assert m.sum() == min(32, kept[b].sum())
+        if kept[b].sum() <= 32:
+            assert abs(np.exp(lps[b, m]).sum() - 1.0) < 1e-9
+        assert np.all(np.diff(xs[b, ids[b, m]]) <= 0)
+
+
+GUMBEL_CHECKS.append(check_top_logprobs)

@@ -294,3 +294,50 @@ def test_interleaved_launches_repeat_bit_for_bit():
         for a, b, what in zip(first[i], got, ("tokens", "status", "kept_mask", "kept_count")):
             bad = np.nonzero((a != b).reshape(a.shape[0], -1).any(axis=1))[0]
             assert bad.size == 0, (cases[i]["name"], rep, what, bad[:8])
+
+
+def check_top_logprobs(case, n):
+    """smp_top_logprobs on smp_sample_logprob's outputs: the n best kept
+    tokens by logit (smallest id first among equal logits) equal the
+    oracle's, and their logprobs are within the probabilities' tolerance of
+    the log of the oracle's final probabilities (2e-5: the drawn token's own
+    logprob plus a difference of two fp32 scaled logits)."""
+    r = H.oracle_run(case, want_probs=True)
+    s = H.sampler()
+    d = H.to_dev(case)
+    g = s.sample(d["logits"], d["temperature"], d["top_k"], d["top_p"], d["seed"], d["offset"],
+                 bitmask=d["bitmask"], want_mask=True, want_logprob=True)
+    t = s.top_logprobs(d["logits"], d["temperature"], g["kept_mask"], g["tokens"], g["logprobs"],
+                       n)
+    torch.cuda.synchronize()
+    gi, gl = t["ids"].cpu().numpy(), t["logprobs"].cpu().numpy()
+    st, tok = g["status"].cpu().numpy(), g["tokens"].cpu().numpy()
+    x = workloads.bits_numpy(case["logits"])
+    xv = x if case["dtype"] == "f32" else torch.from_numpy(x.view(np.int16)).view(
+        torch.bfloat16 if case["dtype"] == "bf16" else torch.float16).float().numpy()
+    wi, wl = oracle.top_logprobs(xv, r["probs"] > 0, r["probs"], r["status"], n)
+    ok = (st == 0) & (r["status"] == 0) & (tok == r["token"]) & (r["flags"] == 0)
+    rows = np.nonzero(ok)[0]
+    assert np.array_equal(gi[rows], wi[rows]), rows[(gi[rows] != wi[rows]).any(axis=1)][:5]
+    fin = np.isfinite(wl[rows])
+    err = np.abs(gl[rows][fin].astype(np.float64) - wl[rows][fin])
+    assert err.max(initial=0.0) <= 2e-5, err.max()
+    assert np.all(gl[rows][~fin] == -np.inf)
+    bad = st != 0
+    assert np.all(gi[bad] == -1) and np.all(np.isnan(gl[bad]))
+    return len(rows)
+
+
+@pytest.mark.parametrize("n", [1, 5, 32])
+def test_top_logprobs_bench_workload(n):
+    assert check_top_logprobs(workloads.make("mixed256x128256_bf16"), n) > 200
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_top_logprobs_random_and_ties(dtype):
+    case = workloads.random_case(5150 + len(dtype), 40, 9000, dtype=dtype, mask_frac=0.3,
+                                 neg_inf_frac=0.01)
+    assert check_top_logprobs(case, 20) > 0
+    ties = workloads.random_case(12, 32, 4096, dtype=dtype, grid=6, mask_frac=0.2,
+                                 topks=(3, 40, 700, 4096), topps=(0.5, 0.9, 1.0))
+    assert check_top_logprobs(ties, 32) > 0

@@ -12,3 +12,7 @@ def test_gumbel_greedy_and_status():
 
 def test_gumbel_uniforms():
     pins_gumbel.check_gumbel_uniforms()
+
+
+def test_top_logprobs_worked_example():
+    pins_gumbel.check_top_logprobs()

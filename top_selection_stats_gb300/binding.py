@@ -16,7 +16,7 @@ _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_
 
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
            "smp_sample_noalloc", "smp_sample_logprob", "smp_spec_verify",
-           "smp_repetition_penalty", "smp_gumbel_sample", "smp_set_row_info",
+           "smp_repetition_penalty", "smp_gumbel_sample", "smp_top_logprobs", "smp_set_row_info",
            "smp_plan",
            "smp_status_string")
 
@@ -62,6 +62,7 @@ def load_library(path=None):
     L.smp_repetition_penalty.argtypes = [P, P, I, I, I, ctypes.c_int64, P, I, ctypes.c_int64, P,
                                          P, P]
     L.smp_gumbel_sample.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P, P]
+    L.smp_top_logprobs.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, I, P, P, P]
     L.smp_set_row_info.argtypes = [P, P]
     L.smp_plan.argtypes = [P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
@@ -259,6 +260,23 @@ class Sampler:
                                         _ptr(offset), _ptr(tokens), _ptr(status), self._stream())
         _check(rc, "smp_gumbel_sample")
         return dict(tokens=tokens, status=status)
+
+    def top_logprobs(self, logits, temperature, kept_mask, tokens, logprobs, n, V=None):
+        """The n most likely kept tokens per row and their logprobs, from the
+        outputs of sample(..., want_mask=True, want_logprob=True)."""
+        B, V, ld, _ = self._prep(logits, V, kept_mask, temperature, None, None, None, None)
+        self._check_tensor(tokens, "tokens", torch.int32)
+        self._check_tensor(logprobs, "logprobs", torch.float32)
+        if kept_mask is None:
+            raise ValueError("kept_mask is required")
+        dev = self.device
+        ids = torch.empty((B, n), dtype=torch.int32, device=dev)
+        lps = torch.empty((B, n), dtype=torch.float32, device=dev)
+        rc = self.lib.smp_top_logprobs(self.h, _ptr(logits), _DTYPES[logits.dtype], B, V, ld,
+                                       _ptr(kept_mask), _ptr(temperature), _ptr(tokens),
+                                       _ptr(logprobs), n, _ptr(ids), _ptr(lps), self._stream())
+        _check(rc, "smp_top_logprobs")
+        return dict(ids=ids, logprobs=lps)
 
     def spec_verify(self, target_probs, draft_probs, draft_tokens, seed, offset, V=None,
                     out_tokens=None, n_accepted=None, status=None):

@@ -25,6 +25,9 @@ int verify_enqueue(const float* p, const float* q, const int32_t* d, int B, int 
                    int64_t ld, const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
                    int32_t* n_acc, int32_t* status, cudaStream_t st);
 cudaError_t penalty_setup();
+int toplp_enqueue(const void* logits, int dtype, int B, int V, long long ld, const uint32_t* kept,
+                  const float* temperature, const int32_t* tokens, const float* logprobs, int n,
+                  int32_t* out_ids, float* out_lp, cudaStream_t st);
 int gumbel_enqueue(const void* logits, int dtype, int B, int V, long long ld,
                    const uint32_t* kept, const float* temperature, const uint64_t* seed,
                    const uint64_t* offset, int32_t* tokens, int32_t* status, cudaStream_t st);
@@ -308,6 +311,21 @@ int smp_gumbel_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, 
   DeviceGuard guard(h->device);
   return gumbel_enqueue(logits, (int)dtype, B, V, ld, kept_mask, temperature, seed, offset, tokens,
                         row_status, (cudaStream_t)stream);
+}
+
+int smp_top_logprobs(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, int64_t ld,
+                     const uint32_t* kept_mask, const float* temperature, const int32_t* tokens,
+                     const float* logprobs, int n, int32_t* top_ids, float* top_logprobs,
+                     smp_stream stream) {
+  if (!h || !logits || !kept_mask || !temperature || !tokens || !logprobs || !top_ids ||
+      !top_logprobs)
+    return SMP_ERR_INVALID_PARAM;
+  if ((int)dtype < 0 || (int)dtype > 2) return SMP_ERR_INVALID_PARAM;
+  if (B < 0 || V < 1 || ld < V || n < 1) return SMP_ERR_INVALID_PARAM;
+  if (B > h->max_batch || V > h->max_vocab) return SMP_ERR_CAPACITY;
+  DeviceGuard guard(h->device);
+  return toplp_enqueue(logits, (int)dtype, B, V, ld, kept_mask, temperature, tokens, logprobs, n,
+                       top_ids, top_logprobs, (cudaStream_t)stream);
 }
 
 const char* smp_status_string(int code) {
