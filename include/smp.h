@@ -21,6 +21,14 @@
  * An empty candidate set is an error; no substitute token is ever produced
  * (KB note section 03, section 07).
  *
+ * Entry points: smp_topk_topp_mask (kept sets), smp_sample (draws),
+ * smp_sample_logprob and smp_top_logprobs (draws with their log-
+ * probabilities), smp_argmax (greedy), smp_sample_noalloc (no handle, no
+ * allocation), smp_repetition_penalty (an in-place logits processor to run
+ * before sampling), smp_gumbel_sample (a sort-free Gumbel-max draw over a
+ * kept set, for comparison) and smp_spec_verify (speculative-decoding
+ * verification against the kept sets' probabilities).
+ *
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees, copies to the host or synchronises inside a
