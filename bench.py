@@ -428,7 +428,7 @@ def run_ours(args, rank, world, local):
     total = args.warmup + args.steps
     offsets = [(case["offset"] + s * B).to(dev) for s in range(total)]
     smp = Sampler(local, max_batch=max(B, 64), max_vocab=max(V, 1024))
-    plan = smp.plan(case["logits"].dtype, V)
+    plan = smp.plan(case["logits"].dtype, V, B=B)
     W = (V + 31) // 32
     tokens = torch.empty(B, dtype=torch.int32, device=dev)
     status = torch.empty(B, dtype=torch.int32, device=dev)

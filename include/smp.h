@@ -301,11 +301,13 @@ int smp_gumbel_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, 
  * off.  Not thread-safe against concurrent calls on the same handle. */
 int smp_set_row_info(smp_handle h, int32_t* row_info);
 
-/* Launch plan for (dtype, V): cluster size, slice length (elements per CTA),
- * dynamic shared memory per CTA (bytes) and candidate capacity.  Any output
- * pointer may be NULL.  Returns SMP_ERR_CAPACITY when V cannot be held. */
-int smp_plan(smp_handle h, smp_dtype dtype, int V, int* cluster, int* slice, int* smem_bytes,
-             int* capacity);
+/* Launch plan of a call with B rows of V tokens of `dtype` on this handle's
+ * device: CTAs per row (the thread-block cluster), slice length (tokens per
+ * CTA), dynamic shared memory per CTA (bytes) and candidate-list capacity per
+ * CTA.  Any output pointer may be NULL.  Returns SMP_ERR_CAPACITY when V
+ * cannot be held. */
+int smp_plan(smp_handle h, smp_dtype dtype, int B, int V, int* cluster, int* slice,
+             int* smem_bytes, int* capacity);
 
 /* Static description of a status code. */
 const char* smp_status_string(int code);

@@ -64,7 +64,7 @@ def load_library(path=None):
     L.smp_gumbel_sample.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P, P]
     L.smp_top_logprobs.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, I, P, P, P]
     L.smp_set_row_info.argtypes = [P, P]
-    L.smp_plan.argtypes = [P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
+    L.smp_plan.argtypes = [P, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
     L.smp_status_string.restype = ctypes.c_char_p
     L.smp_status_string.argtypes = [I]
@@ -159,9 +159,9 @@ class Sampler:
     def row_info(self, B):
         return None if self._row_info is None else self._row_info[:B]
 
-    def plan(self, dtype, V):
+    def plan(self, dtype, V, B=1):
         out = [ctypes.c_int() for _ in range(4)]
-        rc = self.lib.smp_plan(self.h, _DTYPES[dtype], V, *[ctypes.byref(o) for o in out])
+        rc = self.lib.smp_plan(self.h, _DTYPES[dtype], B, V, *[ctypes.byref(o) for o in out])
         _check(rc, "smp_plan")
         return dict(cluster=out[0].value, slice=out[1].value, smem=out[2].value,
                     capacity=out[3].value)

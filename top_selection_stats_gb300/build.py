@@ -15,11 +15,12 @@ LIB = os.path.join(HERE, "libsmp.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = [os.path.join(CSRC, f) for f in ("smp_api.cu", "smp_k_f32.cu", "smp_k_bf16.cu",
                                            "smp_k_f16.cu", "smp_verify.cu", "smp_penalty.cu",
-                                           "smp_gumbel.cu", "smp_toplp.cu")]
+                                           "smp_gumbel.cu", "smp_toplp.cu", "smp_x_bf16.cu",
+                                           "smp_x_f16.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("smp_philox.cuh", "smp_device.cuh", "smp_core.cuh",
                                            "smp_list.cuh",
                                            "smp_stream_passes.cuh", "smp_general.cuh",
-                                           "smp_kernel.cuh")]
+                                           "smp_kernel.cuh", "smp_split.cuh")]
 DEPS = SOURCES + HEADERS + [os.path.join(ROOT, "include", "smp.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -13,6 +13,7 @@
 
 #include "../../include/smp.h"
 #include "smp_core.cuh"
+#include "smp_split.cuh"
 
 namespace smp {
 const void* kernel_f32();
@@ -21,6 +22,10 @@ const void* kernel_f16();
 cudaError_t launch_f32(const KArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_bf16(const KArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_f16(const KArgs& a, int grid, cudaStream_t st);
+const void* split_kernel_bf16();
+const void* split_kernel_f16();
+cudaError_t split_launch_bf16(const XArgs& a, int smem, cudaStream_t st);
+cudaError_t split_launch_f16(const XArgs& a, int smem, cudaStream_t st);
 int verify_enqueue(const float* p, const float* q, const int32_t* d, int B, int G, int V,
                    int64_t ld, const uint64_t* seed, const uint64_t* offset, int32_t* out_tokens,
                    int32_t* n_acc, int32_t* status, cudaStream_t st);
@@ -75,6 +80,43 @@ const void* kernel_for(int dt) {
 }
 
 int chunk_elems(int dt) { return STAGE_BYTES / esize_of(dt); }
+
+// Split-row launch plan (bf16 / fp16): the smallest power-of-two cluster
+// (at most XMAXC CTAs) that gives the launch at least two CTAs per SM, so that
+// every row streams at once; slices of at most XMAXST stages, each a multiple
+// of 256 values; no CTA without values.  Rows too long for XMAXC slices take
+// the streaming kernel instead (returns false).
+struct XPlan {
+  int C, SL, wf, cap, smem;
+};
+constexpr int XSMEM_MAX = (XNS * XSB + 4096 * 2 + 8192 * 2 + 8192 * 4) + (int)sizeof(XSh);
+// The split-row kernel is built and passes the parity tests, but it is not
+// yet faster than the streaming kernel on flat top-p rows; it stays off
+// until it is.
+constexpr bool SPLIT_ENABLED = false;
+bool split_plan(int dt, int B, int V, int sms, XPlan* out) {
+  if (!SPLIT_ENABLED || (dt != DT_BF16 && dt != DT_F16)) return false;
+  const long long smax = (long long)XMAXST * XVS * 8;  // values per slice, at most
+  int C = 1;
+  while (C < XMAXC && ((long long)B * C < 2LL * sms || (V + C - 1) / C > smax)) C *= 2;
+  while (C > 1 && (long long)(C - 1) * 256 >= V) C /= 2;  // every CTA holds values
+  const int SL = ((V + C - 1) / C + 255) / 256 * 256;
+  if (SL > smax) return false;
+  out->C = C;
+  out->SL = SL;
+  out->wf = dt == DT_F16 ? 4096 : 2048;
+  out->cap = C >= 2 ? 2048 : 8192;
+  out->smem = xoff_sh(out->wf, out->cap) + (int)sizeof(XSh);
+  return true;
+}
+cudaError_t split_setup() {
+  for (const void* k : {split_kernel_bf16(), split_kernel_f16()}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, XSMEM_MAX);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+constexpr long long WAIT_LIMIT = 4000000000ll;  // about two seconds of SM clock
 
 struct DeviceGuard {
   int prev = -1;
@@ -134,7 +176,41 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   a.mode = mode;
   const size_t es = (size_t)esize_of(dt);
   a.use_tma = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
-  std::memcpy(a.delta, h->delta, sizeof(a.delta));
+
+  XPlan xp;
+  if (split_plan(dt, B, V, h->sm_count, &xp)) {
+    XArgs r;
+    std::memset(&r, 0, sizeof(r));
+    r.logits = logits;
+    r.ld = ld;
+    r.B = B;
+    r.V = V;
+    r.W = a.W;
+    r.bitmask = bitmask;
+    r.temperature = a.temperature;
+    r.top_k = a.top_k;
+    r.top_p = a.top_p;
+    r.seed = a.seed;
+    r.offset = a.offset;
+    r.tokens = tokens;
+    r.status = status;
+    r.kept_mask = kept_mask;
+    r.kept_count = kept_count;
+    r.probs = probs;
+    r.logprob = logprob;
+    r.row_info = h->row_info;
+    r.mode = mode;
+    r.C = xp.C;
+    r.SL = xp.SL;
+    r.wf = xp.wf;
+    r.cap = xp.cap;
+    r.aligned = a.use_tma;
+    r.wait_limit = WAIT_LIMIT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = dt == DT_BF16 ? split_launch_bf16(r, xp.smem, st)
+                                        : split_launch_f16(r, xp.smem, st);
+    return e == cudaSuccess ? SMP_OK : SMP_ERR_CUDA;
+  }
 
   // one CTA per row, at most two resident per SM; CTAs loop over rows.  With
   // a job board the whole resident grid is launched: CTAs without a row take
@@ -191,7 +267,7 @@ int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
     }
     per_sm = nb < per_sm ? nb : per_sm;
   }
-  if (per_sm < 1 || penalty_setup() != cudaSuccess) {
+  if (per_sm < 1 || penalty_setup() != cudaSuccess || split_setup() != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return SMP_ERR_CUDA;
@@ -256,10 +332,18 @@ int smp_set_row_info(smp_handle h, int32_t* row_info) {
   return SMP_OK;
 }
 
-int smp_plan(smp_handle h, smp_dtype dtype, int V, int* cluster, int* slice, int* smem_bytes,
-             int* capacity) {
-  if (!h || V < 1) return SMP_ERR_INVALID_PARAM;
+int smp_plan(smp_handle h, smp_dtype dtype, int B, int V, int* cluster, int* slice,
+             int* smem_bytes, int* capacity) {
+  if (!h || V < 1 || B < 1) return SMP_ERR_INVALID_PARAM;
   if ((int)dtype < 0 || (int)dtype > 2) return SMP_ERR_INVALID_PARAM;
+  XPlan xp;
+  if (split_plan((int)dtype, B, V, h->sm_count, &xp)) {
+    if (cluster) *cluster = xp.C;
+    if (slice) *slice = xp.SL;
+    if (smem_bytes) *smem_bytes = xp.smem;
+    if (capacity) *capacity = xp.cap;
+    return SMP_OK;
+  }
   const int ce = chunk_elems((int)dtype);
   if (cluster) *cluster = 1;
   if (slice) *slice = ce;
@@ -394,6 +478,10 @@ int noalloc_setup(int dev, cudaStream_t st, smp_ctx** out) {
       per_sm = nb < per_sm ? nb : per_sm;
     }
     if (per_sm < 1) return SMP_ERR_CUDA;
+    if (split_setup() != cudaSuccess) {
+      cudaGetLastError();
+      return SMP_ERR_CUDA;
+    }
     Board* board = nullptr;
     if (cudaGetSymbolAddress((void**)&board, smp_noalloc_scratch) != cudaSuccess ||
         cudaMemsetAsync(board, 0, NOALLOC_SCRATCH_BYTES, st) != cudaSuccess) {
