@@ -428,6 +428,7 @@ def run_ours(args, rank, world, local):
     total = args.warmup + args.steps
     offsets = [(case["offset"] + s * B).to(dev) for s in range(total)]
     smp = Sampler(local, max_batch=max(B, 64), max_vocab=max(V, 1024))
+    smp.set_kernel(args.kernel)
     plan = smp.plan(case["logits"].dtype, V, B=B)
     W = (V + 31) // 32
     tokens = torch.empty(B, dtype=torch.int32, device=dev)
@@ -696,9 +697,11 @@ def run_ours(args, rank, world, local):
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": case["dtype"], "data": "synthetic",
+            "arith": "f32 weights, 64-bit fixed-point masses",
             "config": {"workload": args.workload, "B": B, "V": V, "logits": case["dtype"],
+                       "kernel": args.kernel,
                        "kept_mask": True,
                        "l2": f"inputs rotated over {nbuf} copies ({nbuf * bytes_logits / 1e6:.0f} MB > L2)",
                        "cluster": plan["cluster"], "slice": plan["slice"],
@@ -729,6 +732,8 @@ def main():
                     help="also time smp_top_logprobs (N best kept tokens; implies --logprob)")
     ap.add_argument("--gumbel", action="store_true",
                     help="also time the Gumbel-max sampler (kept mask + smp_gumbel_sample)")
+    ap.add_argument("--kernel", default="board", choices=["board", "split"],
+                    help="sampler kernel (smp_set_kernel): job board, or split rows over clusters")
     ap.add_argument("--logprob", action="store_true",
                     help="also return each drawn token's log-probability (smp_sample_logprob)")
     args = ap.parse_args()

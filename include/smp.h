@@ -27,7 +27,8 @@
  * allocation), smp_repetition_penalty (an in-place logits processor to run
  * before sampling), smp_gumbel_sample (a sort-free Gumbel-max draw over a
  * kept set, for comparison) and smp_spec_verify (speculative-decoding
- * verification against the kept sets' probabilities).
+ * verification against the kept sets' probabilities); smp_set_kernel
+ * chooses between the two sampler kernels.
  *
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers owned by the caller; the library
@@ -182,7 +183,8 @@ int smp_argmax(smp_handle h, const void* logits, smp_dtype dtype, int B, int V, 
  * Set-up: the first call on each device does the set-up, with that device
  * current.  It configures the kernels, looks up the array's device address
  * and clears the array on `stream`.  Make that first call before any stream
- * capture.
+ * capture.  Every call looks the address up again (a host-side query); when
+ * it has changed, as after cudaDeviceReset, the set-up runs again.
  * Limit: V may be at most 128 staging chunks, that is 786,432 tokens for fp32
  * and 1,572,864 for bf16/fp16.  Larger V returns SMP_ERR_CAPACITY and
  * launches nothing.  B has no limit of its own.
@@ -300,6 +302,19 @@ int smp_gumbel_sample(smp_handle h, const void* logits, smp_dtype dtype, int B, 
  * legal kept, 3 sigma-truncation hit, 4 full-row refinement.  NULL turns it
  * off.  Not thread-safe against concurrent calls on the same handle. */
 int smp_set_row_info(smp_handle h, int32_t* row_info);
+
+/* Which sampler kernel later calls on this handle launch (the results are the
+ * same; only the time differs).  SMP_KERNEL_BOARD (the default): one CTA per
+ * row, two resident per SM, with a device job board through which CTAs that
+ * are done take chunks of the slow rows.  SMP_KERNEL_SPLIT (bf16 / fp16
+ * logits only; other dtypes keep the board kernel): each row split over a
+ * thread-block cluster of up to 8 CTAs that stream their slices once through
+ * a shared-memory ring and combine over distributed shared memory; fastest
+ * when top-k bounds every row, slower on rows whose top-p set runs to tens of
+ * thousands of tokens.  Returns SMP_ERR_INVALID_PARAM for another value.  Not
+ * thread-safe against concurrent calls on the same handle. */
+enum { SMP_KERNEL_BOARD = 0, SMP_KERNEL_SPLIT = 1 };
+int smp_set_kernel(smp_handle h, int kernel);
 
 /* Launch plan of a call with B rows of V tokens of `dtype` on this handle's
  * device: CTAs per row (the thread-block cluster), slice length (tokens per

@@ -10,6 +10,15 @@ import gpu_helpers as H
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["board", "split"])
+def kernel(request):
+    """Every parity case runs on both sampler kernels (smp_set_kernel)."""
+    s = H.sampler()
+    s.set_kernel(request.param)
+    yield request.param
+    s.set_kernel("board")
+
+
 def run_and_compare(case, modes=("sample", "mask"), check_probs=True, rows=None):
     r = H.oracle_run(case, want_probs=True, rows=rows)
     out = {}
@@ -39,7 +48,7 @@ def test_ties_on_integer_grid(dtype):
     run_and_compare(case)
 
 
-def test_full_row_fallback_paths():
+def test_full_row_fallback_paths(kernel):
     """Large k beyond the candidate buffer and flat rows under top-p force the
     exact refinement path; it must agree with the oracle too."""
     case = workloads.random_case(5, 32, 60000, dtype="bf16", sigma=0.5, n_head=(0, 4),

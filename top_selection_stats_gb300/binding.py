@@ -10,6 +10,7 @@ lib_path = os.path.join(HERE, "libsmp.so")
 SMP_OK, SMP_ERR_EMPTY, SMP_ERR_NONFINITE, SMP_ERR_INVALID_PARAM = 0, 1, 2, 3
 SMP_ERR_TIMEOUT, SMP_ERR_CUDA, SMP_ERR_CAPACITY = 4, 5, 6
 SMP_F32, SMP_BF16, SMP_F16 = 0, 1, 2
+SMP_KERNEL_BOARD, SMP_KERNEL_SPLIT = 0, 1
 PATH_NAMES = {0: "error", 1: "greedy", 2: "all", 3: "sigma", 4: "full"}
 
 _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_F16}
@@ -17,7 +18,7 @@ _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
            "smp_sample_noalloc", "smp_sample_logprob", "smp_spec_verify",
            "smp_repetition_penalty", "smp_gumbel_sample", "smp_top_logprobs", "smp_set_row_info",
-           "smp_plan",
+           "smp_set_kernel", "smp_plan",
            "smp_status_string")
 
 
@@ -64,6 +65,7 @@ def load_library(path=None):
     L.smp_gumbel_sample.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, P, P, P]
     L.smp_top_logprobs.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, I, P, P, P]
     L.smp_set_row_info.argtypes = [P, P]
+    L.smp_set_kernel.argtypes = [P, ctypes.c_int]
     L.smp_plan.argtypes = [P, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
     L.smp_status_string.restype = ctypes.c_char_p
@@ -158,6 +160,11 @@ class Sampler:
 
     def row_info(self, B):
         return None if self._row_info is None else self._row_info[:B]
+
+    def set_kernel(self, kernel):
+        """smp_set_kernel: "board" (default) or "split" (bf16 / fp16 logits)."""
+        code = {"board": SMP_KERNEL_BOARD, "split": SMP_KERNEL_SPLIT}[kernel]
+        _check(self.lib.smp_set_kernel(self.h, code), "smp_set_kernel")
 
     def plan(self, dtype, V, B=1):
         out = [ctypes.c_int() for _ in range(4)]

@@ -52,6 +52,7 @@ struct smp_ctx {
   int grid_max;
   float delta[DTAB];
   int32_t* row_info;
+  int kernel;    // SMP_KERNEL_BOARD or SMP_KERNEL_SPLIT
   Board* board;  // job board: zeroed at creation, reset by each launch's last CTA
 };
 
@@ -90,12 +91,8 @@ struct XPlan {
   int C, SL, wf, cap, smem;
 };
 constexpr int XSMEM_MAX = (XNS * XSB + 4096 * 2 + 8192 * 2 + 8192 * 4) + (int)sizeof(XSh);
-// The split-row kernel is built and passes the parity tests, but it is not
-// yet faster than the streaming kernel on flat top-p rows; it stays off
-// until it is.
-constexpr bool SPLIT_ENABLED = false;
 bool split_plan(int dt, int B, int V, int sms, XPlan* out) {
-  if (!SPLIT_ENABLED || (dt != DT_BF16 && dt != DT_F16)) return false;
+  if (dt != DT_BF16 && dt != DT_F16) return false;
   const long long smax = (long long)XMAXST * XVS * 8;  // values per slice, at most
   int C = 1;
   while (C < XMAXC && ((long long)B * C < 2LL * sms || (V + C - 1) / C > smax)) C *= 2;
@@ -176,9 +173,10 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   a.mode = mode;
   const size_t es = (size_t)esize_of(dt);
   a.use_tma = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
+  std::memcpy(a.delta, h->delta, sizeof(a.delta));
 
   XPlan xp;
-  if (split_plan(dt, B, V, h->sm_count, &xp)) {
+  if (h->kernel == SMP_KERNEL_SPLIT && split_plan(dt, B, V, h->sm_count, &xp)) {
     XArgs r;
     std::memset(&r, 0, sizeof(r));
     r.logits = logits;
@@ -250,6 +248,7 @@ int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
   h->smem_optin = (int)prop.sharedMemPerBlockOptin;
   h->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
   h->row_info = nullptr;
+  h->kernel = SMP_KERNEL_BOARD;
   for (int i = 0; i < DTAB; ++i) {
     const double l2q = -24.0 + 0.25 * i;
     h->delta[i] = (float)upper_quantile(std::pow(2.0, l2q));
@@ -332,12 +331,18 @@ int smp_set_row_info(smp_handle h, int32_t* row_info) {
   return SMP_OK;
 }
 
+int smp_set_kernel(smp_handle h, int kernel) {
+  if (!h || (kernel != SMP_KERNEL_BOARD && kernel != SMP_KERNEL_SPLIT)) return SMP_ERR_INVALID_PARAM;
+  h->kernel = kernel;
+  return SMP_OK;
+}
+
 int smp_plan(smp_handle h, smp_dtype dtype, int B, int V, int* cluster, int* slice,
              int* smem_bytes, int* capacity) {
   if (!h || V < 1 || B < 1) return SMP_ERR_INVALID_PARAM;
   if ((int)dtype < 0 || (int)dtype > 2) return SMP_ERR_INVALID_PARAM;
   XPlan xp;
-  if (split_plan((int)dtype, B, V, h->sm_count, &xp)) {
+  if (h->kernel == SMP_KERNEL_SPLIT && split_plan((int)dtype, B, V, h->sm_count, &xp)) {
     if (cluster) *cluster = xp.C;
     if (slice) *slice = xp.SL;
     if (smem_bytes) *smem_bytes = xp.smem;
@@ -451,14 +456,24 @@ std::mutex noalloc_mutex;
 smp_ctx noalloc_dev[NOALLOC_MAX_DEVICES];
 bool noalloc_ready[NOALLOC_MAX_DEVICES];
 
-// Once per device, with that device current: the kernels' shared-memory
-// attribute and the resident grid (as smp_create computes them), the sigma
-// table, the scratch's device address, and a clear of the scratch on the
-// caller's stream.  The board must start at zero; every launch's last CTA
-// leaves it at zero again, so later calls need no clear of their own.
+// Once per device context, with that device current: the kernels' shared-
+// memory attribute and the resident grid (as smp_create computes them), the
+// sigma table, the scratch's device address, and a clear of the scratch on
+// the caller's stream.  The board must start at zero; every launch's last CTA
+// leaves it at zero again, so later calls need no clear of their own.  Each
+// call asks for the scratch's address again: after a device reset (a new
+// primary context) the array moves, and the set-up is redone.
 int noalloc_setup(int dev, cudaStream_t st, smp_ctx** out) {
   std::lock_guard<std::mutex> lock(noalloc_mutex);
   smp_ctx& c = noalloc_dev[dev];
+  if (noalloc_ready[dev]) {
+    void* now = nullptr;
+    if (cudaGetSymbolAddress(&now, smp_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return SMP_ERR_CUDA;
+    }
+    if (now != (void*)c.board) noalloc_ready[dev] = false;
+  }
   if (!noalloc_ready[dev]) {
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
@@ -497,6 +512,7 @@ int noalloc_setup(int dev, cudaStream_t st, smp_ctx** out) {
     c.grid_max = per_sm * c.sm_count;
     for (int i = 0; i < DTAB; ++i) c.delta[i] = (float)upper_quantile(std::pow(2.0, -24.0 + 0.25 * i));
     c.row_info = nullptr;
+    c.kernel = SMP_KERNEL_BOARD;
     c.board = board;
     noalloc_ready[dev] = true;
   }

@@ -55,7 +55,9 @@ constexpr int XMAXST = 64;          // stages per slice, at most (512 KB)
 constexpr int XMAXC = 8;            // CTAs per row, at most (portable cluster size)
 constexpr int XSW = 128;            // sampled bins each CTA publishes
 constexpr int XMAXWIN = 36;         // windows of one row, at most
-constexpr int XFLATK = 1536;        // flat top-p rows: kept sets the candidate list aims at
+constexpr int XWT = XNS * XSB / 16;  // keys whose weight the resolution stores (2048)
+constexpr int XBL = 1024;     // copies of the boundary value pass C lists for the id cut
+constexpr uint32_t XFM = 8;  // flat rows: the counted window reaches cap / XFM keys above the sample
 
 enum XClass { XC_ERROR = 0, XC_GREEDY = 1, XC_ALL = 2, XC_TOPK = 3, XC_FLAT = 4, XC_FLATL = 5 };
 
@@ -101,8 +103,11 @@ struct XPub {
   int flags;      // 1 NaN/+inf legal, 2 wait expired, 4 list overflow, 8 above window,
                   // 16 keep-all reference too low
   int ncand;      // candidates listed
+  uint32_t lo, hw;  // this CTA's candidate window: keys [lo, hw]
+  uint32_t skey;  // largest key of this CTA's first stage (the local sample)
+  float xsv;      // the reference of this CTA's masses: that key's value (0 if none)
   int pad[1];
-  double mass;    // keep-all rows: the slice's mass relative to the sample's maximum
+  double mass;    // flat / keep-all rows: legal mass relative to the local sample's maximum    // keep-all rows: the slice's mass relative to the sample's maximum
   uint16_t samp[XSW];  // B1 only: counts of stage 0's values in bins (kmax >> SB) - j
 };
 static_assert(sizeof(XPub) % 16 == 0, "published record: whole 16-byte units");
@@ -116,7 +121,6 @@ struct XWin {
 struct XSh {
   uint64_t bar[XNS];
   XPub stage;
-  XPub pub[XMAXC];
   XPub pub2[XMAXC];
   uint64_t km[XMAXC];
   uint64_t uf[XMAXC];
@@ -126,7 +130,7 @@ struct XSh {
   uint64_t q[XNW];
   float f[XNW];
   int wi[XNW];
-  int bi[24];
+  int bi[24];                // [23]: pass C's expired waits (set remotely)
   uint64_t bq[8];
   double bd[8];
   int ncand;
@@ -193,6 +197,17 @@ template <int DT>
 __device__ __forceinline__ uint32_t xeq2(uint32_t a, uint32_t b) {
   typedef typename XT<DT>::T2 T2;
   return __heq2_mask(*reinterpret_cast<const T2*>(&a), *reinterpret_cast<const T2*>(&b));
+}
+template <int DT>
+__device__ __forceinline__ uint32_t xgt2(uint32_t a, uint32_t b) {
+  typedef typename XT<DT>::T2 T2;
+  return __hgt2_mask(*reinterpret_cast<const T2*>(&a), *reinterpret_cast<const T2*>(&b));
+}
+// One bit per element (element e -> bit e) from four packed compare masks.
+__device__ __forceinline__ uint32_t xbits8(uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3) {
+  const uint32_t p0 = __byte_perm(m0, m1, 0x6420) & 0x08040201u;
+  const uint32_t p1 = __byte_perm(m2, m3, 0x6420) & 0x08040201u;
+  return ((p0 * 0x01010101u) >> 24) | (((p1 * 0x01010101u) >> 24) << 4);
 }
 template <int DT>
 __device__ __forceinline__ uint32_t xvmax(uint4 q) {
@@ -556,7 +571,8 @@ struct XCtx {
   float xs, c2;  // flat rows: the sample's maximum and log2(e) / T
   float zb, xcf;  // keep-all rows: zref log2(e); the exact-weight floor
   uint32_t xc2;   // the floor packed twice in the element type
-  uint32_t* flagw;  // top-k / flat rows: bitmap of vectors holding candidates
+  uint32_t* flagw;  // top-k rows: bitmap of vectors holding candidates
+  uint32_t* hcnt;   // flat rows: one 32-bit counter per key of [lo, hw] (bin hw - k)
 };
 enum { XS_STATS = 0, XS_TOPK = 1, XS_ALL = 2, XS_FLAT = 3 };
 
@@ -575,16 +591,15 @@ __device__ __forceinline__ void xstream(const XCtx cx, XStat& st, int& timed_out
   XSh* const __restrict__ Sp = cx.S;
   const uint16_t* const __restrict__ gsrc = cx.gsrc;
   const uint32_t* const __restrict__ mrow = cx.mrow;
-  uint16_t* const __restrict__ ckey = cx.ckey;
-  int* const __restrict__ cid = cx.cid;
   const float* const __restrict__ tz = cx.tz;
   uint32_t* const __restrict__ mout = cx.mout;
   const long long wait_limit = cx.wait_limit;
-  const int nst = cx.nst, nvec = cx.nvec, nfull = cx.nfull, n = cx.n, s0 = cx.s0, cap = cx.cap;
+  const int nst = cx.nst, nvec = cx.nvec, nfull = cx.nfull, n = cx.n, s0 = cx.s0;
   const uint32_t lo = cx.lo, lo2 = cx.lo2, xc2 = cx.xc2;
   const float T = cx.T, zref = cx.zref, xs = cx.xs, c2 = cx.c2, zb = cx.zb, xcf = cx.xcf;
   uint32_t* const __restrict__ flagw = cx.flagw;
-  constexpr float L2E = 1.4426950408889634f;
+  uint32_t* const __restrict__ hcnt = cx.hcnt;
+  const uint32_t hw = cx.hw;
   constexpr uint32_t NN = R::NINF | (R::NINF << 16);
   for (int s = 0; s < nst; ++s) {
     const int slot = s % XNS;
@@ -603,13 +618,30 @@ __device__ __forceinline__ void xstream(const XCtx cx, XStat& st, int& timed_out
                                     : xfetch<DT>(ring, slot, v, nfull, n, gsrc, mrow);
         vm = (s > 0) ? xstats<DT>(st, q, s0 + v * 8) : xvmax<DT>(q);
       }
-      if (MODE == XS_TOPK || MODE == XS_FLAT) {
+      if (MODE == XS_TOPK) {
         // a vector holding a value >= lo is marked; its candidates are
         // listed after the stream (re-read from L2)
         if (in && xge2<DT>(vm, lo2) != 0u) xred_or_shared(&flagw[v >> 5], 1u << (v & 31));
-        if (MODE == XS_FLAT && in) {
+      } else if (MODE == XS_FLAT) {
+        if (in) {
+          float f0 = 0.f, f1 = 0.f;  // -inf weighs 0
 #pragma unroll
-          for (int e = 0; e < 8; ++e) fm += ex2f((R::f(xhalf(q, e)) - xs) * c2);  // -inf: 0
+          for (int e = 0; e < 8; e += 2) {
+            f0 += ex2f((R::f(xhalf(q, e)) - xs) * c2);
+            f1 += ex2f((R::f(xhalf(q, e + 1)) - xs) * c2);
+          }
+          fm += f0 + f1;
+          // every key of the window counted (values above it: flag 8)
+          if (xge2<DT>(vm, lo2) != 0u) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t k = xkey(xhalf(q, e));
+              if (k >= lo) {
+                if (k <= hw) atomicAdd(&hcnt[hw - k], 1u);
+                else xflags |= 8;
+              }
+            }
+          }
         }
       } else if (MODE == XS_ALL) {
         uint32_t byte = 0;
@@ -628,12 +660,16 @@ __device__ __forceinline__ void xstream(const XCtx cx, XStat& st, int& timed_out
           }
           am += a0 + a1;
           if (xge2<DT>(vm, xc2) != 0u) {  // values near the top: exact z
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const uint32_t h = xhalf(q, e);
-              const float x = R::f(h);
-              if (x >= xcf)
-                am += ex2f((xz<DT>(h, tz, T) - zref) * 1.4426950408889634f) - ex2f(fmaf(x, c2, -zb));
+            // one pass per such value (few per lane), in element order
+            uint32_t cm = xbits8(xge2<DT>(q.x, xc2), xge2<DT>(q.y, xc2), xge2<DT>(q.z, xc2),
+                                 xge2<DT>(q.w, xc2));
+#pragma unroll 1
+            for (; cm; cm &= cm - 1u) {
+              const int e = __ffs(cm) - 1;
+              const uint32_t w = e < 4 ? (e < 2 ? q.x : q.y) : (e < 6 ? q.z : q.w);
+              const uint32_t h = (e & 1) ? (w >> 16) : (w & 0xffffu);
+              am += ex2f((xz<DT>(h, tz, T) - zref) * 1.4426950408889634f) -
+                    ex2f(fmaf(R::f(h), c2, -zb));
             }
           }
         }
@@ -650,6 +686,7 @@ __device__ __forceinline__ void xstream(const XCtx cx, XStat& st, int& timed_out
     if (tid == 0 && !timed_out && s + XNS < nst) {
       const int v0 = (s + XNS) * XVS, v1 = min(nfull, v0 + XVS);
       const uint32_t bytes = v1 > v0 ? (uint32_t)(v1 - v0) * 16u : 0u;
+      if (s == 0) fence_proxy_async_smem();  // slot 0 may hold the masked copy
       mbar_arrive_expect_tx(&Sp->bar[slot], bytes);
       if (bytes) bulk_g2s(ring + slot * XSB, gsrc + (size_t)v0 * 8, bytes, &Sp->bar[slot]);
       ++issued;
@@ -696,6 +733,52 @@ __device__ __forceinline__ uint64_t xmy_mass32(const uint32_t* hist, uint32_t hi
   }
   return xblock_total<uint64_t>(mine, sc);
 }
+// Count of bin b: 16-bit pairs, or one 32-bit counter per bin.
+__device__ __forceinline__ uint32_t xcnt(const uint32_t* h, uint32_t b, bool wide) {
+  return wide ? h[b] : (h[b >> 1] >> ((b & 1u) << 4)) & 0xffffu;
+}
+// Weight of key index i (key gk - i): stored for the first XWT keys.
+template <int DT>
+__device__ __forceinline__ uint64_t xw_at(const uint64_t* wtab, int i, uint32_t gk, float T,
+                                          float zmax) {
+  return i < XWT ? wtab[i] : xwfx(XT<DT>::f(xraw(gk - (uint32_t)i)), T, zmax);
+}
+// The want-th smallest (0-based) of ids[0..nid), ids < 2^18 and distinct:
+// radix selection in three rounds of 6-bit digits (block-wide).
+__device__ __forceinline__ int xsel_id(const int* ids, int nid, int want, XSh& S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0u;
+  for (int round = 0; round < 3; ++round) {
+    const int sh = 12 - 6 * round;
+    if (tid < 64) S.h64[tid] = 0u;
+    __syncthreads();
+    for (int i = tid; i < nid; i += XNT) {
+      const uint32_t id = (uint32_t)ids[i];
+      if ((id >> (sh + 6)) == (prefix >> (sh + 6))) atomicAdd(&S.h64[(id >> sh) & 63u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t c0 = S.h64[2 * lane], c1 = S.h64[2 * lane + 1];
+      const uint32_t sum = c0 + c1;
+      const uint32_t inc = xwarp_incl<uint32_t>(sum);
+      const uint32_t hit = __ballot_sync(0xffffffffu, inc > (uint32_t)want);
+      const int L = hit ? __ffs(hit) - 1 : 31;
+      const uint32_t bef = __shfl_sync(0xffffffffu, inc - sum, L);
+      const uint32_t cc0 = __shfl_sync(0xffffffffu, c0, L);
+      if (lane == 0) {
+        const int d = (bef + cc0 > (uint32_t)want) ? 2 * L : 2 * L + 1;
+        S.bi[7] = d;
+        S.bi[8] = want - (int)(bef + ((d & 1) ? cc0 : 0u));
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)S.bi[7] << sh;
+    want = S.bi[8];
+    __syncthreads();
+  }
+  return (int)prefix;
+}
+
 // Kept: above the boundary value, or a copy of it with a local id before the cut.
 __device__ __forceinline__ bool xkept(float bval, int cut, float x, int id) {
   return x > bval || (x == bval && id < cut);
@@ -763,7 +846,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
   else if (a.mode == MODE_ARGMAX || T == 0.f || kk == 1) pcls = XC_GREEDY;
   else if (kk >= a.V) pcls = (pp >= 1.f) ? XC_ALL : XC_FLAT;
   else pcls = XC_TOPK;
-  const bool want_samp = pcls == XC_TOPK || pcls == XC_FLAT;
+  const bool want_samp = pcls == XC_TOPK;
 
   for (int i = tid; i < (wf >> 1); i += XNT) hist[i] = 0u;
   if (tid == 0) {
@@ -790,81 +873,53 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     if (v < nfull && mrow) reinterpret_cast<uint4*>(xsm)[v] = q;  // masked copy for the stream
     xstats<DT>(st, q, s0 + v * 8);
   }
-  // rows that need the sample's maximum (top-k threshold, flat and keep-all
-  // reference) exchange it; greedy and error rows skip straight to the stream
-  const bool need_b1 = pcls == XC_TOPK || pcls == XC_FLAT || pcls == XC_ALL;
-  if (need_b1) {
+  // The local sample: this CTA's first stage.  Its maximum is the reference
+  // of flat and keep-all masses, and its fine key histogram places this CTA's
+  // candidate threshold; no exchange is needed before the stream, because
+  // every CTA lists all of its values above its own threshold and the
+  // resolution works on the key range that every CTA covers.
+  uint32_t sk = 0u;  // this CTA's stage-0 maximum key
+  uint32_t lo = 0xffffu, hw = 0xffffu;  // candidate window [lo, hw]
+  if (pcls == XC_TOPK || pcls == XC_FLAT || pcls == XC_ALL) {
     xreduce_stats<DT>(S, st, timed_out, 0);
-    if (want_samp) {
-      // every value of stage 0 in the XSW fine bins below the stage's maximum
-      const uint32_t kb = S.stage.kmax >> R::SB;
-      const uint32_t kfloor = kb >= (uint32_t)(XSW - 1) ? (kb - (XSW - 1)) << R::SB : 0u;
-      const uint32_t f2 = xraw(max(kfloor, R::KNINF + 1u)) * 0x10001u;
-      for (int i = tid; i < XSW / 2; i += XNT) hist[i] = 0u;
-      __syncthreads();
+    sk = S.stage.kmax;
+  }
+  if (want_samp) {
+    // every value of stage 0 in the XSW fine bins below the stage's maximum
+    const uint32_t kb = sk >> R::SB;
+    const uint32_t kfloor = kb >= (uint32_t)(XSW - 1) ? (kb - (XSW - 1)) << R::SB : 0u;
+    const uint32_t f2 = xraw(max(kfloor, R::KNINF + 1u)) * 0x10001u;
+    for (int i = tid; i < XSW / 2; i += XNT) hist[i] = 0u;
+    __syncthreads();
 #pragma unroll
-      for (int r = 0; r < XSUB; ++r) {
-        const int v = warp * XVW + r * 32 + lane;
-        if (v >= nvec || !S.stage.kmax) continue;
-        const uint4 q = v < nfull ? reinterpret_cast<const uint4*>(xsm)[v]
-                                  : xfetch<DT>(xsm, 0, v, nfull, n, gsrc, mrow);
-        if (xge2<DT>(xvmax<DT>(q), f2) == 0u) continue;
+    for (int r = 0; r < XSUB; ++r) {
+      const int v = warp * XVW + r * 32 + lane;
+      if (v >= nvec || !sk) continue;
+      const uint4 q = v < nfull ? xlds128(xsm + v * 16) : xfetch<DT>(xsm, 0, v, nfull, n, gsrc, mrow);
+      if (xge2<DT>(xvmax<DT>(q), f2) == 0u) continue;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t h = xhalf(q, e);
-          if (h == R::NINF) continue;
-          const uint32_t k = xkey(h);
-          if (k < kfloor || k <= R::KNINF || k > S.stage.kmax) continue;  // NaN keys lie above
-          const uint32_t b = kb - (k >> R::SB);
-          atomicAdd(&hist[b >> 1], 1u << ((b & 1u) << 4));
-        }
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t h = xhalf(q, e);
+        if (h == R::NINF) continue;
+        const uint32_t k = xkey(h);
+        if (k < kfloor || k <= R::KNINF || k > sk) continue;  // NaN keys lie above
+        const uint32_t b = kb - (k >> R::SB);
+        atomicAdd(&hist[b >> 1], 1u << ((b & 1u) << 4));
       }
-      __syncthreads();
-    }
-    if (tid < XSW) {
-      uint32_t c = 0;
-      if (want_samp && S.stage.kmax) c = (hist[tid >> 1] >> ((tid & 1) << 4)) & 0xffffu;
-      S.stage.samp[tid] = (uint16_t)c;
     }
     __syncthreads();
-    // ---- B1: publish the sample ----
-    xcluster_wait();  // B0 complete: every CTA of the cluster has started
-    {
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(&S.stage);
-      for (int t = tid; t < C * XPUBW; t += XNT) {
-        const int dst = t / XPUBW, w = t % XPUBW;
-        xremote(reinterpret_cast<uint32_t*>(&S.pub[rank]), (uint32_t)dst)[w] = src[w];
-      }
-    }
-    xcluster_sync();
-  }
-  // the sample's maximum over the row, and the top-k threshold
-  uint32_t sk = 0u;
-  if (need_b1)
-    for (int c = 0; c < C; ++c) sk = max(sk, S.pub[c].kmax);
-  uint32_t lo = 0xffffu, hw = 0xffffu;  // top-k window [lo, hw]
-  if (want_samp) {
-    // The sample is every value of each slice's first stage.  Aim the
-    // threshold at K + 3 sigma + 4 sampled values (flat top-p rows: a
-    // virtual K of XFLATK), then take the lower edge of the fine bin that
-    // reaches it.
-    int covered = 0;
-    for (int c = 0; c < C; ++c) covered += min(max(a.V - c * a.SL, 0), min(a.SL, XVS * 8));
-    const float fr = (float)covered / (float)a.V;  // sampled fraction of the row
-    const float kf = (float)(pcls == XC_FLAT ? min(kk, XFLATK) : kk) * fr;
+    // Aim at K + 3 sigma + 4 sampled values, with the sample taken as a
+    // sample of the whole row, and start the window at the lower edge of the
+    // fine bin that reaches it.
+    const float fr = (float)min(n, XVS * 8) / (float)a.V;
+    const float kf = (float)kk * fr;
     const int need = max(1, (int)ceilf(kf + 3.f * sqrtf(kf) + 4.f));
-    const uint32_t gb = sk >> R::SB;
     if (warp == 0) {
-      uint32_t cb[4] = {0u, 0u, 0u, 0u};  // bins gb - (4 lane + i)
-      for (int c = 0; c < C; ++c) {
-        const XPub& P = S.pub[c];
-        if (!P.kmax) continue;
-        const int sh = (int)gb - (int)(P.kmax >> R::SB);
+      uint32_t cb[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j0 = 4 * lane + i - sh;
-          if (j0 >= 0 && j0 < XSW) cb[i] += P.samp[j0];
-        }
+      for (int i = 0; i < 4; ++i) {
+        const int b = 4 * lane + i;
+        cb[i] = (hist[b >> 1] >> ((b & 1) << 4)) & 0xffffu;
       }
       const uint32_t sum = cb[0] + cb[1] + cb[2] + cb[3];
       const uint32_t inc = xwarp_incl<uint32_t>(sum);
@@ -889,10 +944,20 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     }
     __syncthreads();
     const int jb = S.bi[16];
-    const long long bl = ((long long)gb - jb) << R::SB;
-    lo = (uint32_t)max(bl, (long long)(R::KNINF + 1u));
-    if (jb >= XSW || sk == 0u) lo = R::KNINF + 1u;  // sample too thin: list everything legal
+    const long long bl = ((long long)kb - jb) << R::SB;
+    lo = (uint32_t)max(bl, (long long)R::KNINF);
+    if (jb >= XSW || sk == 0u) lo = R::KNINF;  // sample too thin: list every legal value
     hw = min(lo + (uint32_t)wf - 1u, 0xffffu);
+  }
+  // Flat top-p rows count every key of a window of `cap` keys in the stream,
+  // from XFM keys above this CTA's sample maximum down.
+  uint32_t* hcnt = reinterpret_cast<uint32_t*>(cid);
+  if (pcls == XC_FLAT) {
+    const uint32_t WH = (uint32_t)min(a.cap, XNS * XSB / 8);  // the resolution's count array holds as many
+    hw = sk ? min(sk + WH / XFM, 0xffffu) : 0xffffu;
+    lo = hw >= R::KNINF + WH ? hw - (WH - 1u) : R::KNINF + 1u;
+    for (int i = tid; i < (int)WH; i += XNT) hcnt[i] = 0u;
+    __syncthreads();
   }
   const uint32_t lo2 = xraw(lo) | (xraw(lo) << 16);
 
@@ -912,8 +977,8 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
   int xflags = 0;
 
   // keep-all rows: the exact-weight floor, 2^-24 below the sample's maximum
-  float zb = 0.f, xcf = -INFINITY;
-  uint32_t xc2 = 0u;
+  float zb = 0.f, xcf = -INFINITY;  // no sample maximum: every value exact
+  uint32_t xc2 = NN4;
   if (pcls == XC_ALL && sk) {
     zb = zref * L2E;
     const float f = R::f(xraw(sk)) - 10.f * 0.6931471805599453f * T;
@@ -962,6 +1027,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     cx.xcf = xcf;
     cx.xc2 = xc2;
     cx.flagw = flagw;
+    cx.hcnt = hcnt;
     if (pcls == XC_TOPK) xstream<DT, XS_TOPK>(cx, st, timed_out, issued, xflags, fm);
     else if (pcls == XC_FLAT) xstream<DT, XS_FLAT>(cx, st, timed_out, issued, xflags, fm);
     else if (pcls == XC_ALL) xstream<DT, XS_ALL>(cx, st, timed_out, issued, xflags, fm);
@@ -1047,6 +1113,10 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
   if (tid == 0) {
     S.stage.nleg = nvec * 8 - S.stage.nleg;
     S.stage.ncand = want_samp ? S.ncand : 0;
+    S.stage.lo = lo;
+    S.stage.hw = hw;
+    S.stage.skey = sk;
+    S.stage.xsv = sk ? R::f(xraw(sk)) : 0.f;
     double m = 0.0;
     if (pcls == XC_ALL) {
       for (int s = 0; s < nst; ++s)
@@ -1057,7 +1127,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     S.stage.mass = m;
   }
   __syncthreads();
-  if (!need_b1) xcluster_wait();  // B0 complete: every CTA of the cluster has started
+  xcluster_wait();  // B0 complete: every CTA of the cluster has started
   {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(&S.stage);
     for (int t = tid; t < C * XPUBW; t += XNT) {
@@ -1069,7 +1139,6 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
 
   uint32_t gk = 0u;
   int gid = INT_MAX, nleg = 0, flags = 0, ncand = 0;
-  double gmass = 0.0;
   for (int c = 0; c < C; ++c) {
     const XPub& P = S.pub2[c];
     if (P.kmax > gk) {
@@ -1079,7 +1148,6 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     nleg += P.nleg;
     flags |= P.flags;
     ncand += P.ncand;
-    gmass += P.mass;
   }
   int status = ST_OK;
   if (!params_ok) status = ST_INVALID;
@@ -1130,17 +1198,26 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
 
   const float xmax = XT<DT>::f(xraw(gk));
   const float zmax = __fdiv_rn(xmax, T);
-  // flat rows: the legal mass the stream accumulated (relative to the
-  // sample's maximum), rescaled to fixed point of the row's maximum
-  const double Mflat =
-      pcls == XC_FLAT
-          ? (double)gmass * (double)ex2f((XT<DT>::f(xraw(sk)) - xmax) * (L2E / T)) * 1099511627776.0
-          : 0.0;
-  uint64_t* rwq = reinterpret_cast<uint64_t*>(xsm);  // per-(round, warp) sums, in the ring area
+  // Flat and keep-all rows: each CTA's legal mass is relative to its own
+  // sample's maximum; scale factors to the row's maximum, and the row's mass
+  // in those units (Mflat: in fixed point of the largest weight).
+  double xsc[XMAXC];
+  double gm = 0.0, sc_me = 1.0;
+#pragma unroll
+  for (int c = 0; c < XMAXC; ++c) {
+    xsc[c] = 0.0;
+    if (c < C && (pcls == XC_FLAT || pcls == XC_ALL)) {
+      // exp(fl32(xs_c / T) - fl32(xmax / T)): the same z the weights use
+      xsc[c] = (double)ex2f((__fdiv_rn(S.pub2[c].xsv, T) - zmax) * L2E);
+      gm += S.pub2[c].mass * xsc[c];
+    }
+    if (c == (int)rank) sc_me = xsc[c];
+  }
+  const double Mflat = pcls == XC_FLAT ? gm * 1099511627776.0 : 0.0;
 
   // ---- keep-all rows: the masses came with the stream ----
   if (cls == XC_ALL) {
-    const double M = gmass;
+    const double M = gm;
     if (pout) {
       for (int v = tid; v < nvec; v += XNT) {
         const uint4 q = xgfetch<DT>(v, nfull, n, gsrc, mrow);
@@ -1149,7 +1226,8 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
           if (v * 8 + e >= n) break;
           const uint32_t h = xhalf(q, e);
           pout[v * 8 + e] =
-              h != R::NINF ? (float)((double)xall_w<DT>(h, tz, T, zref, L2E / T, zb, xcf) / M) : 0.f;
+              h != R::NINF ? (float)((double)xall_w<DT>(h, tz, T, zref, L2E / T, zb, xcf) * sc_me / M)
+                           : 0.f;
         }
       }
     }
@@ -1158,11 +1236,12 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
       double before = 0.0;
       int cs = C - 1;
       for (int c = 0; c < C; ++c) {
-        if (before + S.pub2[c].mass > tgt) {
+        const double mc = S.pub2[c].mass * xsc[c];
+        if (before + mc > tgt) {
           cs = c;
           break;
         }
-        before += S.pub2[c].mass;
+        before += mc;
       }
       if ((int)rank == cs && warp == 0) {
         // per-(stage, warp) masses of this slice, in id order
@@ -1174,7 +1253,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
           if (j < ne) sacc += (double)S.rwf[j / XNW][j % XNW];
         }
         const double inc = xwarp_incl<double>(sacc);
-        const double t2 = tgt - before;
+        const double t2 = sc_me > 0.0 ? (tgt - before) / sc_me : 0.0;  // in this CTA's units
         const uint32_t hit = __ballot_sync(0xffffffffu, inc > t2);
         const int L = hit ? __ffs(hit) - 1 : 31;
         double bef = __shfl_sync(0xffffffffu, inc - sacc, L);
@@ -1267,7 +1346,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
       __syncthreads();
       if ((int)rank == cs && tid == 0) {
         a.tokens[row] = S.bi[17];
-        if (a.logprob) a.logprob[row] = fminf((float)(log((double)S.f[0]) - log(M)), 0.f);
+        if (a.logprob) a.logprob[row] = fminf((float)(log((double)S.f[0] * sc_me) - log(M)), 0.f);
       }
     }
     xfinish(a, row, rank, ST_OK, -1, nleg, PATH_ALL, 0, nst, 0);
@@ -1283,151 +1362,165 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
   int path = PATH_SIGMA, passes = 1, nwin = 0, band = 0;
   bool failed = false;
   uint32_t whi = 0, wlo = 0;  // the window the boundary was resolved in
-  uint64_t* wtab = reinterpret_cast<uint64_t*>(xsm);  // per-bin weights, in the ring area
+  uint32_t* cntA = reinterpret_cast<uint32_t*>(xsm);  // the row's per-key counts (ring area)
+  uint64_t* wtab = reinterpret_cast<uint64_t*>(xsm + XNS * XSB / 2);  // weights of the first XWT keys
 
   bool sync_first = false;  // the window search must first wait for this pull
   if (cls == XC_TOPK || cls == XC_FLATL) {
-    // bins b = hw - key; keys above gk are empty
-    const int b0 = (int)(hw - gk) & ~1;  // even, so a thread's words are whole
-    const int nbins = wf - b0;
-    band = (int)(gk - lo) + 1;
-    const int cpt = ((nbins + XNT - 1) / XNT + 1) & ~1;  // bins per thread, even
-    const int t0 = b0 + tid * cpt;
-    constexpr int MAXB = 32;  // bins per thread, at most (wf <= 4096, XNT = 128)
-    // pull every CTA's counters of my bins (two 16-bit counts per word)
-    uint32_t bc[MAXB];
-#pragma unroll
-    for (int i = 0; i < MAXB; ++i) bc[i] = 0u;
-    {
-      const int nw = min(cpt, max(0, wf - t0)) >> 1;
+    // Every CTA listed all of its values >= its own threshold, so the key
+    // range [LO, gk] with LO the largest threshold is complete.  Key index
+    // i stands for key gk - i; CTA c counts key k in bin hw_c - k.  The
+    // row's counts go to shared memory (ring area), with the weights of the
+    // first XWT keys beside them.
+    uint32_t LO = 0u;
+    for (int c = 0; c < C; ++c) LO = max(LO, S.pub2[c].lo);
+    const bool wide = cls == XC_FLATL;  // the stream's own window counts
+    const uint32_t* hc = wide ? hcnt : hist;
+    const int nk = gk >= LO ? (int)(gk - LO) + 1 : 0;
+    band = nk;
+    for (int i = tid; i < nk; i += XNT) {
+      const uint32_t k = gk - (uint32_t)i;
+      uint32_t cnt = 0;
 #pragma unroll
       for (int c = 0; c < XMAXC; ++c) {
-        if (c >= C) break;
-        const uint32_t* rh = xremote(hist, (uint32_t)c) + (t0 >> 1);
-#pragma unroll
-        for (int i = 0; i < MAXB / 2; ++i)
-          if (i < nw) {
-            const uint32_t w = rh[i];
-            bc[2 * i] += w & 0xffffu;
-            bc[2 * i + 1] += w >> 16;
+        if (c < C) {
+          const uint32_t hwc = S.pub2[c].hw;
+          if (k <= hwc) {
+            const uint32_t bq = hwc - k;
+            cnt += xcnt(xremote(hc, (uint32_t)c), bq, wide);
           }
+        }
       }
+      cntA[i] = cnt;
+      if (i < XWT) wtab[i] = cnt ? xwfx(XT<DT>::f(xraw(k)), T, zmax) : 0ull;
     }
+    __syncthreads();
+    const int cpt = (nk + XNT - 1) / XNT;
+    const int t0 = min(tid * cpt, nk), t1 = min(t0 + cpt, nk);  // this thread's contiguous keys
     uint32_t ct = 0;
-#pragma unroll
-    for (int i = 0; i < MAXB; ++i) ct += (i < cpt) ? bc[i] : 0u;
+    for (int i = t0; i < t1; ++i) ct += cntA[i];
     uint32_t ctot;
     const uint32_t cpre = xblock_excl<uint32_t>(ct, reinterpret_cast<uint32_t*>(S.wi), &ctot);
-    // the k-th largest key and its quota (a8.5, a8.6); flat rows keep every bin
-    if (tid == 0) {
-      S.bi[18] = cls == XC_FLATL ? wf : -1;
-      S.bi[19] = 0;
-    }
-    __syncthreads();
-    if (cls == XC_TOPK && cpre < (uint32_t)K && cpre + ct >= (uint32_t)K) {
-      uint32_t c = cpre;
-#pragma unroll
-      for (int i = 0; i < MAXB; ++i) {
-        if (i < cpt && c < (uint32_t)K && c + bc[i] >= (uint32_t)K) {
-          S.bi[18] = t0 + i;
-          S.bi[19] = (int)((uint32_t)K - c);
-        }
-        c += (i < cpt) ? bc[i] : 0u;
-      }
-    }
-    __syncthreads();
-    const int kbin = S.bi[18];
-    const int quota = S.bi[19];
-    if (kbin < 0) {
-      failed = true;  // cannot happen when the list was validated
+    // the listed keys must hold the k-th largest value (or every legal one)
+    const bool short_list = cls == XC_TOPK && ctot < (uint32_t)K && ctot != (uint32_t)nleg;
+    if (short_list) {
+      sync_first = true;
+      cls = K < nleg ? -XC_TOPK : XC_FLAT;
     } else {
-      const uint32_t kap = hw - (uint32_t)kbin;
-      // S_k's mass, per-bin weights kept for the draw
-      uint64_t mt = 0;
-#pragma unroll
-      for (int i = 0; i < MAXB; ++i) {
-        const int b = t0 + i;
-        if (i < cpt && b <= kbin && b < wf) {
-          const uint64_t w = bc[i] ? xwfx(XT<DT>::f(xraw(hw - (uint32_t)b)), T, zmax) : 0ull;
-          wtab[b - b0] = w;
-          mt += (uint64_t)(b == kbin ? (uint32_t)quota : bc[i]) * w;
-        }
-      }
-      uint64_t Mk;
-      const uint64_t mpre = xblock_excl<uint64_t>(mt, S.q, &Mk);
-      // flat rows: S_k is every legal value; its mass came with the stream
-      // (relative to the sample's maximum xs, rescaled to the row's maximum)
-      if (cls == XC_TOPK && pp >= 1.f) {
-        beta = kap;
-        nb = quota;
-        Abeta = (uint64_t)(K - quota);
-      } else if (cls == XC_FLATL && (double)Mk < (double)pp * Mflat) {
-        sync_first = true;  // the boundary lies below the listed values
-        cls = XC_FLAT;
-      } else {
-        // top-p (a8.7): the first bin whose prefix reaches ceil(p * Mk)
-        const uint64_t P64 =
-            (uint64_t)ceil((double)pp * (cls == XC_FLATL ? Mflat : (double)Mk));
-        if (tid == 0) S.bi[20] = -1;
-        __syncthreads();
-        if (mpre < P64 && mpre + mt >= P64) {
-          uint64_t c = mpre;
-          uint64_t cc = cpre;
-          bool done = false;
-#pragma unroll
-          for (int i = 0; i < MAXB; ++i) {
-            const int b = t0 + i;
-            if (done || i >= cpt || b > kbin || !bc[i]) continue;
-            const uint64_t avail = (b == kbin) ? (uint64_t)quota : (uint64_t)bc[i];
-            const uint64_t w = wtab[b - b0];
-            if (c + avail * w >= P64) {
-              uint64_t need = w ? (P64 - c + w - 1) / w : avail;
-              need = min(max(need, (uint64_t)1), avail);
-              S.bi[20] = b;
-              S.bi[21] = (int)need;
-              S.bq[0] = cc;
-              done = true;
-            }
-            c += avail * w;
-            cc += avail;
-          }
-        }
-        __syncthreads();
-        if (S.bi[20] < 0) {
-          failed = true;
-        } else {
-          beta = hw - (uint32_t)S.bi[20];
-          nb = S.bi[21];
-          Abeta = S.bq[0];
-        }
-      }
-    }
-    if (!failed && cls != XC_FLAT) {
-      // this CTA's share of beta's copies: ids before this slice come first
-      const int bb = (int)(hw - beta);
-      Nme = (int)((hist[bb >> 1] >> ((bb & 1) << 4)) & 0xffffu);
-      if (warp == 0) {
-        uint32_t c = 0;
-        if (lane < C && lane < (int)rank) {
-          const uint32_t* rh = xremote(hist, (uint32_t)lane);
-          c = (rh[bb >> 1] >> ((bb & 1) << 4)) & 0xffffu;
-        }
-        c = __reduce_add_sync(0xffffffffu, c);
-        if (lane == 0) S.bi[22] = (int)c;
+      // the k-th largest key and its quota (a8.5, a8.6); flat rows, and
+      // top-k rows whose every legal value is listed, keep every key
+      if (tid == 0) {
+        S.bi[18] = (cls == XC_FLATL || ctot < (uint32_t)K) ? nk : -1;
+        S.bi[19] = 0;
       }
       __syncthreads();
-      share = min(max(nb - S.bi[22], 0), Nme);
-      // my kept mass from my own bins above beta, plus my share of beta
-      uint64_t mine = 0;
-      for (int b = b0 + tid; b < bb; b += XNT) {
-        const uint32_t c = (hist[b >> 1] >> ((b & 1) << 4)) & 0xffffu;
-        if (c) mine += (uint64_t)c * wtab[b - b0];
+      if (cls == XC_TOPK && ctot >= (uint32_t)K && cpre < (uint32_t)K && cpre + ct >= (uint32_t)K) {
+        uint32_t c = cpre;
+        for (int i = t0; i < t1; ++i) {
+          if (c + cntA[i] >= (uint32_t)K) {
+            S.bi[18] = i;
+            S.bi[19] = (int)((uint32_t)K - c);
+            break;
+          }
+          c += cntA[i];
+        }
       }
-      mine = xblock_total<uint64_t>(mine, S.q);
-      KMme = mine + (uint64_t)share * wtab[bb - b0];
+      __syncthreads();
+      const int kbin = S.bi[18];
+      const int quota = S.bi[19];
+      if (kbin < 0) {
+        failed = true;
+      } else {
+        uint64_t mt = 0;
+        for (int i = t0; i < min(t1, kbin + 1); ++i) {
+          const uint32_t cnt = (i == kbin) ? (uint32_t)quota : cntA[i];
+          if (cnt) mt += (uint64_t)cnt * xw_at<DT>(wtab, i, gk, T, zmax);
+        }
+        uint64_t Mk;
+        const uint64_t mpre = xblock_excl<uint64_t>(mt, S.q, &Mk);
+        if (cls == XC_TOPK && pp >= 1.f) {
+          if (kbin >= nk) {  // every legal value is kept
+            beta = 0u;
+            nb = 0;
+            Abeta = ctot;
+          } else {
+            beta = gk - (uint32_t)kbin;
+            nb = quota;
+            Abeta = (uint64_t)(K - quota);
+          }
+        } else if (cls == XC_FLATL && (double)Mk < (double)pp * Mflat) {
+          sync_first = true;  // the boundary lies below the listed values
+          cls = XC_FLAT;
+        } else {
+          // top-p (a8.7): the first key whose prefix reaches ceil(p * Mk)
+          const uint64_t P64 =
+              (uint64_t)ceil((double)pp * (cls == XC_FLATL ? Mflat : (double)Mk));
+          if (tid == 0) S.bi[20] = -1;
+          __syncthreads();
+          if (mpre < P64 && mpre + mt >= P64) {
+            uint64_t c = mpre;
+            uint64_t cc = cpre;
+            for (int i = t0; i < min(t1, kbin + 1); ++i) {
+              const uint64_t avail = (i == kbin) ? (uint64_t)quota : (uint64_t)cntA[i];
+              if (!avail) continue;
+              const uint64_t w = xw_at<DT>(wtab, i, gk, T, zmax);
+              if (c + avail * w >= P64) {
+                uint64_t need = w ? (P64 - c + w - 1) / w : avail;
+                need = min(max(need, (uint64_t)1), avail);
+                S.bi[20] = i;
+                S.bi[21] = (int)need;
+                S.bq[0] = cc;
+                break;
+              }
+              c += avail * w;
+              cc += avail;
+            }
+          }
+          __syncthreads();
+          if (S.bi[20] < 0) {
+            failed = true;
+          } else {
+            beta = gk - (uint32_t)S.bi[20];
+            nb = S.bi[21];
+            Abeta = S.bq[0];
+          }
+        }
+      }
+      if (!failed && cls != XC_FLAT) {
+        // this CTA's share of beta's copies (ids before this slice come first)
+        // and the mass it keeps
+        const int ib = beta ? (int)(gk - beta) : nk;  // keys above beta: indices [0, ib)
+        if (beta) {
+          const uint32_t bq = hw - beta;
+          Nme = beta <= hw ? (int)xcnt(hc, bq, wide) : 0;
+          if (warp == 0) {
+            uint32_t c = 0;
+            if (lane < C && lane < (int)rank) {
+              const uint32_t hwc = S.pub2[lane].hw;
+              if (beta <= hwc) {
+                const uint32_t bc2 = hwc - beta;
+                c = xcnt(xremote(hc, (uint32_t)lane), bc2, wide);
+              }
+            }
+            c = __reduce_add_sync(0xffffffffu, c);
+            if (lane == 0) S.bi[22] = (int)c;
+          }
+          __syncthreads();
+          share = min(max(nb - S.bi[22], 0), Nme);
+        }
+        uint64_t mine = 0;
+        for (int i = tid; i < ib; i += XNT) {
+          const uint32_t k = gk - (uint32_t)i;
+          if (k > hw) continue;
+          const uint32_t c = xcnt(hc, hw - k, wide);
+          if (c) mine += (uint64_t)c * xw_at<DT>(wtab, i, gk, T, zmax);
+        }
+        mine = xblock_total<uint64_t>(mine, S.q);
+        KMme = mine + (beta ? (uint64_t)share * xw_at<DT>(wtab, ib, gk, T, zmax) : 0ull);
+      }
+      whi = gk;
+      wlo = LO;
     }
-    whi = hw;
-    wlo = lo;
   }
   if (cls == -XC_TOPK || cls == XC_FLAT) {
     // ---- the exact window search over the slice re-read from global ----
@@ -1700,9 +1793,10 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
   }
 
   // ---- B3: every CTA's kept mass ----
+  if (tid == 0) S.bi[23] = 0;  // pass C's expired waits, set by any CTA of the row
   for (int c = tid; c < C; c += XNT) *xremote(&S.km[rank], (uint32_t)c) = KMme;
   __syncthreads();
-  xcluster_sync();  // no remote access follows
+  xcluster_sync();  // the kept masses are in place
   uint64_t Mp = 0;
   for (int c = 0; c < C; ++c) Mp += S.km[c];
   if (failed || Mp == 0) {
@@ -1717,12 +1811,16 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
   const float Mf = (float)Mp * 0x1p-40f;
   const float bval = beta ? XT<DT>::f(xraw(beta)) : -INFINITY;
   const uint32_t bv2 = beta ? (xraw(beta) | (xraw(beta) << 16)) : 0u;
-  const bool from_list = cls == XC_TOPK || cls == XC_FLATL;
+  const bool from_list = cls == XC_TOPK;
   const int nc = from_list ? min(S.ncand, a.cap) : 0;
+  // Outside the list a partial tie (some of this CTA's copies of beta kept)
+  // is settled after pass C from the copies' ids, which the pass lists, when
+  // they fit the id list; otherwise by a selection over the slice first.
+  const bool dtie = !from_list && beta && share > 0 && share < Nme && Nme <= XBL;
 
   // ---- the id cut among the copies of beta kept here (earliest ids) ----
   int cut = INT_MAX;  // copies of beta with local id < cut are kept
-  if (beta && share < Nme) {
+  if (beta && share < Nme && !dtie) {
     if (share == 0) {
       cut = -1;
     } else {
@@ -1812,7 +1910,6 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     if (pout)
       for (int e = tid; e < n; e += XNT) pout[e] = 0.f;
     __syncthreads();
-    const int b0 = (int)(hw - gk) & ~1;
     for (int i = tid; i < nc; i += XNT) {
       const uint32_t k = ckey[i];
       const int id = cid[i];
@@ -1834,7 +1931,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
         const int id = cid[i];
         if ((unsigned)id >= (unsigned)n || k > gk || !xkept(bval, cut, XT<DT>::f(xraw(k)), id))
           continue;
-        smem_add_u64(&bkt[id / bw], wtab[(int)(hw - k) - b0]);
+        smem_add_u64(&bkt[id / bw], xw_at<DT>(wtab, (int)(gk - k), gk, T, zmax));
       }
       __syncthreads();
       if (warp == 0) {
@@ -1865,10 +1962,10 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
       __syncthreads();
       for (int i = tid; i < ng; i += XNT) {
         const int id = (int)g[i].x;
-        const uint64_t w = wtab[(int)(hw - g[i].y) - b0];
+        const uint64_t w = xw_at<DT>(wtab, (int)(gk - g[i].y), gk, T, zmax);
         uint64_t cum = 0;
         for (int j = 0; j < ng; ++j)
-          if ((int)g[j].x < id) cum += wtab[(int)(hw - g[j].y) - b0];
+          if ((int)g[j].x < id) cum += xw_at<DT>(wtab, (int)(gk - g[j].y), gk, T, zmax);
         if (cum <= rem && rem < cum + w) {
           S.bi[11] = id;
           S.bi[12] = (int)g[i].y;
@@ -1884,103 +1981,206 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
       }
     }
   } else {
-    // ---- pass C over the slice re-read from global ----
-    const int nround = (nvec + XNT - 1) / XNT;
-    if (mout || pout || drawer) {
-      for (int j0 = 0; j0 < nround; j0 += 4) {
-        uint4 q4[4];
+    // ---- pass C: the slice streamed through the ring again ----
+    // Kept: above beta, or a copy of beta before the id cut (an open cut:
+    // the copies are listed and settled after the pass).  The drawer sums
+    // the kept weights per (stage, warp) cell, the cells being consecutive
+    // id ranges of XVW vectors.
+    unsigned char* reg = xsm + xoff_hist();
+    uint64_t* pq = reinterpret_cast<uint64_t*>(reg);  // per-cell kept masses
+    int* blist = reinterpret_cast<int*>(reg + XMAXST * XNW * 8);  // copies of beta
+    uint64_t* wt = reinterpret_cast<uint64_t*>(reg + XMAXST * XNW * 8 + XBL * 4);
+    const int tcap = (xoff_sh(wf, a.cap) - xoff_hist() - XMAXST * XNW * 8 - XBL * 4) / 8;
+    const int ntab = drawer ? (beta ? min((int)(gk - beta) + 1, tcap) : tcap) : 0;
+    const uint32_t kv2 = beta ? bv2 : NN4;  // kept: above this (every legal value when beta = 0)
+    const bool run = mout || pout || drawer;
+    int tfail = 0;
+    if (run) {
+      for (int i = tid; i < ntab; i += XNT) {
+        const uint32_t k = gk - (uint32_t)i;
+        wt[i] = k > R::KNINF ? xwfx(R::f(xraw(k)), T, zmax) : 0ull;
+      }
+      if (tid == 0) S.bi[13] = 0;
+      __syncthreads();  // the ring area is free, the table ready
+      // slot j finished (nst - j + XNS - 1) / XNS phases in the first stream
+      int issued2 = 0;
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        for (int t = 0; t < XNS && t < nst; ++t, ++issued2) {
+          const int v0 = t * XVS, v1 = min(nfull, v0 + XVS);
+          const uint32_t bytes = v1 > v0 ? (uint32_t)(v1 - v0) * 16u : 0u;
+          mbar_arrive_expect_tx(&S.bar[t], bytes);
+          if (bytes) bulk_g2s(xsm + t * XSB, gsrc + (size_t)v0 * 8, bytes, &S.bar[t]);
+        }
+      }
+      const bool ties = beta && (dtie || cut >= 0);  // copies of beta may be kept
+      for (int st2 = 0; st2 < nst; ++st2) {
+        const int slot = st2 % XNS;
+        const int par = (((nst - slot + XNS - 1) / XNS) + st2 / XNS) & 1;
+        if (!tfail && st2 * XVS < nfull && !mbar_wait_bounded(&S.bar[slot], par, a.wait_limit))
+          tfail = 1;
+        uint64_t sw = 0;
+        // the warp's XSUB vectors of this stage, loaded together
+        uint4 q4[XSUB];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int v = (j0 + u) * XNT + tid;
-          q4[u] = v < nvec ? xgfetch<DT>(v, nfull, n, gsrc, mrow) : make_uint4(NN4, NN4, NN4, NN4);
+        for (int r = 0; r < XSUB; ++r) {
+          const int v = st2 * XVS + warp * XVW + r * 32 + lane;
+          q4[r] = (v < nvec && !tfail) ? xfetch<DT>(xsm, slot, v, nfull, n, gsrc, mrow)
+                                       : make_uint4(NN4, NN4, NN4, NN4);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u;
-        if (j >= nround) break;
-        const int v = j * XNT + tid;
-        uint32_t byte = 0;
-        uint64_t s = 0;
-        float pr[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pr[i] = 0.f;
-        if (v < nvec) {
-          const uint4 q = q4[u];
-          if (!beta || xany_ge<DT>(q, bv2)) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t h = xhalf(q, i);
-              if (h == R::NINF) continue;
-              const float x = R::f(h);
-              if (xkept(bval, cut, x, v * 8 + i)) {
-                byte |= 1u << i;
-                if (drawer) s += xwfx(x, T, zmax);
-                if (pout) pr[i] = xweight(x, T, zmax) / Mf;
+        for (int r = 0; r < XSUB; ++r) {
+          const int v = st2 * XVS + warp * XVW + r * 32 + lane;
+          const bool in = v < nvec && !tfail;
+          uint32_t byte = 0;
+          const uint4 q = q4[r];
+          if (in) {
+            byte = xbits8(xgt2<DT>(q.x, kv2), xgt2<DT>(q.y, kv2), xgt2<DT>(q.z, kv2),
+                          xgt2<DT>(q.w, kv2));
+            if (ties) {
+              const uint32_t eb = xbits8(xeq2<DT>(q.x, bv2), xeq2<DT>(q.y, bv2),
+                                         xeq2<DT>(q.z, bv2), xeq2<DT>(q.w, bv2));
+              if (eb) {
+#pragma unroll 1
+                for (uint32_t m = eb; m; m &= m - 1u) {
+                  const int id = v * 8 + (__ffs(m) - 1);
+                  if (dtie) {
+                    const int pos = atomicAdd(&S.bi[13], 1);
+                    if (pos < XBL) blist[pos] = id;
+                  } else if (id < cut) {
+                    byte |= 1u << (__ffs(m) - 1);
+                  }
+                }
               }
             }
           }
-        }
-        if (mout) xput_mask_byte(mout, v, byte, v < nvec);
-        if (pout && v < nvec) {
+          if (mout) xput_mask_byte(mout, v, byte, in);
+          if (drawer && byte) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (v * 8 + i < n) pout[v * 8 + i] = pr[i];
+            for (int e = 0; e < 8; ++e) {
+              if (!((byte >> e) & 1u)) continue;
+              const uint32_t h = xhalf(q, e);
+              const int i = (int)(gk - xkey(h));
+              sw += i < ntab ? wt[i] : xwfx(R::f(h), T, zmax);
+            }
+          }
+          if (pout && in) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (v * 8 + e < n)
+                pout[v * 8 + e] = ((byte >> e) & 1u) ? xweight(R::f(xhalf(q, e)), T, zmax) / Mf : 0.f;
+          }
         }
         if (drawer) {
-          const uint64_t ws = xwarp_sum64(s);
-          if (lane == 0) rwq[j * XNW + warp] = ws;
+          sw = xwarp_sum64(sw);
+          if (lane == 0) pq[st2 * XNW + warp] = sw;
         }
+        // every warp is done with the slot; after an expired wait no more copies go out
+        tfail = __syncthreads_or(tfail);
+        if (tid == 0 && !tfail && st2 + XNS < nst) {
+          const int v0 = (st2 + XNS) * XVS, v1 = min(nfull, v0 + XVS);
+          const uint32_t bytes = v1 > v0 ? (uint32_t)(v1 - v0) * 16u : 0u;
+          mbar_arrive_expect_tx(&S.bar[slot], bytes);
+          if (bytes) bulk_g2s(xsm + slot * XSB, gsrc + (size_t)v0 * 8, bytes, &S.bar[slot]);
+          ++issued2;
+        }
+      }
+      if (tfail && tid == 0) {
+        // wait (bounded again) for every copy still in flight into the ring
+        for (int t = max(0, issued2 - XNS); t < issued2; ++t) {
+          const int sl = t % XNS;
+          mbar_wait_bounded(&S.bar[sl], (((nst - sl + XNS - 1) / XNS) + t / XNS) & 1, a.wait_limit);
+        }
+      }
+      if (dtie && !tfail) {
+        // the share-th earliest copy of beta here; then the kept copies' bits,
+        // probabilities and masses
+        const int nbl = min(S.bi[13], XBL);
+        cut = xsel_id(blist, nbl, share - 1, S) + 1;
+        const uint64_t wb = drawer ? xwfx(bval, T, zmax) : 0ull;
+        for (int i = tid; i < nbl; i += XNT) {
+          const int id = blist[i];
+          if (id >= cut) continue;
+          if (mout) atomicOr(&mout[id >> 5], 1u << (id & 31));
+          if (pout) pout[id] = xweight(bval, T, zmax) / Mf;
+          if (drawer) smem_add_u64(&pq[(id >> 3) / XVW], wb);
+        }
+        __syncthreads();
+      }
+      if (drawer && !tfail) {
+        if (warp == 0) {
+          uint64_t rem;
+          const int e = xlocate<uint64_t>(pq, nst * XNW, tgt - before, &rem);
+          if (lane == 0) {
+            S.bi[12] = e;
+            S.bq[5] = rem;
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          // the cell's XVW vectors, 32 at a time, in id order
+          const int e = S.bi[12];
+          uint64_t rem = S.bq[5];
+          const int vb = (e / XNW) * XVS + (e % XNW) * XVW;
+          uint4 q4[XSUB];
+#pragma unroll
+          for (int r = 0; r < XSUB; ++r) {
+            const int v = vb + r * 32 + lane;
+            q4[r] = v < nvec ? xgfetch<DT>(v, nfull, n, gsrc, mrow) : make_uint4(NN4, NN4, NN4, NN4);
+          }
+          bool done = false;
+#pragma unroll
+          for (int r = 0; r < XSUB; ++r) {
+            if (done) break;
+            const int v = vb + r * 32 + lane;
+            uint64_t sv = 0;
+#pragma unroll
+            for (int e8 = 0; e8 < 8; ++e8) {
+              const uint32_t h = xhalf(q4[r], e8);
+              if (h == R::NINF || !xkept(bval, cut, R::f(h), v * 8 + e8)) continue;
+              const int i = (int)(gk - xkey(h));
+              sv += i < ntab ? wt[i] : xwfx(R::f(h), T, zmax);
+            }
+            const uint64_t inc = xwarp_incl<uint64_t>(sv);
+            const uint64_t tot = __shfl_sync(0xffffffffu, inc, 31);
+            if (rem >= tot && r + 1 < XSUB) {
+              rem -= tot;
+              continue;
+            }
+            done = true;
+            const uint32_t hit = __ballot_sync(0xffffffffu, inc > rem);
+            const int L = hit ? __ffs(hit) - 1 : 31;
+            if (lane == L) {
+              uint64_t c = inc - sv;
+              int tok = -1;
+              float wx = 0.f;
+              for (int e8 = 0; e8 < 8; ++e8) {
+                const uint32_t h = xhalf(q4[r], e8);
+                if (h == R::NINF || !xkept(bval, cut, R::f(h), v * 8 + e8)) continue;
+                const int i = (int)(gk - xkey(h));
+                c += i < ntab ? wt[i] : xwfx(R::f(h), T, zmax);
+                tok = s0 + v * 8 + e8;
+                wx = R::f(h);
+                if (c > rem) break;
+              }
+              a.tokens[row] = tok;
+              if (a.logprob) a.logprob[row] = fminf(logf(xweight(wx, T, zmax)) - logf(Mf), 0.f);
+            }
+          }
         }
       }
     }
-    if (drawer) {
-      __syncthreads();
-      if (warp == 0) {
-        uint64_t rem;
-        const int e = xlocate<uint64_t>(rwq, nround * XNW, tgt - before, &rem);
-        if (lane == 0) {
-          S.bi[12] = e;
-          S.bq[5] = rem;
-        }
-      }
-      __syncthreads();
-      const int e = S.bi[12];
-      const uint64_t rem = S.bq[5];
-      if (warp == e % XNW) {
-        const int v = (e / XNW) * XNT + warp * 32 + lane;
-        uint64_t s = 0;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (v < nvec) {
-          q = xgfetch<DT>(v, nfull, n, gsrc, mrow);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t h = xhalf(q, i);
-            if (h == R::NINF) continue;
-            const float x = R::f(h);
-            if (xkept(bval, cut, x, v * 8 + i)) s += xwfx(x, T, zmax);
-          }
-        }
-        const uint64_t inc = xwarp_incl<uint64_t>(s);
-        const uint32_t hit = __ballot_sync(0xffffffffu, inc > rem);
-        const int L = hit ? __ffs(hit) - 1 : 31;
-        if (lane == L) {
-          uint64_t c = inc - s;
-          int tok = -1;
-          float wt = 0.f;
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t h = xhalf(q, i);
-            if (h == R::NINF) continue;
-            const float x = R::f(h);
-            if (!xkept(bval, cut, x, v * 8 + i)) continue;
-            c += xwfx(x, T, zmax);
-            tok = s0 + v * 8 + i;
-            wt = xweight(x, T, zmax);
-            if (c > rem) break;
-          }
-          a.tokens[row] = tok;
-          if (a.logprob) a.logprob[row] = fminf(logf(wt) - logf(Mf), 0.f);
-        }
-      }
+    // ---- the row's pass C statuses: every CTA learns of any expired wait ----
+    if (tfail && tid < C) atomicOr(xremote(&S.bi[23], (uint32_t)tid), 1);
+    __syncthreads();
+    xcluster_sync();  // no remote access follows
+    if (S.bi[23]) {
+      if (mout)
+        for (int w = tid; w < ((n + 31) >> 5); w += XNT) mout[w] = 0u;
+      if (pout)
+        for (int e = tid; e < n; e += XNT) pout[e] = 0.f;
+      xfinish(a, row, rank, ST_TIMEOUT, -1, 0, PATH_ERROR, __LINE__, passes, nwin);
+      return;
     }
   }
   xfinish(a, row, rank, ST_OK, -1, (int)(Abeta + (uint64_t)nb), path, band, passes, nwin);
