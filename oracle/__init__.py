@@ -24,11 +24,16 @@ Parity status of each function (what pins it is listed in the tests):
   * orc_gumbel_sample -- pinned by its frequencies against the exact softmax
                         of the kept set (the lecture's Gumbel-max identity),
                         greedy at T = 0, statuses and the uniform's range.
-  * orc_spec_verify_u / orc_spec_verify -- pinned by the exact output
-                        distribution (it equals the target's, the identity of
-                        the lecture notes' section 5.2), the acceptance rate
-                        sum(min(p, q)), special cases (p == q, disjoint
-                        supports) and Philox frequencies.
+  * orc_spec_verify_u / orc_spec_verify -- the rule over the reals (double
+                        residual, compensated sums); pinned by the exact
+                        output distribution (it equals the target's, the
+                        identity of the lecture notes' section 5.2), the
+                        acceptance rate sum(min(p, q)), special cases (p == q,
+                        disjoint supports) and Philox frequencies.
+  * orc_spec_verify_fx_u (fixed=True) -- a second, labelled variant in the
+                        CUDA library's stated integer precision; pinned by
+                        agreement with the real-number rule wherever u * S
+                        lies more than 1e-9 of S from a switch point.
 """
 import ctypes
 import os
@@ -65,9 +70,13 @@ def load(path):
     L.orc_spec_verify_u.restype = ctypes.c_int
     L.orc_spec_verify_u.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int64, P, P, P,
                                     P, P, P]
+    L.orc_spec_verify_fx_u.restype = ctypes.c_int
+    L.orc_spec_verify_fx_u.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int64, P, P,
+                                       P, P, P]
     L.orc_spec_verify.restype = ctypes.c_int
     L.orc_spec_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
-                                  ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_int]
+                                  ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_int,
+                                  ctypes.c_int]
     L.orc_f32_to_bf16.restype = ctypes.c_uint16
     L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
     L.orc_f32_to_f16.restype = ctypes.c_uint16
@@ -185,9 +194,10 @@ def row_stats(logits_row_bits, dtype, V, temperature=1.0, mask_row=None):
                 logsumexp=out[5], nonfinite=bool(out[6]))
 
 
-def spec_verify_u(p, q, d, u_acc, u_res, L=None):
+def spec_verify_u(p, q, d, u_acc, u_res, L=None, fixed=False):
     """One sequence with explicit uniforms.  p: float32 [G+1, V], q: float32
-    [G, V], d: int [G], u_acc: [G], u_res: [G+1].  Returns a dict."""
+    [G, V], d: int [G], u_acc: [G], u_res: [G+1].  fixed: the labelled
+    fixed-point variant instead of the real-number rule.  Returns a dict."""
     p = np.ascontiguousarray(p, dtype=np.float32)
     G1, V = p.shape
     G = G1 - 1
@@ -198,15 +208,20 @@ def spec_verify_u(p, q, d, u_acc, u_res, L=None):
     out = np.zeros(G + 1, dtype=np.int32)
     n = np.zeros(1, dtype=np.int32)
     mg = np.zeros(1, dtype=np.float64)
-    st = (L or lib()).orc_spec_verify_u(G, V, _ptr(p), _ptr(q), V, _ptr(d), _ptr(ua), _ptr(ur),
-                                        _ptr(out), _ptr(n), _ptr(mg))
+    if fixed:
+        st = (L or lib()).orc_spec_verify_fx_u(G, V, _ptr(p), _ptr(q), V, _ptr(d), _ptr(ua),
+                                               _ptr(ur), _ptr(out), _ptr(n))
+        mg[0] = np.inf
+    else:
+        st = (L or lib()).orc_spec_verify_u(G, V, _ptr(p), _ptr(q), V, _ptr(d), _ptr(ua),
+                                            _ptr(ur), _ptr(out), _ptr(n), _ptr(mg))
     return dict(status=st, tokens=out, n_accepted=int(n[0]), margin=float(mg[0]))
 
 
-def spec_verify(p, q, d, seed, offset, V=None, n_threads=1, L=None):
+def spec_verify(p, q, d, seed, offset, V=None, n_threads=1, L=None, fixed=False):
     """Batch with Philox uniforms.  p: float32 [B, G+1, ld], q: float32
     [B, G, ld], d: int32 [B, G]; seed, offset: uint64 [B]; V <= ld (default
-    ld)."""
+    ld).  fixed: the labelled fixed-point variant (margin = inf)."""
     p = np.ascontiguousarray(p, dtype=np.float32)
     B, G1, ld = p.shape
     G = G1 - 1
@@ -220,7 +235,8 @@ def spec_verify(p, q, d, seed, offset, V=None, n_threads=1, L=None):
     st = np.zeros(B, dtype=np.int32)
     mg = np.zeros(B, dtype=np.float64)
     (L or lib()).orc_spec_verify(B, G, V, _ptr(p), _ptr(q), ld, _ptr(d), _ptr(s), _ptr(o),
-                                 _ptr(out), _ptr(n), _ptr(st), _ptr(mg), int(n_threads))
+                                 _ptr(out), _ptr(n), _ptr(st), _ptr(mg), int(bool(fixed)),
+                                 int(n_threads))
     return dict(status=st, tokens=out, n_accepted=n, margin=mg)
 
 

@@ -399,71 +399,93 @@ int orc_row_stats(const void* row, int dtype, int V, const uint32_t* mask_row,
 
 static int prob_ok(float v) { return !isnan(v) && v >= 0.0f && v <= 1.0f; }
 
+/* Compensated (Neumaier) running sum: the result is the exact sum rounded
+   once, up to a relative error of about 2^-106 for the sums taken here. */
+typedef struct {
+  double s, c;
+} nsum;
+static void nsum_add(nsum* a, double x) {
+  double t = a->s + x;
+  if (fabs(a->s) >= fabs(x)) a->c += (a->s - t) + x;
+  else a->c += (x - t) + a->s;
+  a->s = t;
+}
+static double nsum_val(const nsum* a) { return a->s + a->c; }
+
+/* The checks and acceptance tests both variants share: returns the position
+   j of the draw (G when every draft is accepted) or -1 for ORC_INVALID. */
+static int spec_accept(int G, int V, const float* p, const float* q, int64_t ld, const int32_t* d,
+                       const double* u_acc) {
+  for (int i = 0; i < G; ++i) {
+    if (d[i] < 0 || d[i] >= V) return -1;
+    if (!prob_ok(p[(size_t)i * ld + d[i]]) || !prob_ok(q[(size_t)i * ld + d[i]])) return -1;
+  }
+  /* acceptance tests in order; u * q < p is exact in double (24 x 24 bits) */
+  int j = G;
+  for (int i = 0; i < G; ++i) {
+    const double a = (double)p[(size_t)i * ld + d[i]];
+    const double b = (double)q[(size_t)i * ld + d[i]];
+    if (u_acc[i] * b < a) continue;
+    j = i;
+    break;
+  }
+  return j;
+}
+/* The rows the draw at position j reads: p_j, and q_j after a rejection
+   (NULL after G acceptances); 0 when one of their values is not a
+   probability. */
+static int spec_rows(int j, int G, int V, const float* p, const float* q, int64_t ld,
+                     const float** pr, const float** qr) {
+  *pr = p + (size_t)j * ld;
+  *qr = (j < G) ? q + (size_t)j * ld : NULL;
+  for (int x = 0; x < V; ++x)
+    if (!prob_ok((*pr)[x]) || (*qr && !prob_ok((*qr)[x]))) return 0;
+  return 1;
+}
+/* Residual weight of id x over the reals: max(0, p(x) - q(x)), or p(x). */
+static double spec_res(const float* pr, const float* qr, int x) {
+  const double r = qr ? (double)pr[x] - (double)qr[x] : (double)pr[x];
+  return r > 0.0 ? r : 0.0;
+}
+
 int orc_spec_verify_u(int G, int V, const float* p, const float* q, int64_t ld,
                       const int32_t* d, const double* u_acc, const double* u_res,
                       int32_t* out_tokens, int32_t* n_acc, double* margin) {
   for (int i = 0; i <= G; ++i) out_tokens[i] = -1;
   *n_acc = 0;
   *margin = INFINITY;
-  /* every draft token and the two probabilities the test reads at it */
-  for (int i = 0; i < G; ++i) {
-    if (d[i] < 0 || d[i] >= V) return ORC_INVALID;
-    if (!prob_ok(p[(size_t)i * ld + d[i]]) || !prob_ok(q[(size_t)i * ld + d[i]]))
-      return ORC_INVALID;
-  }
-  /* acceptance tests in order; u * q < p is exact in double (24 x 24 bits) */
-  int j = G;
-  for (int i = 0; i < G; ++i) {
-    double a = (double)p[(size_t)i * ld + d[i]];
-    double b = (double)q[(size_t)i * ld + d[i]];
-    if (u_acc[i] * b < a) continue;
-    j = i;
-    break;
-  }
+  const int j = spec_accept(G, V, p, q, ld, d, u_acc);
+  if (j < 0) return ORC_INVALID;
   /* the drawn position: residual max(0, p_j - q_j) after a rejection, the
-     target row p_G after G acceptances.  The draw is an integer decision
-     taken from floating-point weights, so it is taken in the library's
-     stated precision: the residual is the binary32 difference, and each
-     weight is held as the integer floor(w * 2^42); sums and prefixes of
-     these are exact. */
-  const float* pr = p + (size_t)j * ld;
-  const float* qr = (j < G) ? q + (size_t)j * ld : NULL;
-  uint64_t* w = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(V > 0 ? V : 1));
-  if (!w) return ORC_INVALID;
-  uint64_t S = 0;
-  for (int x = 0; x < V; ++x) {
-    if (!prob_ok(pr[x]) || (qr && !prob_ok(qr[x]))) {
-      free(w);
-      return ORC_INVALID;
-    }
-    float r = qr ? pr[x] - qr[x] : pr[x];
-    if (!(r > 0.0f)) r = 0.0f;
-    w[x] = (uint64_t)floor(ldexp((double)r, 42));
-    S += w[x];
-  }
-  if (S == 0) {
-    free(w);
-    return ORC_EMPTY;
-  }
+     target row p_G after G acceptances; the weights are real numbers (the
+     difference of the two binary32 values, in double), their total and the
+     prefixes compensated sums */
+  const float *pr, *qr;
+  if (!spec_rows(j, G, V, p, q, ld, &pr, &qr)) return ORC_INVALID;
+  nsum S = {0.0, 0.0};
+  for (int x = 0; x < V; ++x) nsum_add(&S, spec_res(pr, qr, x));
+  const double St = nsum_val(&S);
+  if (!(St > 0.0)) return ORC_EMPTY;
   /* inverse CDF in id order: the first id whose cumulative weight exceeds
-     u * S, u = k * 2^-24; with integer prefixes P, P > u * S iff
-     P > floor(k * S / 2^24) */
-  const uint64_t k = (uint64_t)ldexp(u_res[j], 24);
-  const uint64_t T = (uint64_t)(((unsigned __int128)S * k) >> 24);
-  const double Tr = u_res[j] * (double)S;
-  int tok = -1;
-  uint64_t cum = 0;
+     u * S; the margin is the distance of u * S to the nearest prefix that
+     separates two candidates, over S */
+  const double t = u_res[j] * St;
+  int tok = -1, last = -1;
   double best = INFINITY;
+  nsum cum = {0.0, 0.0};
   for (int x = 0; x < V; ++x) {
-    if (w[x] == 0) continue;
-    cum += w[x];
-    if (tok < 0 && cum > T) tok = x;
-    if (cum < S) {  /* a switch point between two candidates */
-      double dist = fabs((double)cum - Tr) / (double)S;
+    const double r = spec_res(pr, qr, x);
+    if (!(r > 0.0)) continue;
+    last = x;
+    nsum_add(&cum, r);
+    const double c = nsum_val(&cum);
+    if (tok < 0 && c > t) tok = x;
+    if (c < St) {
+      const double dist = fabs(c - t) / St;
       if (dist < best) best = dist;
     }
   }
-  free(w);
+  if (tok < 0) tok = last; /* u * S rounds up to S: the last candidate */
   for (int i = 0; i < j; ++i) out_tokens[i] = d[i];
   out_tokens[j] = tok;
   *n_acc = j;
@@ -471,30 +493,74 @@ int orc_spec_verify_u(int G, int V, const float* p, const float* q, int64_t ld,
   return ORC_OK;
 }
 
+int orc_spec_verify_fx_u(int G, int V, const float* p, const float* q, int64_t ld,
+                         const int32_t* d, const double* u_acc, const double* u_res,
+                         int32_t* out_tokens, int32_t* n_acc) {
+  for (int i = 0; i <= G; ++i) out_tokens[i] = -1;
+  *n_acc = 0;
+  const int j = spec_accept(G, V, p, q, ld, d, u_acc);
+  if (j < 0) return ORC_INVALID;
+  /* the residual as the binary32 difference, each weight the integer
+     floor(w * 2^42); sums and prefixes of these are exact */
+  const float *pr, *qr;
+  if (!spec_rows(j, G, V, p, q, ld, &pr, &qr)) return ORC_INVALID;
+  uint64_t S = 0;
+  for (int x = 0; x < V; ++x) {
+    float r = qr ? pr[x] - qr[x] : pr[x];
+    if (!(r > 0.0f)) r = 0.0f;
+    S += (uint64_t)floor(ldexp((double)r, 42));
+  }
+  if (S == 0) return ORC_EMPTY;
+  /* with integer prefixes P, P > u * S iff P > floor(k * S / 2^24), u = k 2^-24 */
+  const uint64_t k = (uint64_t)ldexp(u_res[j], 24);
+  const uint64_t T = (uint64_t)(((unsigned __int128)S * k) >> 24);
+  int tok = -1;
+  uint64_t cum = 0;
+  for (int x = 0; x < V && tok < 0; ++x) {
+    float r = qr ? pr[x] - qr[x] : pr[x];
+    if (!(r > 0.0f)) continue;
+    cum += (uint64_t)floor(ldexp((double)r, 42));
+    if (cum > T) tok = x;
+  }
+  for (int i = 0; i < j; ++i) out_tokens[i] = d[i];
+  out_tokens[j] = tok;
+  *n_acc = j;
+  return ORC_OK;
+}
+
+static void spec_uniforms(int G, uint64_t seed, uint64_t offset, double* ua, double* ur) {
+  for (int i = 0; i <= G; ++i) {
+    uint64_t c = offset + (uint64_t)i;
+    uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    if (i < G) ua[i] = (double)(out[0] >> 8) * (1.0 / 16777216.0);
+    ur[i] = (double)(out[1] >> 8) * (1.0 / 16777216.0);
+  }
+}
+
 int orc_spec_verify(int B, int G, int V, const float* p, const float* q, int64_t ld,
                     const int32_t* d, const uint64_t* seed, const uint64_t* offset,
                     int32_t* out_tokens, int32_t* n_acc, int32_t* status, double* margin,
-                    int n_threads) {
+                    int fixed, int n_threads) {
   if (n_threads < 1) n_threads = 1;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
 #endif
   for (int s = 0; s < B; ++s) {
     double ua[64], ur[65];
-    for (int i = 0; i <= G; ++i) {
-      uint64_t c = offset[s] + (uint64_t)i;
-      uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
-      uint32_t key[2] = {(uint32_t)seed[s], (uint32_t)(seed[s] >> 32)};
-      uint32_t out[4];
-      orc_philox4x32_10(ctr, key, out);
-      if (i < G) ua[i] = (double)(out[0] >> 8) * (1.0 / 16777216.0);
-      ur[i] = (double)(out[1] >> 8) * (1.0 / 16777216.0);
-    }
+    spec_uniforms(G, seed[s], offset[s], ua, ur);
     int32_t* ot = out_tokens + (size_t)s * (size_t)(G + 1);
-    status[s] = orc_spec_verify_u(G, V, p + (size_t)s * (size_t)(G + 1) * (size_t)ld,
-                                  G ? q + (size_t)s * (size_t)G * (size_t)ld : NULL, ld,
-                                  d + (size_t)s * (size_t)G, ua, ur, ot, &n_acc[s],
-                                  &margin[s]);
+    const float* ps = p + (size_t)s * (size_t)(G + 1) * (size_t)ld;
+    const float* qs = G ? q + (size_t)s * (size_t)G * (size_t)ld : NULL;
+    const int32_t* ds = d + (size_t)s * (size_t)G;
+    if (fixed) {
+      status[s] = orc_spec_verify_fx_u(G, V, ps, qs, ld, ds, ua, ur, ot, &n_acc[s]);
+      margin[s] = INFINITY;
+    } else {
+      status[s] = orc_spec_verify_u(G, V, ps, qs, ld, ds, ua, ur, ot, &n_acc[s], &margin[s]);
+    }
     if (status[s] != ORC_OK) {
       for (int i = 0; i <= G; ++i) ot[i] = -1;
       n_acc[s] = 0;

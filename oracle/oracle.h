@@ -94,10 +94,9 @@ int orc_row_stats(const void* logits_row, int dtype, int V, const uint32_t* mask
  * with probability min(1, p/q)); at the first rejection draw the token from
  * norm(max(0, p_i - q_i)) with u_res[i] and stop; if all G are accepted,
  * draw one more token from p_G with u_res[G].  A draw is the inverse CDF in
- * token-id order: the first id whose cumulative weight exceeds u * S.  As
- * this integer decision is taken from floating-point weights, it is taken in
- * the precision the library states: the residual is the binary32 difference
- * p - q, each weight is the integer floor(w * 2^42), and u = k * 2^-24.
+ * token-id order: the first id whose cumulative weight exceeds u * S, over
+ * the reals: the residual is p - q of the given binary32 values, taken in
+ * double, S and the prefixes are compensated sums, and u = k * 2^-24.
  *   p       : [G+1] rows of V floats, row stride ld
  *   q       : [G] rows of V floats, row stride ld (NULL when G == 0)
  *   u_acc   : [G] uniforms in [0,1); u_res: [G+1] uniforms in [0,1)
@@ -114,16 +113,29 @@ int orc_spec_verify_u(int G, int V, const float* p, const float* q, int64_t ld,
                       int32_t* out_tokens, int32_t* n_acc, double* margin);
 
 /*
+ * A second, labelled variant (not the definition): the same rule with the
+ * draw taken in the precision the CUDA library states for its integer
+ * decision -- the residual as the binary32 difference p - q, each weight the
+ * integer floor(w * 2^42), the target floor(k * S / 2^24).  It differs from
+ * orc_spec_verify_u only where u * S lies within the weights' rounding of a
+ * switch point.  No margin output.
+ */
+int orc_spec_verify_fx_u(int G, int V, const float* p, const float* q, int64_t ld,
+                         const int32_t* d, const double* u_acc, const double* u_res,
+                         int32_t* out_tokens, int32_t* n_acc);
+
+/*
  * Batch of B sequences with Philox4x32-10 uniforms: for draft position i
  * (i = 0..G) the block at key (lo32 seed[s], hi32 seed[s]) and counter
  * offset[s] + i gives u_acc[i] = (word0 >> 8) * 2^-24 and
  * u_res[i] = (word1 >> 8) * 2^-24.  p: [B][G+1][ld], q: [B][G][ld],
- * d: [B][G], out_tokens: [B][G+1].
+ * d: [B][G], out_tokens: [B][G+1].  fixed = 0: orc_spec_verify_u (the
+ * definition); fixed = 1: orc_spec_verify_fx_u (margin set to infinity).
  */
 int orc_spec_verify(int B, int G, int V, const float* p, const float* q, int64_t ld,
                     const int32_t* d, const uint64_t* seed, const uint64_t* offset,
                     int32_t* out_tokens, int32_t* n_acc, int32_t* status, double* margin,
-                    int n_threads);
+                    int fixed, int n_threads);
 
 /* float -> bfloat16 / binary16 with round-to-nearest-even (NaN stays NaN,
  * overflow gives infinity). */

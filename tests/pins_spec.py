@@ -224,5 +224,30 @@ def check_spec_philox_frequencies(L=None, n=60000):
     assert abs(acc - alpha) <= 5 * np.sqrt(alpha * (1 - alpha) / n), (acc, alpha)
 
 
+def check_spec_fx_agrees(L=None, n=300):
+    """The labelled fixed-point variant takes the same decisions as the rule
+    over the reals wherever u * S lies more than 1e-6 of S from a switch point
+    (its weights are floor(w * 2^42) of binary32 differences: together they
+    move a prefix by far less than that), and nearly every draw is that far."""
+    rng = np.random.Generator(np.random.PCG64(29))
+    far = 0
+    for t in range(n):
+        V = int(rng.choice([5, 60, 700, 5000]))
+        G = int(rng.integers(0, 4))
+        p = np.stack([_dist(rng, V, int(rng.integers(1, V + 1))) for _ in range(G + 1)])
+        q = np.stack([_dist(rng, V, int(rng.integers(1, V + 1))) for _ in range(G)]) if G else None
+        d = [int(rng.choice(V, p=q[i].astype(np.float64) / q[i].sum())) for i in range(G)]
+        ua = rng.integers(0, GRID, size=G) / GRID
+        ur = rng.integers(0, GRID, size=G + 1) / GRID
+        qq = q if G else np.zeros((0, V), np.float32)
+        r = oracle.spec_verify_u(p, qq, d, ua, ur, L=L)
+        f = oracle.spec_verify_u(p, qq, d, ua, ur, L=L, fixed=True)
+        assert r["status"] == f["status"] and r["n_accepted"] == f["n_accepted"], (t, r, f)
+        if r["status"] == 0 and r["margin"] > 1e-6:
+            far += 1
+            assert list(r["tokens"]) == list(f["tokens"]), (t, r, f)
+    assert far >= 0.95 * n, far
+
+
 SPEC_CHECKS = [check_spec_special_cases, check_spec_status, check_spec_output_law,
-               check_spec_philox_frequencies]
+               check_spec_philox_frequencies, check_spec_fx_agrees]

@@ -1,9 +1,14 @@
 """Speculative-decoding verification: the CUDA path (through the C ABI)
-against the CPU oracle, sequence by sequence.  The accept / reject decisions
-and the drawn tokens are integer results taken in the precision the library
-states (exact double products for the acceptance tests, integer weights
-floor(w * 2^42) for the draw), so the comparison is exact: statuses, accepted
-counts and every output token."""
+against the CPU oracle, sequence by sequence.
+
+The oracle is the rule over the reals (lecture notes, section 5.2): residual
+max(0, p - q) in double, compensated sums.  Statuses and accepted counts are
+exact (the acceptance test u * q < p is exact in double on both sides).  The
+drawn token must equal the oracle's wherever u * S lies more than 1e-6 of S
+from a switch point of the draw; the sequences closer than that are counted,
+reported and bounded.  A second, labelled check compares every token with the
+oracle's fixed-point variant, which takes the draw in the integer precision
+the library states (floor(w * 2^42) of binary32 differences)."""
 import numpy as np
 import pytest
 import torch
@@ -26,11 +31,14 @@ def run_both(c, V=None):
     g = s.spec_verify(p, q, d, c["seed"].to(dev), c["offset"].to(dev), V=V)
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in g.items()}
-    r = oracle.spec_verify(c["p"].numpy(), c["q"].numpy() if G else None,
-                           c["d"].numpy() if G else None, c["seed"].numpy().view(np.uint64),
-                           c["offset"].numpy().view(np.uint64), V=V,
-                           n_threads=oracle.host_cores())
+    args = (c["p"].numpy(), c["q"].numpy() if G else None, c["d"].numpy() if G else None,
+            c["seed"].numpy().view(np.uint64), c["offset"].numpy().view(np.uint64))
+    r = oracle.spec_verify(*args, V=V, n_threads=oracle.host_cores())
+    r["fixed"] = oracle.spec_verify(*args, V=V, n_threads=oracle.host_cores(), fixed=True)
     return g, r
+
+
+MARGIN = 1e-6
 
 
 def compare(g, r):
@@ -39,8 +47,16 @@ def compare(g, r):
     bad = np.nonzero(g["n_accepted"] != r["n_accepted"])[0]
     assert bad.size == 0, ("n_accepted", bad[:8], g["n_accepted"][bad[:8]],
                            r["n_accepted"][bad[:8]])
-    bad = np.nonzero((g["tokens"] != r["tokens"]).any(axis=1))[0]
+    far = r["margin"] > MARGIN
+    bad = np.nonzero(far & (g["tokens"] != r["tokens"]).any(axis=1))[0]
     assert bad.size == 0, ("tokens", bad[:8], g["tokens"][bad[:4]], r["tokens"][bad[:4]])
+    near = int((~far & (r["status"] == 0)).sum())
+    print(f"spec_verify: {near} of {len(far)} sequences within {MARGIN:g} of a switch point")
+    assert near <= 0.1 * len(far) + 2, near
+    f = r["fixed"]
+    bad = np.nonzero((g["tokens"] != f["tokens"]).any(axis=1))[0]
+    assert bad.size == 0, ("tokens vs fixed-point variant", bad[:8])
+    return near
 
 
 @pytest.mark.parametrize("B,G,V", [(32, 4, 1000), (16, 1, 5), (8, 0, 300), (20, 31, 2000),

@@ -49,23 +49,24 @@ MUTATIONS = [
      "if (u_acc[i] * b > a) continue;"),
     ("verify: accept when u*q <= p", "if (u_acc[i] * b < a) continue;",
      "if (u_acc[i] * b <= a) continue;"),
-    ("verify: residual without max(0, .)", "if (!(r > 0.0f)) r = 0.0f;", "r = fabsf(r);"),
-    ("verify: residual q - p", "float r = qr ? pr[x] - qr[x] : pr[x];",
-     "float r = qr ? qr[x] - pr[x] : pr[x];"),
+    ("verify: residual without max(0, .)", "return r > 0.0 ? r : 0.0;", "return fabs(r);"),
+    ("verify: residual q - p", "const double r = qr ? (double)pr[x] - (double)qr[x] : (double)pr[x];",
+     "const double r = qr ? (double)qr[x] - (double)pr[x] : (double)pr[x];"),
     ("verify: no stop at the first rejection", "    j = i;\n    break;", "    j = i;"),
-    ("verify: bonus drawn from position 0", "const float* pr = p + (size_t)j * ld;",
-     "const float* pr = p + (size_t)(j < G ? j : 0) * ld;"),
-    ("verify: draw uses position 0's uniform",
-     "const uint64_t k = (uint64_t)ldexp(u_res[j], 24);",
-     "const uint64_t k = (uint64_t)ldexp(u_res[0], 24);"),
-    ("verify: draw takes cum >= u*S", "if (tok < 0 && cum > T) tok = x;",
-     "if (tok < 0 && cum >= T) tok = x;"),
+    ("verify: bonus drawn from position 0", "*pr = p + (size_t)j * ld;",
+     "*pr = p + (size_t)(j < G ? j : 0) * ld;"),
+    ("verify: draw uses position 0's uniform", "const double t = u_res[j] * St;",
+     "const double t = u_res[0] * St;"),
+    ("verify: draw takes cum >= u*S", "if (tok < 0 && c > t) tok = x;",
+     "if (tok < 0 && c >= t) tok = x;"),
     ("verify: residual draw reuses word 0", "ur[i] = (double)(out[1] >> 8) * (1.0 / 16777216.0);",
      "ur[i] = (double)(out[0] >> 8) * (1.0 / 16777216.0);"),
-    ("verify: token range check off by one", "if (d[i] < 0 || d[i] >= V) return ORC_INVALID;",
-     "if (d[i] < 0 || d[i] > V) return ORC_INVALID;"),
-    ("verify: drawn row not checked", "if (!prob_ok(pr[x]) || (qr && !prob_ok(qr[x]))) {",
-     "if (0) {"),
+    ("verify: token range check off by one", "if (d[i] < 0 || d[i] >= V) return -1;",
+     "if (d[i] < 0 || d[i] > V) return -1;"),
+    ("verify: drawn row not checked", "if (!prob_ok((*pr)[x]) || (*qr && !prob_ok((*qr)[x]))) return 0;",
+     ";"),
+    ("verify fx: weights in units of 2^-20", "S += (uint64_t)floor(ldexp((double)r, 42));",
+     "S += (uint64_t)floor(ldexp((double)r, 20));"),
     # repetition penalty (CTRL rule) and the float encoders
     ("penalty: every logit divided", "float y = (x > 0.0f) ? x / th : x * th;",
      "float y = x / th;"),
