@@ -28,7 +28,8 @@
  * before sampling), smp_gumbel_sample (a sort-free Gumbel-max draw over a
  * kept set, for comparison) and smp_spec_verify (speculative-decoding
  * verification against the kept sets' probabilities); smp_set_kernel
- * chooses between the two sampler kernels.
+ * chooses between the two sampler kernels and smp_set_wait_limit bounds the
+ * device-side waits.
  *
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers owned by the caller; the library
@@ -315,6 +316,19 @@ int smp_set_row_info(smp_handle h, int32_t* row_info);
  * thread-safe against concurrent calls on the same handle. */
 enum { SMP_KERNEL_BOARD = 0, SMP_KERNEL_SPLIT = 1 };
 int smp_set_kernel(smp_handle h, int kernel);
+
+/* Bound on each device-side wait of later calls on this handle, in SM clock
+ * cycles (cycles <= 0 restores the default, 4e9: about two seconds).  The
+ * waits are those for a staged copy to land and for other CTAs' chunks of a
+ * shared row.  A row whose wait runs out returns SMP_ERR_TIMEOUT with token
+ * -1 and count 0 (its kept mask and probabilities are unspecified); no token
+ * is ever substituted.  A CTA whose wait ran out stages nothing more in that
+ * launch (its later rows also return SMP_ERR_TIMEOUT) and, before it exits,
+ * waits for its copies still in flight with the default bound.  The next call
+ * starts clean.  Meant for tests and diagnostics: a very small bound makes
+ * rows time out on purpose.  Not thread-safe against concurrent calls on the
+ * same handle. */
+int smp_set_wait_limit(smp_handle h, long long cycles);
 
 /* Launch plan of a call with B rows of V tokens of `dtype` on this handle's
  * device: CTAs per row (the thread-block cluster), slice length (tokens per

@@ -18,7 +18,7 @@ _DTYPES = {torch.float32: SMP_F32, torch.bfloat16: SMP_BF16, torch.float16: SMP_
 EXPORTS = ("smp_create", "smp_destroy", "smp_topk_topp_mask", "smp_sample", "smp_argmax",
            "smp_sample_noalloc", "smp_sample_logprob", "smp_spec_verify",
            "smp_repetition_penalty", "smp_gumbel_sample", "smp_top_logprobs", "smp_set_row_info",
-           "smp_set_kernel", "smp_plan",
+           "smp_set_kernel", "smp_set_wait_limit", "smp_plan",
            "smp_status_string")
 
 
@@ -66,6 +66,7 @@ def load_library(path=None):
     L.smp_top_logprobs.argtypes = [P, P, I, I, I, ctypes.c_int64, P, P, P, P, I, P, P, P]
     L.smp_set_row_info.argtypes = [P, P]
     L.smp_set_kernel.argtypes = [P, ctypes.c_int]
+    L.smp_set_wait_limit.argtypes = [P, ctypes.c_longlong]
     L.smp_plan.argtypes = [P, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                            ctypes.POINTER(I)]
     L.smp_status_string.restype = ctypes.c_char_p
@@ -165,6 +166,10 @@ class Sampler:
         """smp_set_kernel: "board" (default) or "split" (bf16 / fp16 logits)."""
         code = {"board": SMP_KERNEL_BOARD, "split": SMP_KERNEL_SPLIT}[kernel]
         _check(self.lib.smp_set_kernel(self.h, code), "smp_set_kernel")
+
+    def set_wait_limit(self, cycles=0):
+        """smp_set_wait_limit: bound on each device wait (SM cycles; 0 = default)."""
+        _check(self.lib.smp_set_wait_limit(self.h, int(cycles)), "smp_set_wait_limit")
 
     def plan(self, dtype, V, B=1):
         out = [ctypes.c_int() for _ in range(4)]

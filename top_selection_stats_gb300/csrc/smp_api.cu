@@ -53,6 +53,7 @@ struct smp_ctx {
   float delta[DTAB];
   int32_t* row_info;
   int kernel;    // SMP_KERNEL_BOARD or SMP_KERNEL_SPLIT
+  long long wait_limit;  // SM clock cycles a bounded device wait may take
   Board* board;  // job board: zeroed at creation, reset by each launch's last CTA
 };
 
@@ -174,6 +175,7 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   const size_t es = (size_t)esize_of(dt);
   a.use_tma = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
   std::memcpy(a.delta, h->delta, sizeof(a.delta));
+  a.wait_limit = h->wait_limit;
 
   XPlan xp;
   if (h->kernel == SMP_KERNEL_SPLIT && split_plan(dt, B, V, h->sm_count, &xp)) {
@@ -203,7 +205,7 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
     r.wf = xp.wf;
     r.cap = xp.cap;
     r.aligned = a.use_tma;
-    r.wait_limit = WAIT_LIMIT;
+    r.wait_limit = h->wait_limit;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = dt == DT_BF16 ? split_launch_bf16(r, xp.smem, st)
                                         : split_launch_f16(r, xp.smem, st);
@@ -249,6 +251,7 @@ int smp_create(smp_handle* out, int device, int max_batch, int max_vocab) {
   h->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
   h->row_info = nullptr;
   h->kernel = SMP_KERNEL_BOARD;
+  h->wait_limit = WAIT_LIMIT;
   for (int i = 0; i < DTAB; ++i) {
     const double l2q = -24.0 + 0.25 * i;
     h->delta[i] = (float)upper_quantile(std::pow(2.0, l2q));
@@ -334,6 +337,12 @@ int smp_set_row_info(smp_handle h, int32_t* row_info) {
 int smp_set_kernel(smp_handle h, int kernel) {
   if (!h || (kernel != SMP_KERNEL_BOARD && kernel != SMP_KERNEL_SPLIT)) return SMP_ERR_INVALID_PARAM;
   h->kernel = kernel;
+  return SMP_OK;
+}
+
+int smp_set_wait_limit(smp_handle h, long long cycles) {
+  if (!h) return SMP_ERR_INVALID_PARAM;
+  h->wait_limit = cycles > 0 ? cycles : WAIT_LIMIT;
   return SMP_OK;
 }
 
@@ -513,6 +522,7 @@ int noalloc_setup(int dev, cudaStream_t st, smp_ctx** out) {
     for (int i = 0; i < DTAB; ++i) c.delta[i] = (float)upper_quantile(std::pow(2.0, -24.0 + 0.25 * i));
     c.row_info = nullptr;
     c.kernel = SMP_KERNEL_BOARD;
+    c.wait_limit = WAIT_LIMIT;
     c.board = board;
     noalloc_ready[dev] = true;
   }

@@ -56,7 +56,7 @@ struct JobHdr {
   uint32_t mxk;  // stream: largest key of the helpers' chunks
   int nleg, nf;
   float xa, xb;  // band: value thresholds of the bracket (above: x >= xa; band: xb <= x < xa)
-  int pad;
+  int bad;  // a helper's bounded wait expired on a chunk of this job
 };
 static_assert(sizeof(JobHdr) % 16 == 0, "job headers keep the board's arrays aligned");
 struct Board {
@@ -88,6 +88,7 @@ struct KArgs {
   int mode;
   int use_tma;  // rows are 16-byte aligned: stage them with bulk copies
   Board* board;  // job board (zeroed between launches), or null
+  long long wait_limit;  // SM clock cycles a bounded wait may take
   float delta[DTAB];
 };
 
@@ -104,7 +105,8 @@ struct Sh {
   int done[NSTAGE];           // warps done with each stage in the current pass
   int n;                      // list entries appended (may exceed CAP: overflow)
   int nf;                     // NaN / +inf seen in a legal slot
-  int timeout;                // a bounded wait expired
+  int timeout;                // a bounded wait expired: no copy is issued after it
+  int niss[NSTAGE];           // bulk copies issued into each stage (for the final drain)
   int gn;                     // gathered entries of the sampled segment
   int bi[8];                  // broadcast ints
   uint32_t bu[8];             // broadcast keys
@@ -587,6 +589,9 @@ __device__ __forceinline__ void issue_chunk(Ctx<DT>& X, int c, int s) {
   const int ne = min(CE, X.V - c * CE);
   const uint32_t bytes = X.use_tma ? (uint32_t)((ne * ES) & ~15) : 0u;
   uint64_t* bar = &X.sh->full[s];
+  // after an expired wait the stages' phases are unknown: nothing more goes out
+  if (X.sh->timeout) return;
+  ++X.sh->niss[s];
   // order earlier generic-proxy accesses of the stage before the async copy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_arrive_expect_tx(bar, bytes);
@@ -614,7 +619,7 @@ __device__ __forceinline__ const char* warp_wait(Ctx<DT>& X, int c) {
   const int s = c % NSTAGE;
   char* stage = X.ring + (size_t)s * STAGE_BYTES;
   const uint32_t par = (X.parity >> s) & 1u;
-  if (!mbar_wait_bounded(&X.sh->full[s], par, 4000000000ll)) X.sh->timeout = 1;
+  if (!X.sh->timeout && !mbar_wait_bounded(&X.sh->full[s], par, X.a->wait_limit)) X.sh->timeout = 1;
   X.parity ^= 1u << s;
   const int ne = min(CE, X.V - c * CE);
   const int nb = X.use_tma ? ((ne * ES) & ~15) / ES : 0;
@@ -654,7 +659,7 @@ __device__ __forceinline__ const char* ring_wait(Ctx<DT>& X, int c) {
   const int s = c % NSTAGE;
   char* stage = X.ring + (size_t)s * STAGE_BYTES;
   const uint32_t par = (X.parity >> s) & 1u;
-  if (!mbar_wait_bounded(&X.sh->full[s], par, 4000000000ll)) X.sh->timeout = 1;
+  if (!X.sh->timeout && !mbar_wait_bounded(&X.sh->full[s], par, X.a->wait_limit)) X.sh->timeout = 1;
   X.parity ^= 1u << s;
   const int ne = min(CE, X.V - c * CE);
   const int nb = X.use_tma ? ((ne * ES) & ~15) / ES : 0;
@@ -689,7 +694,8 @@ __device__ __forceinline__ void ring_drain(Ctx<DT>& X, int c) {
   for (int d = c + 1; d < X.nch && d < c + NSTAGE; ++d) {
     const int s = d % NSTAGE;
     const uint32_t par = (X.parity >> s) & 1u;
-    if (!mbar_wait_bounded(&X.sh->full[s], par, 4000000000ll)) X.sh->timeout = 1;
+    if (!X.sh->timeout && !mbar_wait_bounded(&X.sh->full[s], par, X.a->wait_limit))
+      X.sh->timeout = 1;
     X.parity ^= 1u << s;
   }
   __syncthreads();
@@ -706,7 +712,9 @@ struct RingIt {
   __device__ __forceinline__ const char* wait(Ctx<DT>& X) {
     constexpr int ES = ElemT<DT>::ES, CE = ElemT<DT>::CE, EPV = ElemT<DT>::EPV, VW = ElemT<DT>::VW;
     char* stage = X.ring + s * STAGE_BYTES;
-    if (!mbar_wait_bounded(&X.sh->full[s], (X.parity >> s) & 1u, 4000000000ll)) X.sh->timeout = 1;
+    if (!X.sh->timeout &&
+        !mbar_wait_bounded(&X.sh->full[s], (X.parity >> s) & 1u, X.a->wait_limit))
+      X.sh->timeout = 1;
     X.parity ^= 1u << s;
     if (c >= nfull) {
       // this warp's elements the bulk copy did not cover: plain loads, -inf past V

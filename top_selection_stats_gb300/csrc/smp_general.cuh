@@ -450,6 +450,7 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
     bd->lk[j][base + i] = X.lk[i];
     bd->li[j][base + i] = X.li[i];
   }
+  if (threadIdx.x == 0 && X.sh->timeout) atomicOr((int*)&H->bad, 1);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) atomicAdd((int*)&H->done, 1);

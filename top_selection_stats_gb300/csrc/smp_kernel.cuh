@@ -320,6 +320,7 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
   if (!bd) return;
   if (threadIdx.x == 0) atomicAdd(&bd->ctas_done, 1);
   const long long t0 = clock64();
+  const long long lim = X.a->wait_limit;
 #pragma unroll 1
   while (true) {
     if (threadIdx.x < 32) {
@@ -337,7 +338,10 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
       }
       const uint32_t m = __ballot_sync(0xffffffffu, open);
       int jj = -1, tt = -1, stop = 0;
-      if (lane == 0) {
+      // after an expired wait this CTA takes no more tasks
+      if (lane == 0 && X.sh->timeout) {
+        stop = 1;
+      } else if (lane == 0) {
         const int rot = (int)(blockIdx.x % 32u);
         const uint32_t rm = (m >> rot) | (rot ? (m << (32 - rot)) : 0u);
         uint32_t left = rm;
@@ -354,7 +358,7 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
         }
         __threadfence();  // the job's header is read after its ready flag
         if (jj < 0 && !m) {
-          if (vb->ctas_done >= (int)gridDim.x || clock64() - t0 > 4000000000ll) stop = 1;
+          if (vb->ctas_done >= (int)gridDim.x || clock64() - t0 > lim) stop = 1;
           else __nanosleep(200);
         }
         X.sh->bi[0] = jj;
@@ -381,7 +385,7 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
         H->ends = 0ull;  // reads as closed until the next publish
         H->ready = H->done = H->list_n = H->above_n = 0;
         H->mxk = 0u;
-        H->nleg = H->nf = 0;
+        H->nleg = H->nf = H->bad = 0;
       }
       bd->njobs = 0;
       bd->ctas_done = 0;
@@ -752,10 +756,21 @@ __global__ void __launch_bounds__(NT, 2) smp_kernel(const __grid_constant__ KArg
     fence_mbar_init();
     X.sh->timeout = 0;
     X.sh->n = 0;
+    for (int s = 0; s < NSTAGE; ++s) X.sh->niss[s] = 0;
   }
   __syncthreads();
   for (int row = blockIdx.x; row < a.B; row += gridDim.x) process_row(X, row);
   help_and_exit(X);
+  // After an expired wait: wait again, bounded by a fixed two seconds, for
+  // the last copy issued into each stage before the CTA exits (at most one
+  // per stage is outstanding, as nothing is issued after the expiry).
+  __syncthreads();
+  if (threadIdx.x == 0 && X.sh->timeout) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      const int n = X.sh->niss[s];
+      if (n > 0) mbar_wait_bounded(&X.sh->full[s], (uint32_t)(n - 1) & 1u, 4000000000ll);
+    }
+  }
 }
 
 }  // namespace smp

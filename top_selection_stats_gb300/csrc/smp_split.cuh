@@ -56,6 +56,7 @@ constexpr int XMAXC = 8;            // CTAs per row, at most (portable cluster s
 constexpr int XSW = 128;            // sampled bins each CTA publishes
 constexpr int XMAXWIN = 36;         // windows of one row, at most
 constexpr int XWT = XNS * XSB / 16;  // keys whose weight the resolution stores (2048)
+constexpr long long XDRAIN = 4000000000ll;  // cycles the drain after an expired wait may take
 constexpr int XBL = 1024;     // copies of the boundary value pass C lists for the id cut
 constexpr uint32_t XFM = 8;  // flat rows: the counted window reaches cap / XFM keys above the sample
 
@@ -1192,7 +1193,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     // flight into this CTA's ring before the CTA may exit
     if (timed_out && tid == 0)
       for (int s = max(0, issued - XNS); s < issued; ++s)
-        mbar_wait_bounded(&S.bar[s % XNS], (s / XNS) & 1, a.wait_limit);
+        mbar_wait_bounded(&S.bar[s % XNS], (s / XNS) & 1, XDRAIN);
     return;
   }
 
@@ -2089,7 +2090,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
         // wait (bounded again) for every copy still in flight into the ring
         for (int t = max(0, issued2 - XNS); t < issued2; ++t) {
           const int sl = t % XNS;
-          mbar_wait_bounded(&S.bar[sl], (((nst - sl + XNS - 1) / XNS) + t / XNS) & 1, a.wait_limit);
+          mbar_wait_bounded(&S.bar[sl], (((nst - sl + XNS - 1) / XNS) + t / XNS) & 1, XDRAIN);
         }
       }
       if (dtie && !tfail) {

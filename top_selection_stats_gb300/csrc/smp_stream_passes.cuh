@@ -391,13 +391,14 @@ __device__ bool wait_job(Ctx<DT>& X, int j, int n) {
     const long long t0 = clock64();
     int ok = 1;
     while (H->done < n) {
-      if (clock64() - t0 > 4000000000ll) {
+      if (clock64() - t0 > X.a->wait_limit) {
         ok = 0;
         break;
       }
       __nanosleep(100);
     }
     __threadfence();
+    if (ok && H->bad) ok = 0;  // a helper's chunk never landed
     X.sh->bi[0] = ok;
     if (!ok) X.sh->timeout = 1;
   }
@@ -478,6 +479,7 @@ __device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
   const float mx = bmax_f(nf ? -INFINITY : tmax, X.sh->rf[0]);
   nleg = bsum_i(nleg, X.sh->ri[0]);
   if (threadIdx.x == 0) {
+    if (X.sh->timeout) atomicOr((int*)&H->bad, 1);
     if (nf) atomicOr((int*)&H->nf, 1);
     else if (mx > -INFINITY) atomicMax((unsigned int*)&H->mxk, fkey(mx));
     if (nleg) atomicAdd((int*)&H->nleg, nleg);
