@@ -409,6 +409,120 @@ def run_verify(args, rank, world, local):
     smp.close()
 
 
+def run_decode_loop(args, rank, world, local):
+    """The repeated decode loop: args.steps steps (default 200) of the decode
+    workload, fresh logits generated for every step outside the timed region,
+    the Philox offsets advanced by the B blocks each step consumes, kept masks
+    returned.  Each step's launch is timed alone with CUDA events after an L2
+    flush; the line reports the per-step distribution and the loop total."""
+    from top_selection_stats_gb300 import Sampler, workloads
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    first = workloads.make(args.workload, step=0, device="cuda")
+    B, V = first["B"], first["V"]
+    esize = 4 if first["dtype"] == "f32" else 2
+    W = (V + 31) // 32
+    smp = Sampler(local, max_batch=max(B, 64), max_vocab=max(V, 1024))
+    smp.set_kernel(args.kernel)
+    tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    kmask = torch.empty((B, W), dtype=torch.int32, device=dev)
+    kcount = torch.empty(B, dtype=torch.int32, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    del first
+
+    def launch(c):
+        smp.sample(c["logits"], c["temperature"], c["top_k"], c["top_p"], c["seed"],
+                   c["offset"], bitmask=c["bitmask"], kept_mask=kmask, kept_count=kcount,
+                   tokens=tokens, status=status)
+
+    # warm-up on steps of their own (before step 0 of the loop)
+    for w in range(args.warmup):
+        launch(workloads.make(args.workload, step=args.steps + w, device="cuda"))
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(local) if rank == 0 else None
+    if clk:
+        clk.start()
+        time.sleep(0.3)
+    barrier(world)
+    per_step = []
+    bad = 0
+    for st in range(args.steps):
+        c = workloads.make(args.workload, step=st, device="cuda")
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch(c)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per_step.append(e0.elapsed_time(e1))
+        bad += int((status != 0).sum())
+    barrier(world)
+    clocks = clk.stop() if clk else None
+    total_ms = max_over_ranks(float(np.sum(per_step)), world, dev)
+    ms = np.asarray(per_step)
+    ms_per_step = total_ms / args.steps
+    value = B * world / (ms_per_step / 1000.0)
+
+    # end to end through the public API: each step's logits from pinned host
+    # memory, the tokens, statuses, counts and kept masks back to the host
+    e2e_steps = min(args.steps, 20)
+    host_logits = torch.empty((B, V), dtype=torch.float16 if esize == 2 else torch.float32)
+    host_logits = host_logits.pin_memory()
+    out = [torch.empty(B, dtype=torch.int32).pin_memory() for _ in range(3)]
+    out_mask = torch.empty((B, W), dtype=torch.int32).pin_memory()
+    dl = torch.empty((B, V), dtype=host_logits.dtype, device=dev)
+    e2e_s = 0.0
+    for st in range(e2e_steps):
+        c = workloads.make(args.workload, step=st, device="cuda")
+        host_logits.copy_(c["logits"])
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        dl.copy_(host_logits, non_blocking=True)
+        c2 = dict(c, logits=dl)
+        launch(c2)
+        for o, d in zip(out, (tokens, status, kcount)):
+            o.copy_(d, non_blocking=True)
+        out_mask.copy_(kmask, non_blocking=True)
+        stream.synchronize()
+        e2e_s += time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    e2e = {"value": B * world * e2e_steps / e2e_s, "unit": "rows/s",
+           "h2d_bytes_per_step": B * V * esize, "d2h_bytes_per_step": B * 12 + B * W * 4,
+           "steps": e2e_steps, "params": "on the device (per-row parameters do not change)"}
+    peak, peak_kind = measured_peaks()
+    alg_bytes = B * row_bytes(V, False, True, esize)
+    achieved = alg_bytes / (ms_per_step / 1000.0) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": ms_per_step}
+    if rank == 0:
+        line = {
+            "metric": f"rows/sec over a {args.steps}-step decode loop, B={B} V={V} "
+                      f"{workloads.WORKLOADS[args.workload]['dtype']}",
+            "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": workloads.WORKLOADS[args.workload]["dtype"],
+            "arith": "f32 weights, 64-bit fixed-point masses", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "V": V, "kernel": args.kernel,
+                       "kept_mask": True, "fresh_logits_per_step": True,
+                       "offset_advance": f"{B} Philox blocks per step (one per row)",
+                       "l2": "flushed (2x L2 written) before every step",
+                       "timing": "each step's launch alone, CUDA events on the launch stream",
+                       "per_step_ms": {"mean": float(ms.mean()), "p50": float(np.median(ms)),
+                                       "p90": float(np.percentile(ms, 90)),
+                                       "max": float(ms.max()), "min": float(ms.min())},
+                       "total_ms": total_ms, "error_rows": bad},
+            "roofline": roof, "cpu_baseline": None, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    smp.close()
+
+
 def run_ours(args, rank, world, local):
     from top_selection_stats_gb300 import Sampler, binding, workloads
     dev = torch.device("cuda", local)
@@ -747,7 +861,10 @@ def main():
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py --impl ours needs a CUDA GPU")
-        (run_verify if verify else run_ours)(args, rank, world, local)
+        if args.workload.startswith("decode"):
+            run_decode_loop(args, rank, world, local)
+        else:
+            (run_verify if verify else run_ours)(args, rank, world, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

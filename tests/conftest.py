@@ -28,3 +28,23 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Rows the GPU parity tests excluded at a boundary, per case (the
+    comparisons bound them; this prints the counts)."""
+    H = sys.modules.get("gpu_helpers")
+    if H is None or not getattr(H, "BOUNDARY_LOG", None):
+        return
+    agg = {}
+    for name, st in H.BOUNDARY_LOG:
+        a = agg.setdefault(name, dict(calls=0, rows=0, topp_boundary=0, cdf_boundary=0))
+        a["calls"] += 1
+        for k in ("rows", "topp_boundary", "cdf_boundary"):
+            a[k] += st.get(k, 0)
+    terminalreporter.write_sep("-", "rows excluded at a boundary (top-p mass within 1e-5 of p; "
+                                    "u within 1e-6 of a CDF boundary)")
+    for name, a in sorted(agg.items()):
+        terminalreporter.write_line(f"{name}: {a['calls']} comparisons, {a['rows']} rows, "
+                                    f"top-p boundary {a['topp_boundary']}, "
+                                    f"CDF boundary {a['cdf_boundary']}")

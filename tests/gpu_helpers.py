@@ -62,8 +62,23 @@ def gpu_run(case, mode="sample", want_probs=False, row_info=False):
     return res
 
 
+# Rows excluded from an exact comparison, per case: the top-p cumulative mass
+# within 1e-5 of p, or u within 1e-6 of a CDF boundary.  The tests' session
+# summary prints them (conftest); each comparison bounds them.
+BOUNDARY_LOG = []
+BOUNDARY_BOUND = 0.05  # at most this share of the compared rows, plus 3
+
+
+def record_boundaries(name, stats):
+    BOUNDARY_LOG.append((name, dict(stats)))
+    for k in ("topp_boundary", "cdf_boundary"):
+        assert stats[k] <= BOUNDARY_BOUND * stats["rows"] + 3, (name, k, stats)
+
+
 def compare(case, g, r, rows=None, mode="sample", check_probs=False):
-    """Assert the GPU result g matches oracle result r (oracle rows `rows`)."""
+    """Assert the GPU result g matches oracle result r (oracle rows `rows`).
+    Returns the counts of compared rows and of rows excluded at a boundary,
+    which are recorded and bounded."""
     sel = np.arange(case["B"]) if rows is None else np.asarray(rows)
     stats = dict(rows=len(sel), topp_boundary=0, cdf_boundary=0, token_checked=0)
     for i, b in enumerate(sel):
@@ -99,4 +114,5 @@ def compare(case, g, r, rows=None, mode="sample", check_probs=False):
             rel = np.abs(gp[kept] - rp[kept]) / rp[kept]
             assert rel.max(initial=0.0) <= PROB_RTOL, (case["name"], b, rel.max())
             assert not gp[rp == 0].any(), (case["name"], b)
+    record_boundaries(f"{case.get('name', '?')} [{mode}]", stats)
     return stats

@@ -80,15 +80,33 @@ def test_ties_masks_bf16_full():
     H.compare(case, g, r)
 
 
-def test_decode_f16_sampled_rows():
+def _rows_cpu(case, rows):
+    """The given rows of a (device) case, on the host, as a case of their own."""
+    idx = torch.as_tensor(rows, device=case["logits"].device)
+    out = {k: (v.index_select(0, idx.to(v.device)).cpu() if torch.is_tensor(v) else v)
+           for k, v in case.items()}
+    out["B"] = len(rows)
+    return out
+
+
+def test_decode_loop_f16():
+    """The repeated decode loop: 200 steps of 1024 x 256000 fp16 logits, fresh
+    each step, the Philox offsets advanced by the B blocks each step consumes,
+    kept masks returned.  Every row is compared at steps 0, 1, 2, 99 and 199,
+    32 random rows at every other step."""
     rng = np.random.default_rng(0)
-    for step in (0, 1, 199):
+    full = {0, 1, 2, 99, 199}
+    tot = dict(rows=0, topp_boundary=0, cdf_boundary=0, token_checked=0)
+    for step in range(200):
         case = workloads.make("decode1024x256000_f16", step=step, device="cuda")
-        case_cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in case.items()}
-        rows = np.sort(rng.choice(case["B"], size=48, replace=False))
-        r = H.oracle_run(case_cpu, rows=rows)
-        g = H.gpu_run(case_cpu, mode="sample")
-        H.compare(case_cpu, g, r, rows=rows)
+        B = case["B"]
+        rows = np.arange(B) if step in full else np.sort(rng.choice(B, size=32, replace=False))
+        g = H.gpu_run(case, mode="sample")
+        r = H.oracle_run(_rows_cpu(case, rows))
+        st = H.compare(case, g, r, rows=rows)
+        for k in tot:
+            tot[k] += st[k]
+    H.record_boundaries("decode1024x256000_f16 (200 steps)", tot)
 
 
 def test_argmax_matches_oracle():
