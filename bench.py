@@ -439,7 +439,8 @@ def run_decode_loop(args, rank, world, local):
 
     # warm-up on steps of their own (before step 0 of the loop)
     for w in range(args.warmup):
-        launch(workloads.make(args.workload, step=args.steps + w, device="cuda"))
+        launch(workloads.rank_shard(workloads.make(args.workload, step=args.steps + w,
+                                                   device="cuda"), rank, world))
     torch.cuda.synchronize(dev)
     clk = ClockSampler(local) if rank == 0 else None
     if clk:
@@ -449,7 +450,7 @@ def run_decode_loop(args, rank, world, local):
     per_step = []
     bad = 0
     for st in range(args.steps):
-        c = workloads.make(args.workload, step=st, device="cuda")
+        c = workloads.rank_shard(workloads.make(args.workload, step=st, device="cuda"), rank, world)
         flush.zero_()
         torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -477,7 +478,8 @@ def run_decode_loop(args, rank, world, local):
     dl = torch.empty((B, V), dtype=host_logits.dtype, device=dev)
     e2e_s = 0.0
     for st in range(e2e_steps):
-        c = workloads.make(args.workload, step=st, device="cuda")
+        c = workloads.rank_shard(workloads.make(args.workload, step=st, device="cuda"), rank,
+                                 world)
         host_logits.copy_(c["logits"])
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
@@ -527,7 +529,7 @@ def run_ours(args, rank, world, local):
     from top_selection_stats_gb300 import Sampler, binding, workloads
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    case = workloads.make(args.workload, device="cpu")
+    case = workloads.rank_shard(workloads.make(args.workload, device="cpu"), rank, world)
     B, V = case["B"], case["V"]
     esize = 4 if case["dtype"] == "f32" else 2
     bytes_logits = B * V * esize

@@ -71,3 +71,55 @@ def test_reference_arm_verification_workload():
         assert key in d, key
     assert d["impl"] == "reference" and d["unit"] == "sequences/s" and d["value"] > 0
     assert d["config"]["workload"] == "verify256x4x128256_f32"
+
+
+def _shard_worker(rank, world, port, q):
+    """One rank of the job: its shard of the workload (the helper bench.py
+    uses for --gpus N), run through the oracle, gathered over gloo."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import numpy as np
+    import torch
+    import gpu_helpers as H
+    from top_selection_stats_gb300 import workloads
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    case = workloads.random_case(41, 12, 3001, dtype="bf16", mask_frac=0.3)
+    shard = workloads.rank_shard(case, rank, world)
+    r = H.oracle_run(shard, threads=1)
+    mine = {k: torch.as_tensor(np.ascontiguousarray(r[k]).astype(np.int64))
+            for k in ("status", "token", "kept_count", "kept_mask")}
+    out = {}
+    for k, t in mine.items():
+        parts = [torch.empty_like(t) for _ in range(world)]
+        dist.all_gather(parts, t)
+        out[k] = torch.cat(parts).numpy()
+    if rank == 0:
+        q.put(out)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_row_shards_over_two_ranks_equal_the_single_rank_job():
+    """world_size 2 (gloo, CPU): each rank runs its contiguous shard; the
+    shards' results, concatenated, equal one rank running the whole job."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import gpu_helpers as H
+    from top_selection_stats_gb300 import workloads
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, 29631, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = q.get(timeout=300)
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    case = workloads.random_case(41, 12, 3001, dtype="bf16", mask_frac=0.3)
+    whole = H.oracle_run(workloads.global_job(case, 2), threads=1)
+    for k in ("status", "token", "kept_count", "kept_mask"):
+        assert np.array_equal(got[k], np.asarray(whole[k]).astype(np.int64)), k
+    # the two shards draw differently (their offsets differ)
+    assert not np.array_equal(got["token"][:12], got["token"][12:])

@@ -261,6 +261,33 @@ def verify_case(seed, B, G, V, ld=None, support=(50, 500), wide_frac=0.1, wide=(
                 offset=torch.arange(B, dtype=torch.int64) * (G + 1))
 
 
+def rank_shard(case, rank, world):
+    """Rank `rank`'s batch of a job run on `world` ranks: the job is `world`
+    consecutive copies of the case's B rows, copy r drawing with its Philox
+    offsets advanced by r * B (so no two ranks repeat a draw), and each rank's
+    batch is its own contiguous block of B rows -- one GPU's batch is its
+    shard, with no exchange between ranks.  world = 1 returns the case."""
+    if world <= 1:
+        return case
+    out = dict(case)
+    out["offset"] = case["offset"] + int(rank) * int(case["B"])
+    out["name"] = f"{case['name']}[shard {rank}/{world}]"
+    return out
+
+
+def global_job(case, world):
+    """The whole job that rank_shard splits: its `world` shards' rows,
+    concatenated in rank order (host tensors)."""
+    parts = [rank_shard(case, r, world) for r in range(world)]
+    out = dict(case)
+    for k, v in case.items():
+        if torch.is_tensor(v):
+            out[k] = torch.cat([p[k] for p in parts], dim=0)
+    out["B"] = case["B"] * world
+    out["name"] = f"{case['name']}[x{world}]"
+    return out
+
+
 def make_verify(name):
     cfg = VERIFY_WORKLOADS[name]
     out = verify_case(cfg["seed"], cfg["B"], cfg["G"], cfg["V"])
