@@ -172,7 +172,7 @@ def row_bytes(V, has_mask, write_mask, esize):
     return b
 
 
-def cpu_oracle_rate(case, rows):
+def cpu_oracle_rate(case, rows, threads=None):
     import oracle
     from top_selection_stats_gb300 import workloads
     x = workloads.bits_numpy(case["logits"])
@@ -180,7 +180,7 @@ def cpu_oracle_rate(case, rows):
     sel = np.arange(rows)
     p = {k: case[k].cpu().numpy()[sel] for k in ("temperature", "top_k", "top_p", "seed",
                                                  "offset")}
-    cores = oracle.host_cores()
+    cores = threads or oracle.host_cores()
     xs = np.ascontiguousarray(x[sel])
     bms = None if bm is None else np.ascontiguousarray(bm[sel])
     t0 = time.perf_counter()
@@ -189,12 +189,12 @@ def cpu_oracle_rate(case, rows):
     return rows / dt, cores, dt
 
 
-def cpu_oracle_sample(case, rows, min_seconds=10.0, max_passes=1000):
+def cpu_oracle_sample(case, rows, min_seconds=10.0, max_passes=1000, threads=None):
     """The oracle over the first `rows` rows, repeated until about min_seconds
     of host time have been spent; returns (rows/s, cores, passes, seconds)."""
     passes, total, cores = 0, 0.0, 1
     while passes < max_passes and (passes == 0 or total < min_seconds):
-        _, cores, dt = cpu_oracle_rate(case, rows)
+        _, cores, dt = cpu_oracle_rate(case, rows, threads)
         total += dt
         passes += 1
     return rows * passes / total, cores, passes, total
@@ -805,9 +805,14 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
         rows = min(B, args.cpu_rows)
         rate, cores, passes, secs = cpu_oracle_sample(case, rows)
+        rows1 = min(rows, 16)
+        rate1, _, passes1, secs1 = cpu_oracle_sample(case, rows1, min_seconds=5.0, threads=1)
         cpu = {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
                "sample": f"first {rows} rows of {args.workload}, {passes} passes "
-                         f"({secs:.1f} s wall)"}
+                         f"({secs:.1f} s wall)",
+               "single_thread": {"value": rate1, "unit": "rows/s", "cores": 1,
+                                 "sample": f"first {rows1} rows, {passes1} passes "
+                                           f"({secs1:.1f} s wall)"}}
 
     if rank == 0:
         line = {

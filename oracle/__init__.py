@@ -14,7 +14,6 @@ Parity status of each function (what pins it is listed in the tests):
                         front-end tests (greedy ties, masks, status codes).
   * orc_philox4x32_10 -- pinned against cuRAND's host Philox4x32-10 generator
                         where libcurand is present, and by uniformity tests.
-  * orc_row_stats    -- pinned against numpy on the same inputs.
   * orc_repetition_penalty, orc_f32_to_bf16, orc_f32_to_f16 -- pinned by
                         worked values of the CTRL rule, duplicates and padding
                         in the history, and the encoders against numpy / torch
@@ -89,8 +88,6 @@ def load(path):
     L.orc_gumbel_sample.restype = ctypes.c_int
     L.orc_gumbel_sample.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                     P, P, P, P, P, P, P, ctypes.c_int]
-    L.orc_row_stats.restype = ctypes.c_int
-    L.orc_row_stats.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
     return L
 
 
@@ -183,15 +180,6 @@ def run_batch(logits_bits, dtype, V, temperature=None, top_k=None, top_p=None, s
                            _ptr(kmask), _ptr(probs), _ptr(flags), _ptr(u), int(n_threads))
     return dict(status=status, token=token, kept_count=count, kept_mask=kmask, probs=probs,
                 flags=flags, u=u)
-
-
-def row_stats(logits_row_bits, dtype, V, temperature=1.0, mask_row=None):
-    arr = np.ascontiguousarray(logits_row_bits)
-    out = np.zeros(8, dtype=np.float64)
-    mr = None if mask_row is None else np.ascontiguousarray(mask_row, dtype=np.uint32)
-    lib().orc_row_stats(_ptr(arr), _DT[dtype], V, _ptr(mr), float(temperature), _ptr(out))
-    return dict(max=out[0], argmax=int(out[1]), n_legal=int(out[2]), mean=out[3], std=out[4],
-                logsumexp=out[5], nonfinite=bool(out[6]))
 
 
 def spec_verify_u(p, q, d, u_acc, u_res, L=None, fixed=False):

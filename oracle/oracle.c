@@ -351,43 +351,6 @@ int orc_batch(const void* logits, int dtype, int B, int V, int64_t ld,
   return 0;
 }
 
-int orc_row_stats(const void* row, int dtype, int V, const uint32_t* mask_row,
-                  float t, double out[8]) {
-  double mx = -INFINITY, s = 0.0, s2 = 0.0;
-  int arg = -1, n = 0, nonfinite = 0;
-  for (int i = 0; i < V; ++i) {
-    float xf = load_logit(row, dtype, i);
-    if (!mask_allows(mask_row, i) || (isinf(xf) && xf < 0)) continue;
-    if (isnan(xf) || isinf(xf)) { nonfinite = 1; continue; }
-    ++n;
-    if (xf > mx) { mx = xf; arg = i; }
-    s += xf;
-    s2 += (double)xf * (double)xf;
-  }
-  double mean = n ? s / n : 0.0;
-  double var = n ? s2 / n - mean * mean : 0.0;
-  double lse = -INFINITY;
-  if (n && t > 0.0f) {
-    double m = (double)((float)mx / t), acc = 0.0;
-    for (int i = 0; i < V; ++i) {
-      float xf = load_logit(row, dtype, i);
-      if (!mask_allows(mask_row, i) || isnan(xf) || isinf(xf)) continue;
-      float zf = xf / t;
-      acc += exp((double)zf - m);
-    }
-    lse = m + log(acc);
-  }
-  out[0] = mx;
-  out[1] = arg;
-  out[2] = n;
-  out[3] = mean;
-  out[4] = var > 0 ? sqrt(var) : 0.0;
-  out[5] = lse;
-  out[6] = nonfinite;
-  out[7] = 0.0;
-  return 0;
-}
-
 /* ---------------------------------------------------------------------- */
 /* Speculative-decoding verification, exact rule (lecture notes "Decoding: */
 /* Sampling, Beam Search and Speculative Decoding", section 5.2, after     */

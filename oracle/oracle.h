@@ -76,15 +76,6 @@ int orc_batch(const void* logits, int dtype, int B, int V, int64_t ld,
               int n_threads);
 
 /*
- * Row statistics over legal finite logits: max and its smallest id, count,
- * mean and standard deviation of x, logsumexp of z = fl32(x / T) (T > 0),
- * and whether a NaN / +inf sits in a legal slot.
- * out[8] = {max, argmax, n_legal, mean, std, logsumexp, nonfinite, 0}.
- */
-int orc_row_stats(const void* logits_row, int dtype, int V, const uint32_t* mask_row,
-                  float temperature, double out[8]);
-
-/*
  * Speculative-decoding verification with the exact accept / reject rule
  * (lecture notes "Decoding: Sampling, Beam Search and Speculative Decoding",
  * section 5.2, after Leviathan et al. 2023 and Chen et al. 2023).  One

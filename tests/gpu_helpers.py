@@ -64,15 +64,18 @@ def gpu_run(case, mode="sample", want_probs=False, row_info=False):
 
 # Rows excluded from an exact comparison, per case: the top-p cumulative mass
 # within 1e-5 of p, or u within 1e-6 of a CDF boundary.  The tests' session
-# summary prints them (conftest); each comparison bounds them.
+# summary prints them (conftest).  For the named workloads the counts are
+# bounded; the tie-grid and random edge cases (built to put masses on the
+# boundary) are recorded only.
 BOUNDARY_LOG = []
 BOUNDARY_BOUND = 0.05  # at most this share of the compared rows, plus 3
 
 
-def record_boundaries(name, stats):
+def record_boundaries(name, stats, bounded=False):
     BOUNDARY_LOG.append((name, dict(stats)))
-    for k in ("topp_boundary", "cdf_boundary"):
-        assert stats[k] <= BOUNDARY_BOUND * stats["rows"] + 3, (name, k, stats)
+    if bounded:
+        for k in ("topp_boundary", "cdf_boundary"):
+            assert stats[k] <= BOUNDARY_BOUND * stats["rows"] + 3, (name, k, stats)
 
 
 def compare(case, g, r, rows=None, mode="sample", check_probs=False):
@@ -114,5 +117,6 @@ def compare(case, g, r, rows=None, mode="sample", check_probs=False):
             rel = np.abs(gp[kept] - rp[kept]) / rp[kept]
             assert rel.max(initial=0.0) <= PROB_RTOL, (case["name"], b, rel.max())
             assert not gp[rp == 0].any(), (case["name"], b)
-    record_boundaries(f"{case.get('name', '?')} [{mode}]", stats)
+    record_boundaries(f"{case.get('name', '?')} [{mode}]", stats,
+                      bounded=case.get("name") in workloads.WORKLOADS)
     return stats

@@ -106,7 +106,29 @@ def test_decode_loop_f16():
         st = H.compare(case, g, r, rows=rows)
         for k in tot:
             tot[k] += st[k]
-    H.record_boundaries("decode1024x256000_f16 (200 steps)", tot)
+    H.record_boundaries("decode1024x256000_f16 (200 steps)", tot, bounded=True)
+
+
+def test_far_negative_logits_keep_the_sigma_path(kernel):
+    """A penalised decode input: 16 legal logits per row pushed to -60000.
+    The results still match the oracle, and on the board kernel the
+    sigma-truncated list still serves the rows it serves on the clean input
+    (the deviation estimate leaves far-negative values out)."""
+    case = workloads.make("decode1024x256000_f16", step=3, device="cuda", rows=64)
+    clean = H.gpu_run(case, mode="sample", row_info=True)
+    rng = np.random.default_rng(7)
+    x = case["logits"].clone()
+    for b in range(case["B"]):
+        ids = torch.as_tensor(rng.choice(case["V"], size=16, replace=False), device=x.device)
+        x[b, ids] = -60000.0
+    pen = dict(case, logits=x, name="decode_penalised")
+    g = H.gpu_run(pen, mode="sample", row_info=True)
+    r = H.oracle_run({k: (v.cpu() if torch.is_tensor(v) else v) for k, v in pen.items()})
+    H.compare(pen, g, r)
+    if kernel == "board":
+        n_clean = int((clean["row_info"][:, 0] == 3).sum())
+        n_pen = int((g["row_info"][:, 0] == 3).sum())
+        assert n_clean > 0 and n_pen >= n_clean - 2, (n_clean, n_pen)
 
 
 def test_argmax_matches_oracle():

@@ -44,8 +44,37 @@ __device__ __forceinline__ void chunk_stats(Ctx<DT>& X, const char* stage, float
   s2 = bsum_f(s2, X.sh->rf[2]);
   cnt = (int)n;
   mu = n > 0.f ? s1 / n : 0.f;
-  const float var = n > 0.f ? fmaxf(s2 / n - mu * mu, 0.f) : 0.f;
-  sd = sqrtf(var);
+  sd = sqrtf(n > 0.f ? fmaxf(s2 / n - mu * mu, 0.f) : 0.f);
+  // A few far-negative legal values (a penalised or suppressed token) would
+  // inflate the deviation and lift the threshold: up to two more passes over
+  // the staged chunk leave out the values more than 4 deviations below the
+  // mean (the upper tail, where the candidates are, is always kept).
+#pragma unroll 1
+  for (int rep = 0; rep < 2; ++rep) {
+    const float lo = mu - 4.f * sd;
+    float r1 = 0.f, r2 = 0.f, rn = 0.f;
+#pragma unroll 1
+    for (int it = 0; it < ITW; ++it) {
+      const uint4 r = load_vec(X, stage, 0, warp_vec<DT>(it));
+      float x[EPV];
+      unpack<DT>(r, x);
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) {
+        if (x[j] >= lo && x[j] < INFINITY) {
+          rn += 1.f;
+          r1 += x[j];
+          r2 += x[j] * x[j];
+        }
+      }
+    }
+    rn = bsum_f(rn, X.sh->rf[0]);
+    if (!(rn < n) || rn < 1.f) break;  // nothing left out: the estimate stands
+    r1 = bsum_f(r1, X.sh->rf[1]);
+    r2 = bsum_f(r2, X.sh->rf[2]);
+    n = rn;
+    mu = r1 / n;
+    sd = sqrtf(fmaxf(r2 / n - mu * mu, 0.f));
+  }
 }
 
 // t = mu + delta(q) * sd, delta(q) = Phi^-1(1 - q) interpolated from the host
