@@ -390,3 +390,6 @@ def test_top_logprobs_random_and_ties(dtype):
     ties = workloads.random_case(12, 32, 4096, dtype=dtype, grid=6, mask_frac=0.2,
                                  topks=(3, 40, 700, 4096), topps=(0.5, 0.9, 1.0))
     assert check_top_logprobs(ties, 32) > 0
+    # rows of 9001 tokens: not 16-byte aligned past row 0, and a partial last word
+    odd = workloads.random_case(5170 + len(dtype), 24, 9001, dtype=dtype, mask_frac=0.2)
+    assert check_top_logprobs(odd, 7) > 0

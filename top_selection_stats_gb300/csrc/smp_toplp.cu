@@ -9,12 +9,16 @@
 //     logprob_j = logprob_tok + (fl32(x_j / T) - fl32(x_tok / T)),
 // and the kept set's normaliser is never needed again.
 //
-// One cluster of up to 8 CTAs of 128 threads per row.  A warp keeps the 32
-// best (logit descending, id ascending) kept tokens it has seen as 64-bit
-// order keys, one per lane, sorted across the lanes; a batch of 32 new
-// candidates is merged only when one of them beats the warp's 32nd best (a
-// bitonic sort of the batch and a bitonic merge), which after the first
-// steps is rare.  The warps' lists, then the CTAs' lists (through
+// One cluster of up to 8 CTAs of 128 threads per row.  A warp reads 32 kept-
+// mask words at a time, one per lane (coalesced), so a lane owns 32
+// consecutive tokens; a lane whose word has a kept bit loads those 32 logits
+// as 16-byte vectors, all lanes' loads in flight together.  The warp keeps
+// the 32 best (logit descending, id ascending) kept tokens it has seen as
+// 64-bit order keys, one per lane, sorted across the lanes; unless some
+// lane's best new key beats the warp's 32nd best (after the first steps,
+// rare), the 32 tokens of each lane are skipped at once; otherwise batches of
+// 32 candidates (bit j of every lane) are merged (a bitonic sort of the batch
+// and a bitonic merge).  The warps' lists, then the CTAs' lists (through
 // distributed shared memory), are merged the same way.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -45,6 +49,7 @@ struct TopArgs {
   float* out_lp;      // [B][n]
   int B, V, W, n;
   int nc, seg;
+  int vec;  // rows 16-byte aligned: logits read as 16-byte vectors
 };
 
 // Order key: larger is better (larger logit, then smaller id); 0 = empty.
@@ -114,22 +119,73 @@ __global__ void __launch_bounds__(LT, 8) toplp_kernel(const TopArgs a) {
   const uint32_t* km = a.kept + (size_t)r * a.W;
   const bool live = a.tokens[r] >= 0;
 
-  // this warp's slab of the CTA's segment, 32 elements per step
+  // this CTA's segment (a multiple of 32 tokens), 32 mask words per warp step
+  constexpr int ES = DT == SMP_F32 ? 4 : 2;
+  constexpr int NV = 32 * ES / 16;  // 16-byte vectors per lane's 32 tokens
+  __shared__ unsigned long long tau;  // the best 32nd-best key any warp here holds
+  if (threadIdx.x == 0) tau = 0ull;
+  __syncthreads();
   uint64_t top = 0ull;
   if (live) {
     const int c0 = rank * a.seg, c1 = min(a.V, c0 + a.seg);
-    const int per = (c1 - c0 + LWARPS - 1) / LWARPS;
-    const int s0 = c0 + warp * per, s1 = min(c1, s0 + per);
+    const int w0 = c0 >> 5, w1 = (c1 + 31) >> 5;
 #pragma unroll 1
-    for (int i = s0; i < s1; i += 32) {
-      const int id = i + lane;
-      uint64_t k = 0ull;
-      if (id < s1 && ((__ldg(km + (id >> 5)) >> (id & 31)) & 1u)) {
-        const float x = load_logit<DT>(row, id);
-        if (x > -INFINITY && x < INFINITY) k = order_key(x, id);
+    for (int wb = w0 + warp * 32; wb < w1; wb += LWARPS * 32) {
+      const int w = wb + lane;
+      uint32_t bits = w < w1 ? __ldg(km + w) : 0u;
+      if (w == w1 - 1 && (c1 & 31)) bits &= (1u << (c1 & 31)) - 1u;  // ids >= c1 belong elsewhere
+      if (!__any_sync(0xffffffffu, bits != 0u)) continue;
+      // this lane's 32 tokens as order values (0: not kept or not finite)
+      uint32_t u[32];
+      if (a.vec && (w + 1) * 32 <= a.V) {  // a whole word of tokens inside the row
+        uint4 q[NV];
+        const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)w * 32 * ES);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) q[v] = bits ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t word = reinterpret_cast<const uint32_t*>(q)[j * ES / 4];
+          float x;
+          if constexpr (DT == SMP_F32) x = __uint_as_float(word);
+          else {
+            const unsigned short h = (unsigned short)((j & 1) ? (word >> 16) : (word & 0xffffu));
+            x = DT == SMP_BF16 ? __bfloat162float(__ushort_as_bfloat16(h))
+                               : __half2float(__ushort_as_half(h));
+          }
+          u[j] = (((bits >> j) & 1u) && x > -INFINITY && x < INFINITY)
+                     ? (uint32_t)(order_key(x, 0) >> 32) : 0u;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = ((bits >> j) & 1u) ? load_logit<DT>(row, w * 32 + j) : -INFINITY;
+          u[j] = (x > -INFINITY && x < INFINITY) ? (uint32_t)(order_key(x, 0) >> 32) : 0u;
+        }
       }
-      const uint64_t thr = __shfl_sync(0xffffffffu, top, 31);
-      if (__any_sync(0xffffffffu, k > thr)) top = warp_merge_top(top, k, lane);
+      // rounds: every lane offers its best token not yet offered; those above
+      // the threshold are merged; until no lane has one above it
+      uint32_t offered = 0u;
+#pragma unroll 1
+      while (true) {
+        uint64_t thr = __shfl_sync(0xffffffffu, top, 31);
+        const uint64_t tc = *reinterpret_cast<volatile unsigned long long*>(&tau);
+        thr = tc > thr ? tc : thr;
+        uint32_t bu = 0u;
+        int bj = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const bool take = !((offered >> j) & 1u) && u[j] > bu;  // the earliest of equals
+          bu = take ? u[j] : bu;
+          bj = take ? j : bj;
+        }
+        const uint64_t k = bu ? (((uint64_t)bu << 32) | (uint64_t)(0xffffffffu - (uint32_t)(w * 32 + bj)))
+                              : 0ull;
+        const bool sub = k > thr;
+        if (!__any_sync(0xffffffffu, sub)) break;
+        if (sub) offered |= 1u << bj;
+        top = warp_merge_top(top, sub ? k : 0ull, lane);
+        if (lane == 31 && top) atomicMax(&tau, (unsigned long long)top);
+      }
     }
   }
   wl[warp][lane] = top;
@@ -197,6 +253,8 @@ int toplp_enqueue(const void* logits, int dtype, int B, int V, long long ld, con
   nc = nc < 1 ? 1 : (nc > LMAXC ? LMAXC : nc);
   a.nc = nc;
   a.seg = ((V + nc * 32 - 1) / (nc * 32)) * 32;
+  const size_t es = dtype == SMP_F32 ? 4 : 2;
+  a.vec = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((size_t)ld * es) % 16 == 0) ? 1 : 0;
   if ((long long)B * nc > 0x7fffffffLL) return SMP_ERR_CAPACITY;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * nc));
