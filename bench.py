@@ -62,18 +62,39 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def profiled_traffic(workload, sources=KERNEL_SOURCES):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+TOPLP_SOURCES = ["top_selection_stats_gb300/csrc/smp_toplp.cu"]
+GUMBEL_SOURCES = ["top_selection_stats_gb300/csrc/" + f for f in ("smp_gumbel.cu", "smp_philox.cuh")]
+PENALTY_SOURCES = ["top_selection_stats_gb300/csrc/smp_penalty.cu"]
+
+
+def profiled_entry(key, sources=KERNEL_SOURCES):
+    """The committed ncu summary's entry for `key` (a workload, or
+    "kernel:workload"), if it was taken on the current kernel source; else
+    None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(workload)
+    e = d.get(key)
     if not e or e.get("kernel_source_sha") != kernel_source_hash(sources):
         return None
-    return e.get("dram_bytes_per_launch")
+    return e
+
+
+def profiled_traffic(workload, sources=KERNEL_SOURCES):
+    """DRAM bytes (read + write) per launch from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    e = profiled_entry(workload, sources)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+def passes_over_hbm(entry, logits_bytes):
+    """DRAM bytes read per launch over the logits' bytes (None without a
+    current capture)."""
+    if entry is None or not entry.get("dram_bytes_read_per_launch"):
+        return None
+    return entry["dram_bytes_read_per_launch"] / float(logits_bytes)
 
 
 class ClockSampler:
@@ -498,8 +519,11 @@ def run_decode_loop(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     alg_bytes = B * row_bytes(V, False, True, esize)
     achieved = alg_bytes / (ms_per_step / 1000.0) / 1e9
+    prof = profiled_entry(args.workload)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+            "frac": achieved / peak,
+            "traffic": None if prof is None else prof.get("dram_bytes_per_launch"),
+            "passes_over_hbm": passes_over_hbm(prof, B * V * esize), "peak_kind": peak_kind,
             "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": ms_per_step}
     if rank == 0:
         line = {
@@ -712,11 +736,14 @@ def run_ours(args, rank, world, local):
         pen_info = {"history_per_row": args.repetition_penalty, "kernel_us": 1000 * pen_ms,
                     "timed_theta": "1 (buffers penalised once with 1.1-1.3 before timing)",
                     "algorithmic_bytes": pen_bytes,
-                    "gbs": pen_bytes / (pen_ms / 1000.0) / 1e9}
+                    "gbs": pen_bytes / (pen_ms / 1000.0) / 1e9,
+                    "traffic": profiled_traffic("penalty:" + args.workload, PENALTY_SOURCES)}
     achieved = alg_bytes / (kern_ms / 1000.0) / 1e9
-    traffic = profiled_traffic(args.workload)
+    prof = profiled_entry(args.workload)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+            "frac": achieved / peak,
+            "traffic": None if prof is None else prof.get("dram_bytes_per_launch"),
+            "passes_over_hbm": passes_over_hbm(prof, bytes_logits), "peak_kind": peak_kind,
             "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kern_ms}
 
     toplp_info = None
@@ -751,7 +778,8 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize(dev)
         toplp_info = {"n": args.top_logprobs,
                       "kernel_us": 1000 * q0.elapsed_time(q1) / args.steps,
-                      "note": "one buffer (its kept masks in L2 between launches)"}
+                      "note": "one buffer (its kept masks in L2 between launches)",
+                      "traffic": profiled_traffic("toplp:" + args.workload, TOPLP_SOURCES)}
 
     gumbel_info = None
     if args.gumbel:
@@ -800,6 +828,7 @@ def run_ours(args, rank, world, local):
             torch.cuda.synchronize(dev)
             gumbel_info[name] = 1000 * q0.elapsed_time(q1) / args.steps
         gumbel_info["fused_smp_sample_us"] = 1000 * kern_ms
+        gumbel_info["traffic"] = profiled_traffic("gumbel:" + args.workload, GUMBEL_SOURCES)
 
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
