@@ -10,34 +10,40 @@
 // Layout on GB300.  The work is one pass over the logits (Qrita paper notes:
 // the full-vocabulary passes are the cost), so every row of a launch streams
 // at once: a row is split over C CTAs of one cluster (C chosen so that the
-// launch has at least two CTAs per SM), each CTA streams its slice through a
-// ring of four 8 KB bulk copies (cp.async.bulk + mbarrier, no multicast), and
-// the selection itself happens on the fly:
-//   sample   the first stage of each slice is also a sample: a coarse key
-//            histogram of two values per 16-byte vector, published to the
-//            cluster with the stage's maximum (one cluster barrier).  Every
-//            CTA then places the same top-k threshold `lo` (Qrita's sigma
-//            truncation, read as a quantile of the sample).
+// launch has at least two CTAs per SM), and each CTA streams its slice
+// through a ring of four 8 KB bulk copies (cp.async.bulk + mbarrier, no
+// multicast):
+//   sample   the first stage of a slice is also a sample: its maximum, and for
+//            top-k rows a fine key histogram, place this CTA's own candidate
+//            threshold `lo` (Qrita's sigma truncation, read as a quantile of
+//            the sample); no exchange is needed before the stream.
 //   stream   per vector: maximum and first id, -inf count, NaN / +inf check
 //            (packed bf16x2 / f16x2 max and min), the grammar mask, and by
-//            row class: top-k rows append values >= lo to a candidate list
-//            and count them in a window histogram with one bin per 16-bit
-//            key; keep-all rows accumulate per-(stage, warp) masses and
-//            write their kept-mask words.
-//   resolve  one cluster barrier; every CTA reads all CTAs' window histograms
-//            (distributed shared memory) and finds, identically, the k-th
-//            largest key with its tie quota, the kept set's mass and the
-//            top-p boundary key with the number of its copies kept (a key's
-//            mass is its count times its weight).  One more barrier exchanges
-//            the mass each CTA keeps; the CTA holding the draw finds the
-//            token from its candidates in id order.
-// Rows the stream cannot settle (flat top-p rows, a sample that misplaced the
-// threshold, keep-all rows whose maximum lies far above the sample's) take
-// the exact window search: key windows histogrammed over the slice re-read
-// from global memory (L2), sliding down until both boundaries are inside.
-// Masses that decide kept sets are fixed-point integers (units of 2^-40 of
-// the largest weight), so sums, prefixes and decisions are exact and equal in
-// every CTA.
+//            row class: top-k rows mark the vectors holding a value >= lo
+//            (their candidates are listed after the stream from L2); flat
+//            top-p rows count every key of a 2048-key window below the
+//            sample's maximum (one 32-bit counter per 16-bit key) and sum an
+//            approximate row mass; keep-all rows accumulate per-(stage, warp)
+//            masses and write their kept-mask words.
+//   resolve  one cluster barrier exchanges the statistics; every CTA reads
+//            all CTAs' per-key counts (distributed shared memory) and finds,
+//            identically, the k-th largest key with its tie quota, the kept
+//            set's mass and the top-p boundary key with the number of its
+//            copies kept (a key's mass is its count times its weight; each
+//            CTA's share of the boundary copies follows from the CTAs' rank
+//            order, earliest ids first).  A second barrier exchanges the
+//            mass each CTA keeps; the CTA holding the draw finds the token.
+//   outputs  from the candidate list when it holds the kept set; otherwise a
+//            second pass streams the slice through the ring again: mask bits
+//            by packed compares, the drawing CTA's per-(stage, warp) kept
+//            masses from a table of the kept keys' weights, and boundary
+//            copies listed during the pass when their id cut is still open.
+// Rows the stream cannot settle (a list or window that misses the boundary,
+// keep-all rows whose maximum lies far above the sample's) take the exact
+// window search: key windows histogrammed over the slice re-read from global
+// memory (L2), sliding down until both boundaries are inside.  Masses that
+// decide kept sets are fixed-point integers (units of 2^-40 of the largest
+// weight), so sums, prefixes and decisions are exact and equal in every CTA.
 #pragma once
 
 #include "smp_device.cuh"
@@ -53,7 +59,7 @@ constexpr int XVW = XVS / XNW;      // vectors per warp per stage (128), a conti
 constexpr int XSUB = XVW / 32;      // vectors per lane per stage (4)
 constexpr int XMAXST = 64;          // stages per slice, at most (512 KB)
 constexpr int XMAXC = 8;            // CTAs per row, at most (portable cluster size)
-constexpr int XSW = 128;            // sampled bins each CTA publishes
+constexpr int XSW = 128;            // fine sample bins below a stage's maximum (top-k threshold)
 constexpr int XMAXWIN = 36;         // windows of one row, at most
 constexpr int XWT = XNS * XSB / 16;  // keys whose weight the resolution stores (2048)
 constexpr long long XDRAIN = 4000000000ll;  // cycles the drain after an expired wait may take
@@ -96,7 +102,7 @@ __host__ __device__ inline int xoff_cid(int wf, int cap) {
 }
 __host__ __device__ inline int xoff_sh(int wf, int cap) { return xoff_cid(wf, cap) + cap * 4; }
 
-// Published after the sample (B1) and after the stream (B2).
+// What each CTA publishes to the cluster after the stream (B2).
 struct XPub {
   uint32_t kmax;  // largest legal key seen (0: none)
   int amax;       // smallest id holding it
@@ -108,8 +114,7 @@ struct XPub {
   uint32_t skey;  // largest key of this CTA's first stage (the local sample)
   float xsv;      // the reference of this CTA's masses: that key's value (0 if none)
   int pad[1];
-  double mass;    // flat / keep-all rows: legal mass relative to the local sample's maximum    // keep-all rows: the slice's mass relative to the sample's maximum
-  uint16_t samp[XSW];  // B1 only: counts of stage 0's values in bins (kmax >> SB) - j
+  double mass;    // flat / keep-all rows: legal mass relative to the local sample's maximum
 };
 static_assert(sizeof(XPub) % 16 == 0, "published record: whole 16-byte units");
 constexpr int XPUBW = (int)sizeof(XPub) / 4;
@@ -561,17 +566,15 @@ struct XCtx {
   const uint16_t* gsrc;
   const uint32_t* mrow;
   uint32_t* hist;
-  uint16_t* ckey;
-  int* cid;
   const float* tz;
   uint32_t* mout;
   long long wait_limit;
-  int nst, nvec, nfull, n, s0, cap;
+  int nst, nvec, nfull, n, s0;
   uint32_t lo, hw, lo2;
   float T, zref;
   float xs, c2;  // flat rows: the sample's maximum and log2(e) / T
-  float zb, xcf;  // keep-all rows: zref log2(e); the exact-weight floor
-  uint32_t xc2;   // the floor packed twice in the element type
+  float zb;       // keep-all rows: zref log2(e)
+  uint32_t xc2;   // keep-all rows: the exact-weight floor, packed twice in the element type
   uint32_t* flagw;  // top-k rows: bitmap of vectors holding candidates
   uint32_t* hcnt;   // flat rows: one 32-bit counter per key of [lo, hw] (bin hw - k)
 };
@@ -597,7 +600,7 @@ __device__ __forceinline__ void xstream(const XCtx cx, XStat& st, int& timed_out
   const long long wait_limit = cx.wait_limit;
   const int nst = cx.nst, nvec = cx.nvec, nfull = cx.nfull, n = cx.n, s0 = cx.s0;
   const uint32_t lo = cx.lo, lo2 = cx.lo2, xc2 = cx.xc2;
-  const float T = cx.T, zref = cx.zref, xs = cx.xs, c2 = cx.c2, zb = cx.zb, xcf = cx.xcf;
+  const float T = cx.T, zref = cx.zref, xs = cx.xs, c2 = cx.c2, zb = cx.zb;
   uint32_t* const __restrict__ flagw = cx.flagw;
   uint32_t* const __restrict__ hcnt = cx.hcnt;
   const uint32_t hw = cx.hw;
@@ -1006,8 +1009,6 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     cx.gsrc = gsrc;
     cx.mrow = mrow;
     cx.hist = hist;
-    cx.ckey = ckey;
-    cx.cid = cid;
     cx.tz = tz;
     cx.mout = mout;
     cx.wait_limit = a.wait_limit;
@@ -1016,7 +1017,6 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     cx.nfull = nfull;
     cx.n = n;
     cx.s0 = s0;
-    cx.cap = a.cap;
     cx.lo = lo;
     cx.hw = hw;
     cx.lo2 = lo2;
@@ -1025,7 +1025,6 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
     cx.xs = sk ? R::f(xraw(sk)) : 0.f;
     cx.c2 = T > 0.f ? L2E / T : 0.f;
     cx.zb = zb;
-    cx.xcf = xcf;
     cx.xc2 = xc2;
     cx.flagw = flagw;
     cx.hcnt = hcnt;
