@@ -130,6 +130,7 @@ struct XSh {
   XPub pub2[XMAXC];
   uint64_t km[XMAXC];
   uint64_t uf[XMAXC];
+  uint32_t kbelow[XMAXC];   // window search: each CTA's largest legal key below the window
   float rwf[XMAXST][XNW];   // keep-all rows: per-(stage, warp) masses
   XWin win[XMAXWIN];
   uint32_t h64[64];         // radix counters of the tie cut
@@ -1561,6 +1562,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
       uint64_t ufm = 0;
       const bool want_uf = first && ccls == XC_FLAT && !have_mflat;
       uint32_t* myh = wh + warp * WB;
+      uint32_t kbl = 0u;  // this thread's largest legal key below the window
       for (int v0 = tid; v0 < nvec; v0 += 4 * XNT) {
         uint4 q4[4];
 #pragma unroll
@@ -1571,7 +1573,8 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint4 q = q4[u];
-          if (xany_ge<DT>(q, l2) || want_uf) {
+          const uint32_t vm = xvmax<DT>(q);
+          if (xge2<DT>(vm, l2) != 0u || want_uf) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const uint32_t h = xhalf(q, e);
@@ -1579,10 +1582,13 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
               const uint32_t k = xkey(h);
               if (k >= wl) {
                 if (k <= hi) atomicAdd(&myh[hi - k], 1u);
-              } else if (want_uf) {
-                ufm += xwfx_fast(R::f(h), xmax, c2);
+              } else {
+                kbl = max(kbl, k);
+                if (want_uf) ufm += xwfx_fast(R::f(h), xmax, c2);
               }
             }
+          } else {  // the whole vector lies below the window
+            kbl = max(kbl, max(xkey(vm & 0xffffu), xkey(vm >> 16)));
           }
         }
       }
@@ -1598,8 +1604,21 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
         ufm = xblock_total<uint64_t>(ufm, S.q);
         for (int c = tid; c < C; c += XNT) *xremote(&S.uf[rank], (uint32_t)c) = ufm;
       }
+      kbl = __reduce_max_sync(0xffffffffu, kbl);
+      if (lane == 0) S.wi[warp] = (int)kbl;
+      __syncthreads();
+      if (tid < C) {
+        uint32_t kb = 0u;
+        for (int w = 0; w < XNW; ++w) kb = max(kb, (uint32_t)S.wi[w]);
+        *xremote(&S.kbelow[rank], (uint32_t)tid) = kb;
+      }
       __syncthreads();
       xcluster_sync();  // every CTA's window histogram is complete
+      // the next window starts at the largest legal key below this one (empty
+      // key ranges are skipped); none below: this window is the last
+      uint32_t nxt = 0u;
+      for (int c = 0; c < C; ++c) nxt = max(nxt, S.kbelow[c]);
+      const bool none_below = nxt < floor_key;
       uint64_t uf_total = 0;
       if (want_uf)
         for (int c = 0; c < C; ++c) uf_total += S.uf[c];
@@ -1668,11 +1687,11 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
           MA += mtot;
           myMA += mine;
           first = false;
-          if (wl <= floor_key || nwin >= XMAXWIN - 1) {
+          if (wl <= floor_key || none_below || nwin >= XMAXWIN - 1) {
             failed = true;
             break;
           }
-          hi = wl - 1u;
+          hi = min(wl - 1u, nxt);
           wl = hi >= floor_key + (uint32_t)(WB - 1) ? hi - (uint32_t)(WB - 1) : floor_key;
           continue;
         }
@@ -1716,7 +1735,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
           MA += mtot;
           myMA += mine;
           first = false;
-          if (wl <= floor_key || nwin >= XMAXWIN - 1) {
+          if (wl <= floor_key || none_below || nwin >= XMAXWIN - 1) {
             beta = 0u;  // no prefix reaches p after rounding: keep every legal value
             nb = 0;
             Abeta = A;
@@ -1724,7 +1743,7 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
             resolved = true;
             break;
           }
-          hi = wl - 1u;
+          hi = min(wl - 1u, nxt);
           wl = hi >= floor_key + (uint32_t)(WB - 1) ? hi - (uint32_t)(WB - 1) : floor_key;
           continue;
         }
