@@ -109,6 +109,16 @@ def test_decode_loop_f16():
     H.record_boundaries("decode1024x256000_f16 (200 steps)", tot, bounded=True)
 
 
+def test_topk_covering_a_sparse_legal_set():
+    """Rows whose top_k exceeds a sparse legal set (30 % -inf, grammar masks)
+    and top_p = 1 keep every legal token, also when the legal set is larger
+    than a slice's candidate list (found by a randomised sweep)."""
+    case = workloads.random_case(752032311, 33, 70001, dtype="f16", mask_frac=0.8,
+                                 neg_inf_frac=0.3, sigma=4.0, n_head=(0, 500),
+                                 temps=(0.0, 0.5, 1.0, 1.3, 2.0))
+    run_and_compare(case)
+
+
 def test_far_negative_logits_keep_the_sigma_path(kernel):
     """A penalised decode input: 16 legal logits per row pushed to -60000.
     The results still match the oracle, and on the board kernel the

@@ -1706,9 +1706,12 @@ __global__ void __launch_bounds__(XNT, 4) split_kernel(const XArgs a) {
           phase = FIND_P;
         }
       } else if (first) {
-        // flat row: the whole legal mass, from the stream or from this pass
+        // flat row: the whole legal mass, from the stream or from this pass.
+        // top_p = 1 keeps every legal value (a top-k row whose k covers the
+        // legal set): no target is reached, the windows walk to the last
+        // legal key and sum the exact masses on the way.
         const double m = have_mflat ? Mflat : (double)(mtot + uf_total);
-        P64 = (uint64_t)ceil((double)pp * m);
+        P64 = pp >= 1.f ? ~0ull : (uint64_t)ceil((double)pp * m);
       }
       if (!resolved && phase == FIND_P) {
         if (MA >= P64 && nwin > 0) {
