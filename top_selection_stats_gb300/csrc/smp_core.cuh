@@ -60,7 +60,8 @@ struct JobHdr {
 };
 static_assert(sizeof(JobHdr) % 16 == 0, "job headers keep the board's arrays aligned");
 struct Board {
-  int njobs, ctas_done, exits, pad;
+  int njobs, ctas_done, exits;
+  int next_row;  // the next row a CTA takes (rows are handed out as CTAs free up)
   JobHdr hdr[MAXJOBS];
   float cmass[MAXJOBS][MAXCH * NWARP];  // per-(chunk, warp) masses of the helpers' chunks
   uint32_t lk[MAXJOBS][CAP];            // band: the helpers' bracket elements (key, id)
@@ -109,6 +110,7 @@ struct Sh {
   int niss[NSTAGE];           // bulk copies issued into each stage (for the final drain)
   int gn;                     // gathered entries of the sampled segment
   int bi[8];                  // broadcast ints
+  int row_next;               // the row this CTA takes next (from the board)
   uint32_t bu[8];             // broadcast keys
   uint64_t bq[4];             // broadcast masses
   double bd[4];               // broadcast doubles

@@ -389,6 +389,7 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
       }
       bd->njobs = 0;
       bd->ctas_done = 0;
+      bd->next_row = 0;
       bd->exits = 0;
       __threadfence();
     }
@@ -759,7 +760,21 @@ __global__ void __launch_bounds__(NT, 2) smp_kernel(const __grid_constant__ KArg
     for (int s = 0; s < NSTAGE; ++s) X.sh->niss[s] = 0;
   }
   __syncthreads();
-  for (int row = blockIdx.x; row < a.B; row += gridDim.x) process_row(X, row);
+  if (a.board) {
+    // rows are handed out in order as CTAs free up, so that rows of unequal
+    // cost (and B beyond the resident grid) balance over the CTAs
+#pragma unroll 1
+    while (true) {
+      if (threadIdx.x == 0) X.sh->row_next = atomicAdd(&a.board->next_row, 1);
+      __syncthreads();
+      const int row = X.sh->row_next;
+      __syncthreads();
+      if (row >= a.B) break;
+      process_row(X, row);
+    }
+  } else {
+    for (int row = blockIdx.x; row < a.B; row += gridDim.x) process_row(X, row);
+  }
   help_and_exit(X);
   // After an expired wait: wait again, bounded by a fixed two seconds, for
   // the last copy issued into each stage before the CTA exits (at most one
