@@ -99,6 +99,7 @@ struct Sh {
   uint64_t rq[2][NWARP];
   double rd[2][NWARP];
   float rf[3][NWARP];
+  float r5[5][NWARP];         // the first chunk's statistics (one reduction)
   uint32_t ru[2][NWARP];
   int ri[2][NWARP];
   float cmass[MAXCH][NWARP];  // per-chunk, per-warp masses of the keep-all stream

@@ -19,12 +19,14 @@
 
 namespace smp {
 
-// Mean and deviation of the legal finite elements of a staged chunk.
+// Mean and deviation of the legal finite elements of a staged chunk, and
+// their maximum (-inf if none), in one pass and one block reduction.
 template <int DT>
 __device__ __forceinline__ void chunk_stats(Ctx<DT>& X, const char* stage, float& mu, float& sd,
-                                         int& cnt) {
+                                         int& cnt, float* mx_out = nullptr) {
   constexpr int EPV = ElemT<DT>::EPV;
-  float s1 = 0.f, s2 = 0.f, n = 0.f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float s1 = 0.f, s2 = 0.f, n = 0.f, mn = INFINITY, mx = -INFINITY;
 #pragma unroll 1
   for (int it = 0; it < ITW; ++it) {
     const uint4 r = load_vec(X, stage, 0, warp_vec<DT>(it));
@@ -36,19 +38,49 @@ __device__ __forceinline__ void chunk_stats(Ctx<DT>& X, const char* stage, float
         n += 1.f;
         s1 += x[j];
         s2 += x[j] * x[j];
+        mn = fminf(mn, x[j]);
+        mx = fmaxf(mx, x[j]);
       }
     }
   }
-  n = bsum_f(n, X.sh->rf[0]);
-  s1 = bsum_f(s1, X.sh->rf[1]);
-  s2 = bsum_f(s2, X.sh->rf[2]);
+  n = warp_sum(n);
+  s1 = warp_sum(s1);
+  s2 = warp_sum(s2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  __syncthreads();
+  if (lane == 0) {
+    X.sh->r5[0][warp] = n;
+    X.sh->r5[1][warp] = s1;
+    X.sh->r5[2][warp] = s2;
+    X.sh->r5[3][warp] = mn;
+    X.sh->r5[4][warp] = mx;
+  }
+  __syncthreads();
+  n = s1 = s2 = 0.f;
+  mn = INFINITY;
+  mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) {  // in warp order: every thread the same sums
+    n += X.sh->r5[0][w];
+    s1 += X.sh->r5[1][w];
+    s2 += X.sh->r5[2][w];
+    mn = fminf(mn, X.sh->r5[3][w]);
+    mx = fmaxf(mx, X.sh->r5[4][w]);
+  }
+  if (mx_out) *mx_out = mx;
   cnt = (int)n;
   mu = n > 0.f ? s1 / n : 0.f;
   sd = sqrtf(n > 0.f ? fmaxf(s2 / n - mu * mu, 0.f) : 0.f);
   // A few far-negative legal values (a penalised or suppressed token) would
-  // inflate the deviation and lift the threshold: up to two more passes over
-  // the staged chunk leave out the values more than 4 deviations below the
-  // mean (the upper tail, where the candidates are, is always kept).
+  // inflate the deviation and lift the threshold: when the smallest value
+  // lies more than 4 deviations below the mean, up to two more passes over
+  // the staged chunk leave those values out (the upper tail, where the
+  // candidates are, is always kept).
+  if (!(mn < mu - 4.f * sd)) return;
 #pragma unroll 1
   for (int rep = 0; rep < 2; ++rep) {
     const float lo = mu - 4.f * sd;
@@ -103,10 +135,10 @@ __device__ __forceinline__ void make_threshold(float t, uint32_t& t2, float& tf)
 // Threshold of a sigma-truncated list from the staged first chunk.
 template <int DT>
 __device__ __forceinline__ void list_threshold(Ctx<DT>& X, const char* stage, float Kt, float vest,
-                                               uint32_t& t2, float& tf) {
+                                               uint32_t& t2, float& tf, float* mx_out = nullptr) {
   float mu, sd;
   int n1;
-  chunk_stats(X, stage, mu, sd, n1);
+  chunk_stats(X, stage, mu, sd, n1, mx_out);
   const float t = (n1 >= 64) ? sigma_threshold(*X.a, mu, sd, Kt / vest) : -INFINITY;
   make_threshold<DT>(t, t2, tf);
 }
@@ -547,7 +579,13 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
     const int c = R.c;
     const char* stage = R.wait(X);
     if (c == 0) {
-      if (ref_in != ref_in) {  // reference = the first chunk's maximum
+      if (EMIT) {
+        // the list threshold and the reference (the first chunk's maximum)
+        // from one pass over the chunk
+        float m = -INFINITY;
+        list_threshold(X, stage, Kt, vest, t2, tf, &m);
+        if (ref_in != ref_in) ref = (m > -INFINITY) ? m : 0.f;
+      } else if (ref_in != ref_in) {  // reference = the first chunk's maximum
         float m = -INFINITY;
 #pragma unroll 1
         for (int it = 0; it < ITW; ++it) {
@@ -562,7 +600,6 @@ __device__ __noinline__ ExpOut exp_stream(Ctx<DT>& Xr, float Kt, float vest, flo
       }
       nref = -ref * c2;
       if (EMIT) {
-        list_threshold(X, stage, Kt, vest, t2, tf);
         if (p_hist > 0.f) {
           // top-p row: if the first chunk's mass at or above the list
           // threshold is below p of its mass, the kept set will not fit the
