@@ -63,6 +63,8 @@ def measured_peaks():
 
 
 TOPLP_SOURCES = ["top_selection_stats_gb300/csrc/smp_toplp.cu"]
+SPLIT_SOURCES = ["top_selection_stats_gb300/csrc/" + f for f in (
+    "smp_device.cuh", "smp_philox.cuh", "smp_split.cuh", "smp_x_bf16.cu", "smp_x_f16.cu", "smp_api.cu")]
 GUMBEL_SOURCES = ["top_selection_stats_gb300/csrc/" + f for f in ("smp_gumbel.cu", "smp_philox.cuh")]
 PENALTY_SOURCES = ["top_selection_stats_gb300/csrc/smp_penalty.cu"]
 
@@ -519,7 +521,8 @@ def run_decode_loop(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     alg_bytes = B * row_bytes(V, False, True, esize)
     achieved = alg_bytes / (ms_per_step / 1000.0) / 1e9
-    prof = profiled_entry(args.workload)
+    prof = (profiled_entry(args.workload) if args.kernel == "board"
+            else profiled_entry("split:" + args.workload, SPLIT_SOURCES))
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": None if prof is None else prof.get("dram_bytes_per_launch"),
@@ -739,7 +742,8 @@ def run_ours(args, rank, world, local):
                     "gbs": pen_bytes / (pen_ms / 1000.0) / 1e9,
                     "traffic": profiled_traffic("penalty:" + args.workload, PENALTY_SOURCES)}
     achieved = alg_bytes / (kern_ms / 1000.0) / 1e9
-    prof = profiled_entry(args.workload)
+    prof = (profiled_entry(args.workload) if args.kernel == "board"
+            else profiled_entry("split:" + args.workload, SPLIT_SOURCES))
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": None if prof is None else prof.get("dram_bytes_per_launch"),
