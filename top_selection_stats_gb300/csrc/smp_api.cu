@@ -213,9 +213,12 @@ int launch(smp_ctx* h, int mode, const void* logits, int dt, int B, int V, int64
   }
 
   // one CTA per row, at most two resident per SM; CTAs loop over rows.  With
-  // a job board the whole resident grid is launched: CTAs without a row take
-  // chunk tasks of the slow rows from the start.
-  const int grid = (B < h->grid_max && !h->board) ? B : h->grid_max;
+  // a job board and rows long enough to share (jobs are published for rows
+  // of three chunks or more) the whole resident grid is launched: CTAs
+  // without a row take chunk tasks of the slow rows from the start.
+  const int nch = (V + chunk_elems(dt) - 1) / chunk_elems(dt);
+  const bool helpers = h->board && nch > 2;
+  const int grid = (B < h->grid_max && !helpers) ? B : h->grid_max;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (dt) {
