@@ -331,10 +331,11 @@ int smp_set_kernel(smp_handle h, int kernel);
 int smp_set_wait_limit(smp_handle h, long long cycles);
 
 /* Launch plan of a call with B rows of V tokens of `dtype` on this handle's
- * device: CTAs per row (the thread-block cluster), slice length (tokens per
- * CTA), dynamic shared memory per CTA (bytes) and candidate-list capacity per
- * CTA.  Any output pointer may be NULL.  Returns SMP_ERR_CAPACITY when V
- * cannot be held. */
+ * device, for the kernel smp_set_kernel chose: CTAs per row (the
+ * thread-block cluster; 1 for the board kernel), slice length (tokens per
+ * CTA; the board kernel's staging chunk), dynamic shared memory per CTA
+ * (bytes) and candidate-list capacity per CTA.  Any output pointer may be
+ * NULL.  Returns SMP_ERR_CAPACITY when V cannot be held. */
 int smp_plan(smp_handle h, smp_dtype dtype, int B, int V, int* cluster, int* slice,
              int* smem_bytes, int* capacity);
 
