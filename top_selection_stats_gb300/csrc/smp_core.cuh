@@ -43,13 +43,17 @@ constexpr int WHOFF = 256;
 // chunk back - 1 if that is >= front.  Once the owner's claim fails, chunks
 // [front, nch) are exactly the helpers' ones, and it waits (bounded) for
 // that many tasks.  ENDS_OFF keeps failed helper claims from borrowing into
-// the front half.
+// the front half; bit ENDS_KIND of the back half holds the job's kind.  The
+// word is written last when a job is published (after the header and a
+// fence), so a claim that succeeds sees the whole header, and a helper finds
+// open jobs with one load per slot.
 constexpr int MAXJOBS = 32;
 constexpr int JOB_BAND = 0, JOB_STREAM = 1;
 constexpr uint32_t ENDS_OFF = 1u << 20;
+constexpr uint32_t ENDS_KIND = 1u << 30;
 struct JobHdr {
   unsigned long long ends;
-  int ready, row, kind, nch;
+  int pad, row, kind, nch;
   int b_lo, b_hi, done, list_n;
   float nref, nm, c2;
   int above_n;

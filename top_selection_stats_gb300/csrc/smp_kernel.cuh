@@ -330,14 +330,10 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
       static_assert(MAXJOBS <= 32, "one lane per job slot");
       volatile Board* vb = bd;
       const int lane = threadIdx.x;
-      const int nj = min(vb->njobs, MAXJOBS);
-      bool open = false;
-      if (lane < nj && vb->hdr[lane].ready) {
-        const unsigned long long e = vb->hdr[lane].ends;
-        open = ends_front(e) < ends_back(e);
-      }
+      const unsigned long long e = vb->hdr[lane].ends;  // unpublished slots read as closed
+      const bool open = ends_front(e) < ends_back(e);
       const uint32_t m = __ballot_sync(0xffffffffu, open);
-      int jj = -1, tt = -1, stop = 0;
+      int jj = -1, tt = -1, stop = 0, kind = 0;
       // after an expired wait this CTA takes no more tasks
       if (lane == 0 && X.sh->timeout) {
         stop = 1;
@@ -354,9 +350,10 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
           if (d >= ends_front(old)) {
             jj = q;
             tt = d;
+            kind = ends_kind(old);
           }
         }
-        __threadfence();  // the job's header is read after its ready flag
+        __threadfence();  // the job's header is read after the claim
         if (jj < 0 && !m) {
           if (vb->ctas_done >= (int)gridDim.x || clock64() - t0 > lim) stop = 1;
           else __nanosleep(200);
@@ -364,7 +361,7 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
         X.sh->bi[0] = jj;
         X.sh->bi[1] = tt;
         X.sh->bi[2] = stop;
-        X.sh->bi[3] = (jj >= 0) ? vb->hdr[jj].kind : 0;
+        X.sh->bi[3] = kind;
       }
     }
     __syncthreads();
@@ -383,7 +380,7 @@ __device__ __noinline__ void help_and_exit(Ctx<DT>& X) {
       for (int q = 0; q < nj; ++q) {
         JobHdr* H = &bd->hdr[q];
         H->ends = 0ull;  // reads as closed until the next publish
-        H->ready = H->done = H->list_n = H->above_n = 0;
+        H->done = H->list_n = H->above_n = 0;
         H->mxk = 0u;
         H->nleg = H->nf = H->bad = 0;
       }

@@ -368,7 +368,10 @@ __device__ __forceinline__ void whist_add(uint32_t* wh, float x, float c2, float
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int ends_front(unsigned long long e) { return (int)(e >> 32); }
 __device__ __forceinline__ int ends_back(unsigned long long e) {
-  return (int)(uint32_t)e - (int)ENDS_OFF;
+  return (int)((uint32_t)e & (ENDS_KIND - 1u)) - (int)ENDS_OFF;
+}
+__device__ __forceinline__ int ends_kind(unsigned long long e) {
+  return ((uint32_t)e & ENDS_KIND) ? JOB_STREAM : JOB_BAND;
 }
 
 template <int DT>
@@ -388,9 +391,6 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, fl
     for (int b = threadIdx.x; b < WBINS; b += NT) bd->wh[j][b] = 0u;
   if (threadIdx.x == 0) {
     JobHdr* H = &bd->hdr[j];
-    // the owner holds chunk 0 of a band job and chunks 0 and 1 of a stream
-    // job (its ring already has them)
-    H->ends = ((kind == JOB_BAND ? 1ull : 2ull) << 32) | (unsigned long long)((uint32_t)nch + ENDS_OFF);
     H->row = X.row;
     H->kind = kind;
     H->nch = nch;
@@ -404,7 +404,12 @@ __device__ int publish_job(Ctx<DT>& X, int kind, int nch, int b_lo, int b_hi, fl
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) atomicExch(&bd->hdr[j].ready, 1);
+  // opened last: the owner holds chunk 0 of a band job and chunks 0 and 1 of
+  // a stream job (its ring already has them)
+  if (threadIdx.x == 0)
+    atomicExch(&bd->hdr[j].ends,
+               ((kind == JOB_BAND ? 1ull : 2ull) << 32) |
+                   (unsigned long long)((uint32_t)nch + ENDS_OFF + (kind == JOB_STREAM ? ENDS_KIND : 0u)));
   return j;
 }
 
