@@ -661,9 +661,8 @@ __device__ __forceinline__ void warp_release(Ctx<DT>& X, int c) {
 }
 
 template <int DT>
-__device__ __forceinline__ const char* ring_wait(Ctx<DT>& X, int c) {
+__device__ __forceinline__ const char* ring_wait_at(Ctx<DT>& X, int c, int s) {
   constexpr int ES = ElemT<DT>::ES, CE = ElemT<DT>::CE;
-  const int s = c % NSTAGE;
   char* stage = X.ring + (size_t)s * STAGE_BYTES;
   const uint32_t par = (X.parity >> s) & 1u;
   if (!X.sh->timeout && !mbar_wait_bounded(&X.sh->full[s], par, X.a->wait_limit)) X.sh->timeout = 1;
@@ -685,6 +684,20 @@ __device__ __forceinline__ const char* ring_wait(Ctx<DT>& X, int c) {
     __syncthreads();
   }
   return stage;
+}
+template <int DT>
+__device__ __forceinline__ const char* ring_wait(Ctx<DT>& X, int c) {
+  return ring_wait_at(X, c, c % NSTAGE);
+}
+
+// A helper's next chunk of job j, claimed from the back (see JobHdr) by
+// thread 0 while the current chunk is processed: -1 when none is left or the
+// CTA stopped streaming after an expired wait.
+__device__ __forceinline__ int helper_claim(Board* bd, int j, int timeout) {
+  if (timeout) return -1;
+  const unsigned long long old = atomicAdd(&bd->hdr[j].ends, ~0ull);
+  const int d = (int)((uint32_t)old & (ENDS_KIND - 1u)) - (int)ENDS_OFF - 1;
+  return (d >= (int)(old >> 32)) ? d : -1;
 }
 
 template <int DT>

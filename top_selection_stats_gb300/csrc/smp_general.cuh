@@ -409,10 +409,11 @@ __device__ __noinline__ int band_owner_pass(Ctx<DT>& Xr, int j, int b_lo, int b_
 }
 
 // ---------------------------------------------------------------------------
-// One chunk of a published band pass (job j), run by a helper: band_chunk
-// into this CTA's list area, then the entries are copied behind one
-// reservation in the job's list; the cells go to the job and the count to
-// its header.
+// Chunks of a published band pass (job j), run by a helper from chunk c on
+// (the next chunk claimed and its copy issued while one is processed):
+// band_chunk into this CTA's list area, the cells to the job; at the end the
+// entries are copied behind one reservation in the job's list and the counts
+// go to its header.
 // ---------------------------------------------------------------------------
 template <int DT>
 __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
@@ -429,15 +430,29 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
   X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
   X.c2 = c2;
   uint32_t* mrow = a.kept_mask ? a.kept_mask + (size_t)row * X.W : nullptr;
+  int s = 0;
   if (threadIdx.x == 0) {
-    issue_chunk(X, c, c % NSTAGE);  // (the previous task's last barrier freed the stage)
+    issue_chunk(X, c, s);  // (the previous task's last barrier freed both stages)
     X.sh->n = 0;
   }
   __syncthreads();
-  const char* stage = ring_wait(X, c);
-  int nk = 0;
-  const float ws = warp_sum(band_chunk<DT>(X, stage, c, xa, xb, c2, nm, mrow, nk));
-  if (lane == 0) bd->cmass[j][c * NWARP + warp] = ws;
+  int nk = 0, ndone = 0;
+#pragma unroll 1
+  for (int it = 0;; ++it) {
+    if (threadIdx.x == 0) {
+      const int d = helper_claim(bd, j, X.sh->timeout);
+      if (d >= 0) issue_chunk(X, d, s ^ 1);
+      X.sh->bi[6 + (it & 1)] = d;
+    }
+    const char* stage = ring_wait_at(X, c, s);
+    const float ws = warp_sum(band_chunk<DT>(X, stage, c, xa, xb, c2, nm, mrow, nk));
+    if (lane == 0) bd->cmass[j][c * NWARP + warp] = ws;
+    ++ndone;
+    __syncthreads();  // the stage is free, the next claim visible
+    c = X.sh->bi[6 + (it & 1)];
+    if (c < 0) break;
+    s ^= 1;
+  }
   nk = __reduce_add_sync(0xffffffffu, nk);
   if (lane == 0 && nk) atomicAdd((int*)&H->above_n, nk);
   __syncthreads();
@@ -453,7 +468,7 @@ __device__ __noinline__ void band_task(Ctx<DT>& Xr, int j, int c) {
   if (threadIdx.x == 0 && X.sh->timeout) atomicOr((int*)&H->bad, 1);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) atomicAdd((int*)&H->done, 1);
+  if (threadIdx.x == 0) atomicAdd((int*)&H->done, ndone);
 }
 
 // ---------------------------------------------------------------------------

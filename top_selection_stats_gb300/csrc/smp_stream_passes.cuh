@@ -507,9 +507,12 @@ __device__ __forceinline__ float mass_hist_chunk(const Ctx<DT>& X, const char* s
 }
 
 // ---------------------------------------------------------------------------
-// One chunk of a published mass stream (job j), run by a helper: its
-// per-warp masses, legal count, largest value, NaN / +inf flag and weight
-// histogram (built in this CTA's histogram area, then added to the job's).
+// Chunks of a published mass stream (job j), run by a helper from chunk c on:
+// while a chunk is processed the next one is claimed and its copy issued into
+// the other stage, so the helper stays on the job until its chunks run out.
+// Per chunk: the per-warp masses.  Once, at the end: the legal count, largest
+// value, NaN / +inf flag and weight histogram (built in this CTA's histogram
+// area, then added to the job's) and the number of chunks done.
 // ---------------------------------------------------------------------------
 template <int DT>
 __device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
@@ -525,17 +528,31 @@ __device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
   X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
   X.c2 = c2;
   // the chunk's copy first, the histogram clear while it is in flight (the
-  // previous task's last barrier freed the stage)
-  if (threadIdx.x == 0) issue_chunk(X, c, c % NSTAGE);
+  // previous task's last barrier freed both stages)
+  int s = 0;
+  if (threadIdx.x == 0) issue_chunk(X, c, s);
   uint32_t* wh = X.wh;
   for (int b = threadIdx.x; b < WBINS; b += NT) wh[b] = 0u;
   __syncthreads();
-  const char* stage = ring_wait(X, c);
   uint32_t amax = p_ninf<DT>();
-  int nleg = 0;
-  const float cs = mass_hist_chunk<DT>(X, stage, c, c2, nref, wh, amax, nleg);
-  const float ws = warp_sum(cs);
-  if ((threadIdx.x & 31) == 0) bd->cmass[j][c * NWARP + (threadIdx.x >> 5)] = ws;
+  int nleg = 0, ndone = 0;
+#pragma unroll 1
+  for (int it = 0;; ++it) {
+    if (threadIdx.x == 0) {
+      const int d = helper_claim(bd, j, X.sh->timeout);
+      if (d >= 0) issue_chunk(X, d, s ^ 1);
+      X.sh->bi[6 + (it & 1)] = d;
+    }
+    const char* stage = ring_wait_at(X, c, s);
+    const float cs = mass_hist_chunk<DT>(X, stage, c, c2, nref, wh, amax, nleg);
+    const float ws = warp_sum(cs);
+    if ((threadIdx.x & 31) == 0) bd->cmass[j][c * NWARP + (threadIdx.x >> 5)] = ws;
+    ++ndone;
+    __syncthreads();  // the stage is free, the next claim visible
+    c = X.sh->bi[6 + (it & 1)];
+    if (c < 0) break;
+    s ^= 1;
+  }
   const float tmax = p2f_max<DT>(amax);
   const int nf = bsum_i((tmax < INFINITY) ? 0 : 1, X.sh->ri[1]);  // (its barrier ends the histogram)
   for (int b = threadIdx.x; b < WBINS; b += NT) {
@@ -552,7 +569,7 @@ __device__ __noinline__ void stream_task(Ctx<DT>& Xr, int j, int c) {
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) atomicAdd((int*)&H->done, 1);
+  if (threadIdx.x == 0) atomicAdd((int*)&H->done, ndone);
 }
 
 template <int DT, bool ALLM, bool EMIT>
