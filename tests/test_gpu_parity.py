@@ -254,6 +254,41 @@ def test_tie_groups_beyond_list_capacity(dtype):
     H.compare(case, gm, r, mode="mask", check_probs=True)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tie_groups_of_hundreds_at_the_boundary(dtype):
+    """A value with 300-2040 copies holds the top-k or top-p boundary, so the
+    earliest-id quota ranks hundreds of tied ids: spread over the row (ranked
+    within one bin of consecutive ids) or packed into consecutive ids (a bin
+    with more copies than threads takes the radix ranking)."""
+    V, B = 128256, 16
+    rng = np.random.default_rng(31)
+    x = np.clip(rng.standard_normal((B, V)), -6.0, 3.5).astype(np.float32)
+    T = np.empty(B, np.float32)
+    K = np.empty(B, np.int32)
+    P = np.empty(B, np.float32)
+    for r_ in range(B):
+        m = (300, 700, 1500, 2040)[r_ % 4]
+        topk_row = (r_ // 4) % 2 == 0
+        ids = (np.arange(1024, 1024 + m) if r_ >= 8 else rng.choice(V - 8, size=m, replace=False))
+        x[r_, ids] = 4.0
+        head = np.setdiff1d(np.arange(V - 8, V), ids)[:5]
+        x[r_, head] = 6.0 + 0.5 * np.arange(5)
+        T[r_] = 1.0 if r_ % 3 else 0.7
+        xv = workloads.to_dtype(x[r_], dtype).float().numpy().astype(np.float64)
+        w = np.exp((xv - xv.max()) / T[r_])
+        if topk_row:
+            K[r_], P[r_] = 5 + m // 2, 1.0
+        else:
+            w4 = np.exp((4.0 - xv.max()) / T[r_])
+            K[r_] = V
+            P[r_] = np.float32((w[xv > 4.0].sum() + (m // 2 + 0.5) * w4) / w.sum())
+    case = dict(name="tiegroups", B=B, V=V, dtype=dtype, logits=workloads.to_dtype(x, dtype),
+                bitmask=None, temperature=torch.from_numpy(T), top_k=torch.from_numpy(K),
+                top_p=torch.from_numpy(P), seed=torch.full((B,), 3, dtype=torch.int64),
+                offset=torch.arange(B))
+    run_and_compare(case)
+
+
 def test_few_legal_tokens_take_the_whole_legal_set():
     """Grammar masks that leave a handful of tokens: the list takes every legal
     token, k beyond the legal count keeps them all."""

@@ -494,9 +494,63 @@ __device__ void hist16_build(Ctx<DT>& X, int n, uint32_t kbase, bool sk, uint32_
   __syncthreads();
 }
 
+// j-th smallest (1-based) of the m distinct ids g[0..m), NT < m <= TG16: a
+// count of the ids in NT bins of consecutive ids (one bin per thread), a block
+// scan to the bin that holds the j-th, then ranks among that bin's ids.  -2
+// when that bin holds more than NT ids.  Scratch: the 16-bit key histogram's
+// area (its counts are no longer needed when a tie quota is taken).
+template <int DT>
+__device__ int nth_id_bins(Ctx<DT>& X, const int* g, int m, int j) {
+  uint32_t* bc = hist16(X);             // NT bin counts
+  int* gb = reinterpret_cast<int*>(bc + NT);  // the chosen bin's ids
+  uint32_t* bs = bc + 2 * NT;           // chosen bin, rank in it, gathered, result
+  const int t = threadIdx.x;
+  int sh = 0;
+  while (((X.V - 1) >> sh) >= NT) ++sh;  // bin of id: id >> sh, below NT
+  bc[t] = 0u;
+  if (t == 0) {
+    bs[0] = (uint32_t)NT;  // no bin yet
+    bs[2] = 0u;
+    bs[3] = 0xffffffffu;
+  }
+  __syncthreads();
+  for (int i = t; i < m; i += NT) atomicAdd(&bc[min(g[i] >> sh, NT - 1)], 1u);
+  __syncthreads();
+  const uint32_t c = bc[t];
+  uint32_t tot;
+  const uint32_t cum = bscan_excl<uint32_t>(c, X.sh->ru[0], tot);
+  if (cum < (uint32_t)j && cum + c >= (uint32_t)j) {
+    bs[0] = (uint32_t)t;
+    bs[1] = (uint32_t)j - cum;
+  }
+  __syncthreads();
+  const int b = (int)bs[0];
+  if (b >= NT) return -1;  // j beyond the ids (every thread: the same answer)
+  const int jb = (int)bs[1];
+  const int cb = (int)bc[b];
+  if (cb > NT) return -2;
+  for (int i = t; i < m; i += NT) {
+    const int id = g[i];
+    if (min(id >> sh, NT - 1) == b) gb[atomicAdd(&bs[2], 1u)] = id;
+  }
+  __syncthreads();
+  if (t < cb) {
+    const int ida = gb[t];
+    int r = 0;
+#pragma unroll 4
+    for (int q = 0; q < cb; ++q) r += (gb[q] < ida) ? 1 : 0;
+    if (r == jb - 1) bs[3] = (uint32_t)ida;
+  }
+  __syncthreads();
+  const int id = (int)bs[3];
+  __syncthreads();  // the scratch may be reused once every thread has read it
+  return id;
+}
+
 // The j-th smallest id (j >= 1) among the entries with key v that are S_k
-// members; -2 when more than NT entries share the key (the caller then ranks
-// them by radix selection on ids).
+// members: up to NT entries ranked directly, up to TG16 through nth_id_bins;
+// -2 beyond that, or when one bin of ids holds more than NT of them (the
+// caller then ranks them by radix selection on ids).
 template <int DT>
 __device__ int nth_id16(Ctx<DT>& X, int n, uint32_t v, int j, uint32_t vK, int idK) {
   int* g = tie16(X);
@@ -515,7 +569,8 @@ __device__ int nth_id16(Ctx<DT>& X, int n, uint32_t v, int j, uint32_t vK, int i
   }
   __syncthreads();
   const int m = X.sh->gn;
-  if (m > NT) return -2;
+  if (m > TG16) return -2;
+  if (m > NT) return nth_id_bins(X, g, m, j);
   if ((int)threadIdx.x < m) {
     const int ida = g[threadIdx.x];
     int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // ids are distinct
