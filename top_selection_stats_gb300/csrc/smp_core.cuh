@@ -116,6 +116,7 @@ struct Sh {
   int gn;                     // gathered entries of the sampled segment
   int bi[8];                  // broadcast ints
   int row_next;               // the row this CTA takes next (from the board)
+  int primed;                 // chunks 0.. of the row are in flight for its first pass
   uint32_t bu[8];             // broadcast keys
   uint64_t bq[4];             // broadcast masses
   double bd[4];               // broadcast doubles
@@ -611,9 +612,25 @@ __device__ __forceinline__ void ring_begin(Ctx<DT>& X, int first = 0) {
   if (threadIdx.x == 0)
     for (int s = 0; s < NSTAGE; ++s) X.sh->done[s] = 0;
   __syncthreads();
-  if (threadIdx.x == 0)
-    for (int s = 0; s < NSTAGE && first + s < X.nch; ++s)
-      issue_chunk(X, first + s, (first + s) % NSTAGE);
+  if (threadIdx.x == 0) {
+    if (X.sh->primed && first == 0) {
+      X.sh->primed = 0;  // the row's first pass: its chunks were issued with the row
+    } else {
+      for (int s = 0; s < NSTAGE && first + s < X.nch; ++s)
+        issue_chunk(X, first + s, (first + s) % NSTAGE);
+    }
+  }
+}
+
+// The first chunks of a row, issued as soon as the row is known (before its
+// parameters are read) for the first pass to take over in ring_begin.
+template <int DT>
+__device__ __forceinline__ void ring_prime(Ctx<DT>& X) {
+  if (threadIdx.x == 0 && !X.sh->timeout) {
+    for (int s = 0; s < NSTAGE; ++s) X.sh->done[s] = 0;
+    for (int s = 0; s < NSTAGE && s < X.nch; ++s) issue_chunk(X, s, s);
+    X.sh->primed = 1;
+  }
 }
 
 // Per-warp consumption of a pass (no block barrier inside the loop): each warp

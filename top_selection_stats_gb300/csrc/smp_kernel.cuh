@@ -60,6 +60,13 @@ __device__ __noinline__ void error_row(Ctx<DT>& Xr, int status, int where = 0) {
   LocalCtx<DT> lc_(Xr);
   Ctx<DT>& X = lc_.v;
   __syncthreads();
+  if (X.sh->primed) {
+    // the row ends before its first pass: take the issued chunks off the ring
+    ring_wait(X, 0);
+    if (X.nch > 1) ring_wait(X, 1);
+    __syncthreads();
+    if (threadIdx.x == 0) X.sh->primed = 0;
+  }
   zero_outputs(X);
   write_row(X, status, -1, 0, PATH_ERROR);
   if (threadIdx.x == 0 && X.a->row_info) X.a->row_info[(size_t)X.row * 4 + 2] = where;
@@ -692,6 +699,7 @@ __device__ __forceinline__ void process_row(Ctx<DT>& X, int row) {
   X.src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.ld * ElemT<DT>::ES;
   X.bm = a.bitmask ? a.bitmask + (size_t)row * X.W : nullptr;
   __syncthreads();
+  ring_prime(X);
   // an expired wait leaves the ring's phases unknown: this CTA streams no more
   if (X.sh->timeout) return error_row(X, ST_TIMEOUT, __LINE__);
 
@@ -754,6 +762,7 @@ __global__ void __launch_bounds__(NT, 2) smp_kernel(const __grid_constant__ KArg
     fence_mbar_init();
     X.sh->timeout = 0;
     X.sh->n = 0;
+    X.sh->primed = 0;
     for (int s = 0; s < NSTAGE; ++s) X.sh->niss[s] = 0;
   }
   __syncthreads();
