@@ -37,12 +37,13 @@ constexpr int WHOFF = 256;
 // stream of a row whose kept set is predicted to be large (kind JOB_STREAM),
 // and the band pass over a weight-histogram bracket (JOB_BAND).  The owner
 // keeps streaming the row from the front through its ring; CTAs without a row
-// of their own, or done with theirs, take single chunks from the back.  One
+// of their own, or done with theirs, take chunks from the back, one claim at a
+// time, and stay on the job while chunks are left.  One
 // 64-bit word holds both ends (front << 32 | back + ENDS_OFF): the owner adds
 // 1 << 32 and owns chunk `front` if front < back; a helper adds -1 and owns
 // chunk back - 1 if that is >= front.  Once the owner's claim fails, chunks
-// [front, nch) are exactly the helpers' ones, and it waits (bounded) for
-// that many tasks.  ENDS_OFF keeps failed helper claims from borrowing into
+// [front, nch) are exactly the helpers' ones, and it waits (bounded) until
+// the helpers report that many chunks done.  ENDS_OFF keeps failed helper claims from borrowing into
 // the front half; bit ENDS_KIND of the back half holds the job's kind.  The
 // word is written last when a job is published (after the header and a
 // fence), so a claim that succeeds sees the whole header, and a helper finds

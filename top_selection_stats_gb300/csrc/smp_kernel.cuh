@@ -245,9 +245,9 @@ __device__ __noinline__ void finish_band(Ctx<DT>& X, int n, const BandOut& bo, u
 }
 
 // ---------------------------------------------------------------------------
-// Band jobs.  The owner of a bracketed row publishes its band pass (one task
-// per chunk), runs tasks itself, waits (bounded) for the tasks others
-// claimed, and gathers the list, the cell masses and the count above the
+// Band jobs.  The owner of a bracketed row publishes its band pass, runs its
+// chunks from the front, waits (bounded) for the chunks helpers claimed from
+// the back, and gathers the list, the cell masses and the count above the
 // bracket.
 // ---------------------------------------------------------------------------
 // The owner's side of band job j: its band pass from the front, a bounded wait

@@ -359,12 +359,12 @@ __device__ __forceinline__ void whist_add(uint32_t* wh, float x, float c2, float
 }
 
 // ---------------------------------------------------------------------------
-// Job board primitives.  publish_job writes a job's header for this CTA's row
-// (fenced before the ready flag; the owner keeps chunk 0, and chunk 1 of a
-// stream job) and returns
-// its slot, or -1 without a board or a free slot.  OwnerClaims walks the
-// owner's claims from the front, one chunk ahead of the ring.  wait_job
-// waits, bounded, until n helper tasks of job j are done.
+// Job board primitives.  publish_job writes a job's header for this CTA's row,
+// then (after a fence) the claim word that opens it (the owner keeps chunk 0,
+// and chunk 1 of a stream job), and returns its slot, or -1 without a board
+// or a free slot.  OwnerClaims walks the owner's claims from the front, one
+// chunk ahead of the ring.  wait_job waits, bounded, until the helpers report
+// n chunks of job j done.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int ends_front(unsigned long long e) { return (int)(e >> 32); }
 __device__ __forceinline__ int ends_back(unsigned long long e) {
