@@ -381,50 +381,9 @@ __device__ __forceinline__ uint32_t p_pinf() {
   return DT == DT_F32 ? 0x7f800000u : (DT == DT_BF16 ? 0x7f807f80u : 0x7c007c00u);
 }
 
-// Some element <= t, or NaN (t = -inf: the vector holds an illegal slot).
-template <int DT>
-__device__ __forceinline__ bool any_le(const uint4 r, uint32_t t2, float tf) {
-  if constexpr (DT == DT_F32) {
-    return !(__uint_as_float(r.x) > tf && __uint_as_float(r.y) > tf &&
-             __uint_as_float(r.z) > tf && __uint_as_float(r.w) > tf);
-  } else if constexpr (DT == DT_BF16) {
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
-    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
-    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
-    const __nv_bfloat162 m = __hmin2_nan(__hmin2_nan(a, b), __hmin2_nan(c, d));
-    return !__hbgt2(m, *reinterpret_cast<const __nv_bfloat162*>(&t2));
-  } else {
-    const __half2 a = *reinterpret_cast<const __half2*>(&r.x);
-    const __half2 b = *reinterpret_cast<const __half2*>(&r.y);
-    const __half2 c = *reinterpret_cast<const __half2*>(&r.z);
-    const __half2 d = *reinterpret_cast<const __half2*>(&r.w);
-    const __half2 m = __hmin2_nan(__hmin2_nan(a, b), __hmin2_nan(c, d));
-    return !__hbgt2(m, *reinterpret_cast<const __half2*>(&t2));
-  }
-}
-// Packed +inf and -inf of the element type.
-template <int DT>
-__device__ __forceinline__ uint32_t pinf2() {
-  return DT == DT_F32 ? 0x7f800000u : (DT == DT_BF16 ? 0x7f807f80u : 0x7c007c00u);
-}
 template <int DT>
 __device__ __forceinline__ uint32_t ninf2() {
   return DT == DT_F32 ? 0xff800000u : ElemT<DT>::NEG2;
-}
-// True when the vector holds -inf (an illegal slot).
-template <int DT>
-__device__ __forceinline__ bool any_neg_inf(const uint4 r) {
-  if constexpr (DT == DT_F32) {
-    return r.x == 0xff800000u || r.y == 0xff800000u || r.z == 0xff800000u || r.w == 0xff800000u;
-  } else {
-    constexpr uint32_t N = ElemT<DT>::NEG2 & 0xffffu;
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-    bool f = false;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) f |= ((w[q] & 0xffffu) == N) | ((w[q] >> 16) == N);
-    return f;
-  }
 }
 // Replace masked-out elements (bit 0 in lb) by -inf.
 template <int DT>
@@ -724,20 +683,6 @@ __device__ __forceinline__ void ring_release(Ctx<DT>& X, int c) {
   if (threadIdx.x == 0 && c + NSTAGE < X.nch) issue_chunk(X, c + NSTAGE, c % NSTAGE);
 }
 
-// Waits for the chunks after c that are already in flight (chunks up to
-// c + NSTAGE - 1) when a pass stops after chunk c without releasing it: no
-// copy may still be landing in a stage that is reused as scratch.
-template <int DT>
-__device__ __forceinline__ void ring_drain(Ctx<DT>& X, int c) {
-  for (int d = c + 1; d < X.nch && d < c + NSTAGE; ++d) {
-    const int s = d % NSTAGE;
-    const uint32_t par = (X.parity >> s) & 1u;
-    if (!X.sh->timeout && !mbar_wait_bounded(&X.sh->full[s], par, X.a->wait_limit))
-      X.sh->timeout = 1;
-    X.parity ^= 1u << s;
-  }
-  __syncthreads();
-}
 
 // Register-resident iterator of a per-warp pass: stage index, pass round and
 // the last chunk fully covered by bulk copies, kept incrementally so the

@@ -130,76 +130,12 @@ __device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t offset)
 }
 
 // --------------------------------------------------------------------------
-// Warp and block reductions (block = NT threads; `scratch` holds NWARP slots
-// and is reused: every block_* call starts and ends with __syncthreads()).
+// Warp reductions and scans.
 // --------------------------------------------------------------------------
 template <class T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
-  return __reduce_min_sync(0xffffffffu, v);
-}
-__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
-  return __reduce_max_sync(0xffffffffu, v);
-}
-
-template <class T>
-__device__ T block_sum(T v, T* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum(v);
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  T r = scratch[0];
-#pragma unroll
-  for (int w = 1; w < NWARP; ++w) r += scratch[w];
-  __syncthreads();
-  return r;
-}
-__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, uint32_t* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_min_u32(v);
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  uint32_t r = scratch[0];
-#pragma unroll
-  for (int w = 1; w < NWARP; ++w) r = min(r, scratch[w]);
-  __syncthreads();
-  return r;
-}
-__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_max_u32(v);
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  uint32_t r = scratch[0];
-#pragma unroll
-  for (int w = 1; w < NWARP; ++w) r = max(r, scratch[w]);
-  __syncthreads();
-  return r;
-}
-
-// (min key, multiplicity of that key) pairs.
-struct MinCnt {
-  uint32_t key;
-  int cnt;
-};
-__device__ __forceinline__ MinCnt mc_combine(MinCnt a, MinCnt b) {
-  if (a.key < b.key) return a;
-  if (b.key < a.key) return b;
-  return MinCnt{a.key, a.cnt + b.cnt};
-}
-__device__ __forceinline__ MinCnt warp_mincnt(MinCnt v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MinCnt w{__shfl_xor_sync(0xffffffffu, v.key, o), __shfl_xor_sync(0xffffffffu, v.cnt, o)};
-    v = mc_combine(v, w);
-  }
   return v;
 }
 

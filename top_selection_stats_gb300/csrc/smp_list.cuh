@@ -80,26 +80,6 @@ __device__ __forceinline__ uint32_t list_append(Ctx<DT>& X, const uint4 r, int i
   return kmax;
 }
 
-// Per-lane append (no warp collective): the elements flagged in cm (bit j =
-// element j of the vector r, ids id0 + j).  Returns the largest key appended.
-template <int DT>
-__device__ __forceinline__ uint32_t lane_append(uint32_t* lk, int* li, int* n, const uint4 r, int id0,
-                                                uint32_t cm) {
-  uint32_t kmax = 0u;
-  int pos = atomicAdd(n, __popc(cm));
-  while (cm) {
-    const int j = __ffs(cm) - 1;
-    cm &= cm - 1u;
-    const uint32_t k = bits_key<DT>(elem_bits_dyn<DT>(r, j));
-    kmax = max(kmax, k);
-    if (pos < CAP) {
-      lk[pos] = k;
-      li[pos] = id0 + j;
-    }
-    ++pos;
-  }
-  return kmax;
-}
 
 // Bits of the elements >= t (packed compares; NaN compares false); a NaN in
 // the vector raises nf (+inf is kept and caught by the list's largest key).
@@ -193,18 +173,6 @@ __device__ __forceinline__ uint32_t warp_append_hits(Ctx<DT>& X, const char* sta
   return kmax;
 }
 
-// Bits of the elements >= tf; NaN or +inf raises nf.
-template <int DT>
-__device__ __forceinline__ uint32_t ge_bits(const uint4 r, float tf, int& nf) {
-  uint32_t cm = 0u;
-#pragma unroll
-  for (int j = 0; j < ElemT<DT>::EPV; ++j) {
-    const float x = bits_value<DT>(elem_bits<DT>(r, j));
-    if (x >= tf) cm |= 1u << j;
-    if (x != x || x == INFINITY) nf = 1;
-  }
-  return cm;
-}
 
 // ---------------------------------------------------------------------------
 // Thread groups
@@ -222,11 +190,6 @@ template <int G>
 __device__ __forceinline__ uint64_t gsum_q(uint64_t v, uint64_t* s) {
   if (G == 32) return warp_sum(v);
   return bsum_q(v, s);
-}
-template <int G>
-__device__ __forceinline__ int gsum_i(int v, int* s) {
-  if (G == 32) return __reduce_add_sync(0xffffffffu, v);
-  return bsum_i(v, s);
 }
 template <int G>
 __device__ __forceinline__ uint32_t gmax_u(uint32_t v, uint32_t* s) {

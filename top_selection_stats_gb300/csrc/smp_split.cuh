@@ -220,10 +220,6 @@ template <int DT>
 __device__ __forceinline__ uint32_t xvmax(uint4 q) {
   return xmax2<DT>(xmax2<DT>(q.x, q.y), xmax2<DT>(q.z, q.w));
 }
-template <int DT>
-__device__ __forceinline__ bool xany_ge(uint4 q, uint32_t t2) {
-  return (xge2<DT>(q.x, t2) | xge2<DT>(q.y, t2) | xge2<DT>(q.z, t2) | xge2<DT>(q.w, t2)) != 0u;
-}
 
 // Shared-space loads (the pointers below always point into shared memory).
 __device__ __forceinline__ uint4 xlds128(const void* p) {
@@ -715,17 +711,6 @@ __device__ __forceinline__ void xfinish(const XArgs& a, int row, uint32_t rank, 
       ri[3] = i3;
     }
   }
-}
-// This CTA's mass over window bins [0, upto) (bin b holds key hi - b).
-template <int DT>
-__device__ __forceinline__ uint64_t xmy_mass(const uint32_t* hist, uint32_t hi, int upto, float T,
-                                             float zmax, uint64_t* sc) {
-  uint64_t mine = 0;
-  for (int b = threadIdx.x; b < upto; b += XNT) {
-    const uint32_t c = (hist[b >> 1] >> ((b & 1) << 4)) & 0xffffu;
-    if (c) mine += (uint64_t)c * xwfx(XT<DT>::f(xraw(hi - (uint32_t)b)), T, zmax);
-  }
-  return xblock_total<uint64_t>(mine, sc);
 }
 // The same over a histogram with one 32-bit counter per bin.
 template <int DT>

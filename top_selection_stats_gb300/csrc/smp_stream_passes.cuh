@@ -143,20 +143,6 @@ __device__ __forceinline__ void list_threshold(Ctx<DT>& X, const char* stage, fl
   make_threshold<DT>(t, t2, tf);
 }
 
-// Vector vi of a staged chunk c with the legal mask applied (no context).
-template <int DT>
-__device__ __forceinline__ uint4 stage_vec(const char* stage, const uint32_t* bm, int W, int c,
-                                           int vi) {
-  constexpr int EPV = ElemT<DT>::EPV, CE = ElemT<DT>::CE;
-  uint4 r = reinterpret_cast<const uint4*>(stage)[vi];
-  if (bm) {
-    const int e = c * CE + vi * EPV;
-    const int w = e >> 5;
-    const uint32_t lb = (w < W) ? (__ldg(bm + w) >> (e & 31)) & ((1u << EPV) - 1u) : 0u;
-    if (lb != (1u << EPV) - 1u) r = apply_mask<DT>(r, lb);
-  }
-  return r;
-}
 
 // ---------------------------------------------------------------------------
 // Argmax over the legal finite elements: (largest key, earliest id).
